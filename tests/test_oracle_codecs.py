@@ -1,0 +1,94 @@
+"""Pins for the oracle's number-format codecs against library casts and closed forms."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode_bf16, decode_e4m3, encode_e4m3, unpack_int4, decode_int4_grouped
+from synth.inputs import _pack_int4, _encode_expert
+
+
+def test_bf16_decode_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = decode_bf16(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+def test_e4m3_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    # closed forms from the format definition
+    assert decode_e4m3(np.array([0x7E]))[0] == 448.0
+    assert decode_e4m3(np.array([0x01]))[0] == 2.0 ** -9
+    assert decode_e4m3(np.array([0x08]))[0] == 2.0 ** -6
+    assert decode_e4m3(np.array([0x38]))[0] == 1.0
+    assert decode_e4m3(np.array([0xB8]))[0] == -1.0
+
+
+def _e4m3_probe_values():
+    finite = np.sort(np.unique(decode_e4m3(np.arange(256, dtype=np.uint8))))
+    finite = finite[np.isfinite(finite)]
+    mids = (finite[:-1] + finite[1:]) / 2.0
+    f32 = np.float32
+    vals = [finite, mids]
+    for m in (mids, finite):
+        m32 = m.astype(f32)
+        vals.append(np.nextafter(m32, f32(np.inf)).astype(np.float64))
+        vals.append(np.nextafter(m32, f32(-np.inf)).astype(np.float64))
+    rng = np.random.default_rng(0)
+    vals.append(rng.standard_normal(200_000) * 30.0)
+    vals.append(np.exp2(rng.uniform(-12, 9, 200_000)) * rng.choice([-1, 1], 200_000))
+    v = np.concatenate(vals).astype(np.float32)
+    return v[np.abs(v) < 464.0]
+
+
+def test_e4m3_encode_matches_torch_cast_in_range():
+    v = _e4m3_probe_values()
+    ours = encode_e4m3(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_saturates():
+    big = np.array([448.0, 463.9, 464.0, 470.0, 1e6, 3e38], dtype=np.float32)
+    assert np.all(decode_e4m3(encode_e4m3(big)) == 448.0)
+    assert np.all(decode_e4m3(encode_e4m3(-big)) == -448.0)
+    assert encode_e4m3(np.array([np.nan], dtype=np.float32))[0] & 0x7F == 0x7F
+
+
+def test_int4_unpack_closed_form_all_bytes():
+    b = np.arange(256, dtype=np.uint8)
+    q = unpack_int4(b[:, None])
+    lo = b & 0xF
+    hi = b >> 4
+    sext = lambda v: np.where(v >= 8, v.astype(np.int64) - 16, v.astype(np.int64))
+    assert np.array_equal(q[:, 0], sext(lo))
+    assert np.array_equal(q[:, 1], sext(hi))
+    assert q.min() == -8 and q.max() == 7
+
+
+def test_int4_pack_matches_unpack():
+    g = torch.Generator().manual_seed(3)
+    codes = torch.randint(-8, 8, (5, 64), generator=g, dtype=torch.int8)
+    packed = _pack_int4(codes).numpy()
+    assert np.array_equal(unpack_int4(packed), codes.numpy().astype(np.int64))
+
+
+def test_int4_grouped_decode_brute_force():
+    g = torch.Generator().manual_seed(4)
+    w = torch.randn((3, 256), generator=g) * 0.02
+    packed, s16 = _encode_expert(w, "int4", 128)
+    deq = decode_int4_grouped(packed.numpy(), s16.numpy(), 128)
+    q = unpack_int4(packed.numpy())
+    for r in range(3):
+        for k in range(256):
+            assert deq[r, k] == q[r, k] * float(s16[r, k // 128])
+    # symmetric quantisation error is at most half a step per element
+    step = np.repeat(s16.float().numpy(), 128, axis=1)
+    assert np.all(np.abs(deq - w.numpy()) <= step * 0.5 + 1e-12)
