@@ -1,0 +1,480 @@
+"""Benchmark of the fused MoE layer forward pass on GB300.
+
+One step = one moe_forward (gate, align/permute, gate_up+SwiGLU GEMM, down GEMM,
+unpermute+reduce) over one batch of T synthetic tokens with the Mixtral-8x7B
+layer shape (H=4096, I=14336, E=8, top_k=2, softmax renormalised, bf16
+weights ~N(0, 0.02)); default T = 4096.  Inputs are resident in HBM; the expert
+weights (2.8 GB) exceed L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+instead, on a bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s and achieved % of roofline (HBM or tensor) vs batch 1–4096"
+UNIT = "tokens/s"
+CONFIG_NAME = "mixtral"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+
+def layer_bytes_flops(shape, T, touched):
+    """Algorithmic bytes / flops of one forward (weights of touched experts,
+    x in, out, logits; 6*k*H*I flops per token)."""
+    from synth import SHAPES  # noqa
+    H, I, E, k = shape.H, shape.I, shape.E, shape.top_k
+    if shape.wdtype == "bf16":
+        wbytes = 3 * H * I * 2
+    elif shape.wdtype == "fp8":
+        wbytes = 3 * H * I + 8
+    else:
+        wbytes = 3 * H * I // 2 + 3 * H * I // shape.group_size * 2
+    B = touched * wbytes + T * H * 2 * 2 + T * E * 4
+    F = 6.0 * k * H * I * T
+    return B, F
+
+
+def run_ours(args):
+    import torch
+    import mixture_experts_layer_gate_gb300 as moe
+    from synth import SHAPES, T_SWEEP, make_tokens, make_weights
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local = _env_int("LOCAL_RANK", 0)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load()
+    shape = SHAPES[args.config]
+    T = args.T
+    hbm, bf16_peak, bf16_sust, peak_src = _peaks()
+
+    w = make_weights(shape, dev, seed=0)
+    tok = make_tokens(shape, T, dev, seed=rank)
+    p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
+                    renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
+                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype)
+    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+    ws = moe.alloc_workspace(p, dev)
+    out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    plan = moe.get_plan(p)
+
+    def fwd():
+        moe.forward(p, wts, tok.x, tok.logits, tok.bias, out, ws, stream.cuda_stream)
+
+    # capture one step in a CUDA graph (routing stays on the device)
+    with torch.cuda.stream(stream):
+        fwd()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            fwd()
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    stream.synchronize()
+    err = moe.get_device_error(ws, stream.cuda_stream)
+    if err != 0:
+        raise RuntimeError(f"device error {err}")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.05)
+    if dist is not None:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # routing facts for the roofline
+    counts = ws[0:0]  # placeholder keep-alive
+    ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
+    tw = torch.empty((T, shape.top_k), dtype=torch.float32, device=dev)
+    moe.gate_topk(p, tok.logits, tok.bias, ids, tw, stream.cuda_stream)
+    stream.synchronize()
+    touched = int(torch.unique(ids).numel())
+    B, F = layer_bytes_flops(shape, T, touched)
+    t_roof = max(B / (hbm * 1e9), F / (bf16_peak * 1e12))
+    layer_frac = t_roof / (ms / 1e3)
+
+    # dominant kernel: the gate_up grouped GEMM, timed alone on its stream
+    S = T * shape.top_k
+    counts_t = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(shape.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(S, dtype=torch.int32, device=dev)
+    inv = torch.empty(S, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((S, shape.H), dtype=torch.bfloat16, device=dev)
+    act = torch.empty((S, shape.I), dtype=torch.bfloat16, device=dev)
+    moe.align_permute(p, ids, tok.x, tok.a1_scale, counts_t, offsets, perm, inv, x_perm, ws, stream.cuda_stream)
+    for _ in range(3):
+        moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(5, args.steps)
+    g0.record(stream)
+    for _ in range(reps):
+        moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
+    g1.record(stream)
+    stream.synchronize()
+    k_ms = g0.elapsed_time(g1) / reps
+    up_flops = 2.0 * S * (2 * shape.I) * shape.H
+    up_bytes = touched * (2 * shape.I * shape.H * 2) + S * shape.H * 2 + S * shape.I * 2
+    t_tensor = up_flops / (bf16_peak * 1e12)
+    t_hbm = up_bytes / (hbm * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": up_flops / (k_ms / 1e3) / 1e12, "peak": bf16_peak,
+                "unit": "TFLOP/s", "peak_kind": f"bf16 dense burst, {peak_src}"}
+    else:
+        roof = {"bound": "hbm", "achieved": up_bytes / (k_ms / 1e3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "grouped_gemm_kernel<bf16> (gate_up + SwiGLU)"
+    roof["kernel_ms"] = k_ms
+    roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
+
+    # end to end through the public call with host buffers
+    x_h = tok.x.cpu().pin_memory()
+    l_h = tok.logits.cpu().pin_memory()
+    o_h = torch.empty((T, shape.H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(tok.x)
+    l_d = torch.empty_like(tok.logits)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_d.copy_(x_h, non_blocking=True)
+            l_d.copy_(l_h, non_blocking=True)
+            moe.forward(p, wts, x_d, l_d, tok.bias, out, ws, stream.cuda_stream)
+            o_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    e_ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+
+    launches_per_step = 7 + (plan.splits_up > 1) + (plan.splits_down > 1)
+
+    sweep = []
+    if args.sweep and rank == 0:
+        sweep = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "mixtral_8x7b_moe_layer", "T": T, "H": shape.H, "I": shape.I, "E": shape.E,
+                   "top_k": shape.top_k, "gate": "softmax top-2, renormalised", "weights": "bf16 N(0,0.02)",
+                   "global_batch": world * T, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "no flush: expert weights (2.8 GB) exceed L2 every step",
+                   "cuda_graph": True, "plan": {"bn_max": plan.bn_max_up, "splits_up": plan.splits_up,
+                                                "splits_down": plan.splits_down, "stages_up": plan.stages_up,
+                                                "sms": plan.num_sms}},
+        "layer_roofline": {"t_roof_us": t_roof * 1e6, "frac": layer_frac, "touched_experts": touched,
+                           "bytes": B, "flops": F},
+        "roofline": roof,
+        "e2e": {"value": world * T / (e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_h.numel() * 2 + l_h.numel() * 4),
+                "d2h_bytes_per_step": int(o_h.numel() * 2), "ms_per_step": e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if sweep:
+        line["sweep"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, w, tok, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak):
+    """Per-T tokens/s and roofline fraction of the whole layer (CUDA graph, 20 reps)."""
+    from synth import T_SWEEP, make_tokens
+    rows = []
+    for T in T_SWEEP:
+        tok = make_tokens(shape, T, dev, seed=0)
+        p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
+                        renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
+                        routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype)
+        wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+        ws = moe.alloc_workspace(p, dev)
+        out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            moe.forward(p, wts, tok.x, tok.logits, tok.bias, out, ws, stream.cuda_stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                moe.forward(p, wts, tok.x, tok.logits, tok.bias, out, ws, stream.cuda_stream)
+            for _ in range(3):
+                g.replay()
+        reps = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                g.replay()
+        b.record(stream)
+        stream.synchronize()
+        ms = a.elapsed_time(b) / reps
+        ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
+        tw = torch.empty((T, shape.top_k), dtype=torch.float32, device=dev)
+        moe.gate_topk(p, tok.logits, tok.bias, ids, tw, stream.cuda_stream)
+        stream.synchronize()
+        touched = int(torch.unique(ids).numel())
+        B, F = layer_bytes_flops(shape, T, touched)
+        tb, tf = B / (hbm * 1e9), F / (bf16_peak * 1e12)
+        rows.append({"T": T, "us": ms * 1e3, "tokens_s": T / (ms / 1e3), "tflops": F / (ms / 1e3) / 1e12,
+                     "gbs": B / (ms / 1e3) / 1e9, "bound": "hbm" if tb >= tf else "tensor",
+                     "roofline_frac": max(tb, tf) / (ms / 1e3), "touched": touched})
+        del g, ws
+    return rows
+
+
+def _traffic_for(kernel, config, T):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}_T{T}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_sha256") != _gemm_source_hash():
+            return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def _gemm_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "mixture_experts_layer_gate_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class _OracleRunner:
+    """fp64 CPU oracle on a bounded token sample, decoded experts cached."""
+
+    def __init__(self, shape, w, tok, sample):
+        import numpy as np
+        import oracle
+        self.np, self.oracle = np, oracle
+        from tests.oracle_io import np_of, bf16_bits
+        T = tok.x.shape[0]
+        n = min(sample, T)
+        rows = np.linspace(0, T - 1, n).astype(np.int64)
+        self.rows = rows
+        self.x_bits = bf16_bits(tok.x)[rows]
+        self.logits = np_of(tok.logits)[rows]
+        self.bias = np_of(tok.bias)
+        self.p = oracle.Problem(T=n, H=shape.H, I=shape.I, E=shape.E, top_k=shape.top_k, scoring=shape.scoring,
+                                renormalize=shape.renormalize, n_group=shape.n_group,
+                                topk_group=shape.topk_group, routed_scaling_factor=shape.routed_scaling_factor,
+                                wdtype=shape.wdtype, group_size=shape.group_size)
+        self.a1 = None if tok.a1_scale is None else float(tok.a1_scale.cpu()[0])
+        self.a2 = None if tok.a2_scale is None else float(tok.a2_scale.cpu()[0])
+        self.cache = {}
+        self._w = w
+        outer = self
+
+        class Cached(oracle.ExpertWeights):
+            def __call__(self_inner, e):
+                if e not in outer.cache:
+                    t0 = time.perf_counter()
+                    sub = oracle.ExpertWeights(outer.p, {e: np_of(w.w13[e])}, {e: np_of(w.w2[e])},
+                                               None if w.w13_scale is None else {e: np_of(w.w13_scale[e])},
+                                               None if w.w2_scale is None else {e: np_of(w.w2_scale[e])})
+                    outer.cache[e] = sub(e)
+                    self_inner.prep_seconds += time.perf_counter() - t0
+                return outer.cache[e]
+
+        self.experts = Cached(self.p, None, None)
+
+    def step(self):
+        st = {}
+        self.oracle.forward(self.p, self.x_bits, self.logits, self.bias, self.experts, self.a1, self.a2, stats=st)
+        return st["seconds"], len(self.rows)
+
+
+def cpu_baseline(shape, w, tok, sample):
+    r = _OracleRunner(shape, w, tok, sample)
+    r.step()  # decode the touched experts (excluded from timing)
+    secs, n = r.step()
+    return {"value": n / secs, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of the {tok.x.shape[0]} tokens (evenly spaced), fp64 numpy, expert decode excluded",
+            "seconds": secs}
+
+
+def run_reference(args):
+    rank = _env_int("RANK", 0)
+    if rank != 0:
+        return
+    import torch
+    from synth import SHAPES, make_tokens, make_weights
+    shape = SHAPES[args.config]
+    dev = torch.device("cuda", _env_int("LOCAL_RANK", 0)) if torch.cuda.is_available() else torch.device("cpu")
+    w = make_weights(shape, dev, seed=0)
+    tok = make_tokens(shape, args.T, dev, seed=0)
+    r = _OracleRunner(shape, w, tok, args.ref_sample)
+    for _ in range(args.warmup):
+        r.step()
+    total, n = 0.0, 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s, k = r.step()
+        total += s
+        n += k
+    wall = time.perf_counter() - t0
+    v = n / total
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "mixtral_8x7b_moe_layer", "T": args.T, "sample_tokens_per_step": len(r.rows)},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{len(r.rows)} of {args.T} tokens per step, fp64 numpy, expert decode excluded"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=CONFIG_NAME)
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=64)
+    ap.add_argument("--ref-sample", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * moe.h - C ABI of a fused Mixture-of-Experts layer forward pass for GB300
+ * (sm_103a).  One library, plain pointers and sizes, no framework types.
+ *
+ * The layer (prose of the pages; none prints a formula):
+ *   1. gate: router logits -> top-k expert ids and weights
+ *      ("Add deepseek_v3 fused gate", the fused gate and its PyTorch reference;
+ *       softmax top-k as in Mixtral on "Optimized fused MoE Kernel, take 2").
+ *   2. align + permute: group the T*k token slots by expert
+ *      ("[Kernel] add triton fused moe kernel for gptq/awq", note 1 on
+ *       moe_align_block_size; "Add deepseek_v3 fused gate", TensorRT-LLM's
+ *       expand_and_permute, which needs no padding).
+ *   3. grouped GEMMs per expert: gate_up, SiLU-and-mul, down
+ *      (Triton fused_moe on "Optimized fused MoE Kernel, take 2"; split-K on
+ *       "[kernel] introduce fused_moe_triton_splitk to sglang"; the FBGEMM
+ *       grouped GEMM blog; weight formats bf16, fp8 e4m3 per-tensor, int4
+ *       group-128 from those pages).
+ *   4. unpermute + top-k weighted reduction ("Add deepseek_v3 fused gate",
+ *      TensorRT-LLM's unpermute_and_reduce).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers, row-major, 16-byte aligned,
+ *     owned by the caller.  The library allocates nothing and keeps no state
+ *     between calls other than per-device constants (SM count, driver entry
+ *     point) looked up on first use.
+ *   - Every call is asynchronous and stream-ordered on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).  No call synchronises with
+ *     the host except moe_get_device_error.  Calls can be captured in a CUDA
+ *     graph.
+ *   - Argument errors are reported synchronously by the return value and
+ *     nothing is launched.  Data-dependent errors found by the kernels (an
+ *     expert id outside [0, E), a pipeline wait that ran out) are recorded in
+ *     a sticky error word at the start of the workspace and read with
+ *     moe_get_device_error; the kernels then finish their bounded work with
+ *     memory-safe (but meaningless) results.
+ *   - A workspace `ws` of at least moe_scratch_size() bytes (stage calls) or
+ *     moe_workspace_size() bytes (moe_forward) is passed to the calls that
+ *     need one.  Its first 256 bytes are the error header and must be zero
+ *     when the workspace is first used (allocate it zeroed once).
+ *
+ * Shapes: T tokens, H hidden, I intermediate per expert, E experts, k = top_k,
+ * S = T*k slots.  Requirements: H % 128 == 0, I % 128 == 0, 1 <= k <= E <= 1024,
+ * T >= 0; grouped gating needs n_group <= 32, E % n_group == 0,
+ * 1 <= topk_group <= n_group and k <= topk_group * E / n_group.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* bad shape, null or misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. E > 1024) */
+  MOE_ERR_WORKSPACE = 3,        /* workspace missing or too small */
+  MOE_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_BAD_INDEX = 5, /* a kernel saw an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 6           /* a kernel pipeline wait ran out (about 1 s) */
+} moe_status_t;
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_INT4_G128 = 2 } moe_wdtype_t;
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+
+/* Problem description.  Enum-valued fields are stored as int32_t so the
+ * struct layout is fixed: 12 four-byte fields, no padding. */
+typedef struct {
+  int32_t T, H, I, E, top_k;
+  int32_t scoring;               /* moe_score_t */
+  int32_t renormalize;           /* 1: divide the k selected scores by their sum */
+  int32_t n_group, topk_group;   /* 0, 0 = ungrouped selection */
+  float routed_scaling_factor;   /* multiplies the final weights (1.0f = none) */
+  int32_t wdtype;                /* moe_wdtype_t */
+  int32_t group_size;            /* int4 only: must be 128 */
+} moe_problem_t;
+
+/* Expert weights (device pointers).
+ *   bf16 : w13 bf16 [E, 2I, H], w2 bf16 [E, H, I]; scales NULL.
+ *   fp8  : w13 uint8 e4m3 [E, 2I, H], w2 uint8 e4m3 [E, H, I];
+ *          w13_scale, w2_scale float [E] (value = e4m3(code) * scale[e]);
+ *          a1_scale, a2_scale: float [1] static activation scales for the
+ *          token rows entering gate_up and the activation entering down.
+ *   int4 : w13 uint8 [E, 2I, H/2], w2 uint8 [E, H, I/2], two signed
+ *          two's-complement codes per byte, the low nibble holding the even K
+ *          index; w13_scale half [E, 2I, H/128], w2_scale half [E, H, I/128]
+ *          (value = code * scale, symmetric, no zero point).
+ * In w13, rows [0, I) are the gate projection (SiLU applied) and rows
+ * [I, 2I) the up projection. */
+typedef struct {
+  const void* w13;
+  const void* w2;
+  const void* w13_scale;
+  const void* w2_scale;
+  const float* a1_scale;
+  const float* a2_scale;
+} moe_weights_t;
+
+/* Bytes of workspace the stage calls need (error header, align scratch,
+ * split-K partial sums).  Depends only on the problem.  Returns 0 for an
+ * invalid problem. */
+size_t moe_scratch_size(const moe_problem_t* p);
+
+/* Bytes of workspace moe_forward needs: moe_scratch_size() plus every
+ * intermediate (ids, weights, counts, offsets, perm, inv, x_perm, act,
+ * y_perm).  Returns 0 for an invalid problem. */
+size_t moe_workspace_size(const moe_problem_t* p);
+
+/* Stage 1: top-k gate ("Add deepseek_v3 fused gate"; reading of the
+ * selection rule below, the pages name the gate but print no formula).
+ *   logits   float [T, E]
+ *   bias     float [E] or NULL (sigmoid only; steers selection, not weights)
+ *   topk_ids int32 [T, k]  out: ids ordered by selection key, descending,
+ *                           equal keys to the lower expert index
+ *   topk_w   float [T, k]  out
+ * Softmax: key = logit; weight = softmax probability over all E, divided by
+ * the sum of the k selected if renormalize, times routed_scaling_factor.
+ * Sigmoid: s = sigmoid(logit); key = s + bias (raw logit when ungrouped and
+ * bias is NULL); with n_group > 0 the experts form n_group contiguous groups,
+ * each scored by the sum of its two largest keys, and only the topk_group best
+ * groups (ties to the lower group) compete; weight = s, renormalised if asked,
+ * times routed_scaling_factor.  NaN logits rank lowest. */
+moe_status_t moe_gate_topk(const moe_problem_t* p, const float* logits, const float* bias,
+                           int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* Stage 2: align and permute ("[Kernel] add triton fused moe kernel for
+ * gptq/awq", note 1, moe_align_block_size; "Add deepseek_v3 fused gate",
+ * expand_and_permute).  A stable counting sort of the flat slots f = t*k + j.
+ *   topk_ids int32 [T, k]
+ *   x        bf16 [T, H] token rows
+ *   a1_scale float [1] (fp8 only, else ignored/NULL)
+ *   counts   int32 [E]      out: slots per expert
+ *   offsets  int32 [E + 1]  out: exclusive prefix sum, offsets[E] = S
+ *   perm     int32 [S]      out: row -> slot; the r-th slot (ascending f)
+ *                                routed to e is row offsets[e] + r
+ *   inv      int32 [S]      out: slot -> row
+ *   x_perm   [S, H]         out: x[perm[r] / k]; bf16, or for fp8 the e4m3
+ *                                code of x / a1 (float32 division, round to
+ *                                nearest even, saturating at 448)
+ * Ids outside [0, E) set MOE_ERR_DEVICE_BAD_INDEX and are treated as 0. */
+moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, const void* x,
+                               const float* a1_scale, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv, void* x_perm, void* ws,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* Padded view of the sorted slots for a GEMM row block of `block` rows (the
+ * layout moe_align_block_size produces, "[Kernel] add triton fused moe kernel
+ * for gptq/awq", note 1).  Each expert's segment is padded up to a multiple of
+ * `block` with the sentinel S.
+ *   offsets      int32 [E + 1], perm int32 [S]   (from moe_align_permute)
+ *   sorted_ids   int32 [moe_padded_capacity(p, block)]             out
+ *   block_expert int32 [moe_padded_capacity(p, block) / block]    out
+ *   total_padded int32 [1]                                         out
+ * Entries past total_padded are left untouched.  1 <= block <= 1024. */
+moe_status_t moe_align_block_size(const moe_problem_t* p, const int32_t* offsets,
+                                  const int32_t* perm, int32_t block, int32_t* sorted_ids,
+                                  int32_t* block_expert, int32_t* total_padded,
+                                  moe_stream_t stream);
+
+/* Upper bound on total_padded: S + E * (block - 1), rounded up to a multiple
+ * of block. */
+size_t moe_padded_capacity(const moe_problem_t* p, int32_t block);
+
+/* Stage 3a: grouped gate_up GEMM with SiLU-and-mul fused into its epilogue.
+ * For every expert e and row r in [offsets[e], offsets[e+1]):
+ *   h = W13[e] x_perm[r]  (fp32 accumulation; fp8: times a1 * w13_scale[e];
+ *                          int4: codes times group scales, rounded to bf16)
+ *   act[r, i] = silu(h[i]) * h[I + i],  silu(z) = z / (1 + exp(-z))
+ * act is bf16 [S, I], or for fp8 the e4m3 code of act / a2.
+ * Uses ws for split-K partial sums when the expert row counts are small. */
+moe_status_t moe_grouped_gemm_swiglu(const moe_problem_t* p, const moe_weights_t* w,
+                                     const void* x_perm, const int32_t* offsets, void* act,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Stage 3b: grouped down GEMM: y_perm[r] = W2[e] act[r] for rows of expert e
+ * (fp8: times a2 * w2_scale[e]).  y_perm is bf16 [S, H].  Small row counts
+ * split K across CTAs into fp32 partials in ws, summed in a fixed order
+ * (no atomics; the result does not depend on scheduling). */
+moe_status_t moe_grouped_gemm_down(const moe_problem_t* p, const moe_weights_t* w,
+                                   const void* act, const int32_t* offsets, void* y_perm,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Stage 4: unpermute and reduce ("Add deepseek_v3 fused gate",
+ * unpermute_and_reduce):
+ *   out[t] = sum_{j=0..k-1} topk_w[t, j] * y_perm[inv[t*k + j]]
+ * accumulated in fp32 in j order (deterministic), stored bf16 [T, H]. */
+moe_status_t moe_unpermute_reduce(const moe_problem_t* p, const void* y_perm, const int32_t* inv,
+                                  const float* topk_w, void* out, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* The whole layer: gate, align/permute, gate_up+SwiGLU, down, unpermute and
+ * reduce, all on `stream`, intermediates in ws (moe_workspace_size bytes).
+ *   x bf16 [T, H], logits float [T, E], bias float [E] or NULL, out bf16 [T, H]. */
+moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const void* x,
+                         const float* logits, const float* bias, void* out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, returns the sticky device error recorded in ws (MOE_OK
+ * if none) and clears it.  Debug/test use: it is the only blocking call. */
+moe_status_t moe_get_device_error(void* ws, moe_stream_t stream);
+
+/* Static, human-readable name of a status. */
+const char* moe_status_string(moe_status_t s);
+
+/* Tile choices the library makes for a problem (for tests and benchmarks):
+ * token tile limit and split-K factor of the two GEMMs on the current device. */
+typedef struct {
+  int32_t bn_max_up, splits_up, stages_up;
+  int32_t bn_max_down, splits_down, stages_down;
+  int32_t num_sms;
+} moe_plan_t;
+moe_status_t moe_get_plan(const moe_problem_t* p, moe_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

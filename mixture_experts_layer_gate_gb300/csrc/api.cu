@@ -1,0 +1,563 @@
+// Host side of the C ABI declared in include/moe.h: argument validation,
+// workspace layout, launch planning (token tile, split-K, pipeline depth),
+// TMA descriptor encoding and the stage launches.  No call here synchronises
+// with the host except moe_get_device_error.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxSplits = 16;
+constexpr int kMaxStages = 8;
+constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
+constexpr size_t kMaxDynSmem = 232448;
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int roundup16(int x) { return (x + 15) & ~15; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t validate_problem(const moe_problem_t* p) {
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->H % 128 != 0 || p->I % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (p->top_k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->E > kMaxE || p->top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (p->T > 65535) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(p->T) * p->top_k > (1ll << 24)) return MOE_ERR_UNSUPPORTED;
+  if (p->scoring != MOE_SCORE_SOFTMAX && p->scoring != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (p->renormalize != 0 && p->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(p->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  if (p->n_group < 0 || p->topk_group < 0) return MOE_ERR_INVALID_ARG;
+  if (p->n_group > 0) {
+    if (p->scoring != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if (p->n_group > 32 || p->E % p->n_group != 0) return MOE_ERR_INVALID_ARG;
+    if (p->topk_group < 1 || p->topk_group > p->n_group) return MOE_ERR_INVALID_ARG;
+    if (p->top_k > p->topk_group * (p->E / p->n_group)) return MOE_ERR_INVALID_ARG;
+  } else if (p->topk_group != 0) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (p->wdtype != MOE_W_BF16 && p->wdtype != MOE_W_FP8_E4M3 && p->wdtype != MOE_W_INT4_G128)
+    return MOE_ERR_INVALID_ARG;
+  if (p->wdtype == MOE_W_INT4_G128 && p->group_size != 128) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------ device facts
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ok = false;
+};
+
+cudaError_t device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].ok) {
+    int sms = 0;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    cache[dev].sms = sms;
+    cache[dev].ok = true;
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr,
+                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr),
+                  reinterpret_cast<const cuuint64_t*>(dims),
+                  reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                  reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- planning
+
+struct GemmPlan {
+  int bn_max, P, stages, FB, KB;
+  size_t smem;
+};
+
+int wkind_of(const moe_problem_t& p) {
+  return p.wdtype == MOE_W_FP8_E4M3 ? kW_FP8 : (p.wdtype == MOE_W_INT4_G128 ? kW_INT4 : kW_BF16);
+}
+
+// Token tile limit: generous enough that one tile usually holds all of an
+// expert's tokens (each extra token block re-reads the expert's weights).
+int plan_bn_max(const moe_problem_t& p) {
+  const long long S = static_cast<long long>(p.T) * p.top_k;
+  if (S <= 0) return 16;
+  const long long touched = std::max(1ll, std::min<long long>(p.E, S));
+  const long long m_avg = (S + touched - 1) / touched;
+  long long bn = std::max(3 * m_avg, m_avg + 24);
+  bn = std::min<long long>(256, std::max<long long>(16, bn));
+  return roundup16(static_cast<int>(bn));
+}
+
+long long plan_tiles(const moe_problem_t& p, bool up, int bn_max) {
+  const long long S = static_cast<long long>(p.T) * p.top_k;
+  const long long touched = std::max(1ll, std::min<long long>(p.E, S));
+  const long long m_avg = (S + touched - 1) / touched;
+  const int FB = up ? p.I / 64 : p.H / 128;
+  return touched * ((m_avg + bn_max - 1) / bn_max) * FB;
+}
+
+int plan_splits(const moe_problem_t& p, bool up, int bn_max, int KB, int sms) {
+  const long long tiles = plan_tiles(p, up, bn_max);
+  if (tiles >= 4ll * sms) return 1;
+  const int pmax = std::max(1, std::min(kMaxSplits, KB / 4));
+  int best = 1;
+  double best_eff = 0.0;
+  for (int P = 1; P <= pmax; ++P) {
+    const long long units = tiles * P;
+    const long long waves = (units + sms - 1) / sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+    if (eff >= 0.9) return P;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = P;
+    }
+  }
+  return best;
+}
+
+GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
+  GemmPlan g;
+  const int wk = wkind_of(p);
+  g.bn_max = plan_bn_max(p);
+  g.FB = up ? p.I / 64 : p.H / 128;
+  const int K = up ? p.H : p.I;
+  g.KB = K / (wk == kW_FP8 ? 128 : 64);
+  g.P = plan_splits(p, up, g.bn_max, g.KB, std::min(sms, kSmsForSizing));
+  const size_t per_stage =
+      16384 + static_cast<size_t>(g.bn_max) * 128 + (wk == kW_INT4 ? 4096 : 0) + 24;
+  const size_t fixed = gemm_smem_bytes(wk, g.bn_max, 0, p.E);
+  g.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - fixed) / per_stage));
+  while (g.stages > 2 && gemm_smem_bytes(wk, g.bn_max, g.stages, p.E) > kMaxDynSmem) --g.stages;
+  g.smem = gemm_smem_bytes(wk, g.bn_max, g.stages, p.E);
+  return g;
+}
+
+// ---------------------------------------------------------- workspace layout
+
+struct Layout {
+  size_t hdr, align_counts, partial, scratch_end;
+  size_t ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, total;
+};
+
+size_t partial_bytes(const moe_problem_t& p, bool up) {
+  const int bn = plan_bn_max(p);
+  const long long tiles = plan_tiles(p, up, bn);
+  if (tiles >= 4ll * kSmsForSizing) return 0;
+  const size_t S = static_cast<size_t>(p.T) * p.top_k;
+  const size_t N = up ? 2 * static_cast<size_t>(p.I) : static_cast<size_t>(p.H);
+  return static_cast<size_t>(kMaxSplits) * S * N * sizeof(float);
+}
+
+Layout layout_of(const moe_problem_t& p) {
+  Layout L;
+  const size_t S = static_cast<size_t>(p.T) * p.top_k;
+  const size_t esz = (p.wdtype == MOE_W_FP8_E4M3) ? 1 : 2;
+  size_t o = 0;
+  L.hdr = o;
+  o += kHeaderBytes;
+  L.align_counts = o;
+  o = align256(o + static_cast<size_t>(std::max(1, align_blocks(static_cast<int>(S)))) * p.E * 4);
+  L.partial = o;
+  o = align256(o + std::max(partial_bytes(p, true), partial_bytes(p, false)));
+  L.scratch_end = o;
+  L.ids = o;
+  o = align256(o + S * 4);
+  L.w = o;
+  o = align256(o + S * 4);
+  L.counts = o;
+  o = align256(o + static_cast<size_t>(p.E) * 4);
+  L.offsets = o;
+  o = align256(o + static_cast<size_t>(p.E + 1) * 4);
+  L.perm = o;
+  o = align256(o + S * 4);
+  L.inv = o;
+  o = align256(o + S * 4);
+  L.x_perm = o;
+  o = align256(o + S * p.H * esz);
+  L.act = o;
+  o = align256(o + S * p.I * esz);
+  L.y_perm = o;
+  o = align256(o + S * p.H * 2);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ----------------------------------------------------------------- stages
+
+moe_status_t run_gate(const moe_problem_t& p, const float* logits, const float* bias, int32_t* ids,
+                      float* w, cudaStream_t s) {
+  GateArgs a;
+  a.logits = logits;
+  a.bias = (p.scoring == MOE_SCORE_SIGMOID) ? bias : nullptr;
+  a.ids = ids;
+  a.w = w;
+  a.T = p.T;
+  a.E = p.E;
+  a.k = p.top_k;
+  a.sigmoid = p.scoring == MOE_SCORE_SIGMOID;
+  a.renormalize = p.renormalize;
+  a.n_group = p.n_group;
+  a.topk_group = p.topk_group;
+  a.scale = p.routed_scaling_factor;
+  return cuda_status(launch_gate(a, s));
+}
+
+moe_status_t run_align(const moe_problem_t& p, const int32_t* ids, const void* x, const float* a1,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       void* x_perm, void* ws, cudaStream_t s) {
+  const Layout L = layout_of(p);
+  AlignArgs a;
+  a.ids = ids;
+  a.S = p.T * p.top_k;
+  a.E = p.E;
+  a.k = p.top_k;
+  a.H = p.H;
+  a.block_counts = at<int32_t>(ws, L.align_counts);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.inv = inv;
+  a.x = x;
+  a.x_perm = x_perm;
+  a.a1 = a1;
+  a.fp8 = p.wdtype == MOE_W_FP8_E4M3;
+  a.err = at<uint32_t>(ws, L.hdr);
+  return cuda_status(launch_align(a, s));
+}
+
+moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, const void* in,
+                      const int32_t* offsets, void* out, void* ws, cudaStream_t s) {
+  const int S = p.T * p.top_k;
+  if (S == 0) return MOE_OK;
+  DeviceInfo di;
+  if (device_info(&di) != cudaSuccess) return MOE_ERR_CUDA;
+  const GemmPlan g = plan_gemm(p, up, di.sms);
+  const Layout L = layout_of(p);
+  const int wk = wkind_of(p);
+  const uint64_t E = p.E, H = p.H, I = p.I;
+
+  GemmMaps maps;
+  // A: expert weights.
+  bool ok;
+  if (up) {
+    // [E][2][I/16][16][K] viewed as dims (K, 16, 2, I/16, E): one box = 4 blocks
+    // of 16 rows of gate followed by the 16 matching rows of up.
+    const uint64_t Kb = (wk == kW_INT4) ? H / 2 : (wk == kW_FP8 ? H : H * 2);  // bytes per row
+    const uint64_t dimK = (wk == kW_BF16) ? H : Kb;
+    uint64_t dims[5] = {dimK, 16, 2, I / 16, E};
+    uint64_t str[4] = {Kb, I * Kb, 16 * Kb, 2 * I * Kb};
+    uint32_t box[5] = {wk == kW_INT4 ? 32u : (wk == kW_FP8 ? 128u : 64u), 16, 2, 4, 1};
+    ok = encode_map(&maps.a, wk == kW_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                    5, wt.w13, dims, str, box,
+                    wk == kW_INT4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    const uint64_t Kb = (wk == kW_INT4) ? I / 2 : (wk == kW_FP8 ? I : I * 2);
+    const uint64_t dimK = (wk == kW_BF16) ? I : Kb;
+    uint64_t dims[3] = {dimK, H, E};
+    uint64_t str[2] = {Kb, H * Kb};
+    uint32_t box[3] = {wk == kW_INT4 ? 32u : (wk == kW_FP8 ? 128u : 64u), 128, 1};
+    ok = encode_map(&maps.a, wk == kW_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                    3, wt.w2, dims, str, box,
+                    wk == kW_INT4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return MOE_ERR_CUDA;
+  {
+    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path).
+    const uint64_t K = up ? H : I;
+    const bool f8 = wk == kW_FP8;
+    uint64_t dims[2] = {K, static_cast<uint64_t>(S)};
+    uint64_t str[1] = {K * (f8 ? 1 : 2)};
+    uint32_t box[2] = {f8 ? 128u : 64u, 16};
+    if (!encode_map(&maps.b, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+
+  GemmParams gp;
+  gp.offsets = offsets;
+  gp.err = at<uint32_t>(ws, L.hdr);
+  gp.a_scale = up ? wt.a1_scale : wt.a2_scale;
+  gp.w_scale = static_cast<const float*>(up ? wt.w13_scale : wt.w2_scale);
+  gp.q_scale = wt.a2_scale;
+  gp.w4_scale = up ? wt.w13_scale : wt.w2_scale;
+  gp.E = p.E;
+  gp.S = S;
+  gp.I = p.I;
+  gp.FB = g.FB;
+  gp.KB = g.KB;
+  gp.P = g.P;
+  gp.bn_max = g.bn_max;
+  gp.stages = g.stages;
+  gp.is_up = up ? 1 : 0;
+  gp.R = up ? 2 * p.I : p.H;
+  gp.G = up ? p.H / 128 : p.I / 128;
+  float* part = at<float>(ws, L.partial);
+  if (g.P == 1) {
+    gp.epi = up ? kEpiSwiglu : kEpiStore;
+    gp.out = out;
+    gp.out_ld = up ? p.I : p.H;
+    gp.part_stride = 0;
+  } else {
+    gp.epi = kEpiPartial;
+    gp.out = part;
+    gp.out_ld = up ? 2 * static_cast<int64_t>(p.I) : p.H;
+    gp.part_stride = static_cast<int64_t>(S) * gp.out_ld;
+  }
+  cudaError_t err = launch_grouped_gemm(wk, maps, gp, di.sms, g.smem, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (g.P > 1) {
+    if (up)
+      err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8, out, s);
+    else
+      err = launch_down_finish(part, g.P, gp.part_stride, S, p.H, out, s);
+  }
+  return cuda_status(err);
+}
+
+moe_status_t check_weights(const moe_problem_t& p, const moe_weights_t* w) {
+  if (w == nullptr || w->w13 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w->w13, 16) || !aligned(w->w2, 16)) return MOE_ERR_INVALID_ARG;
+  if (p.wdtype == MOE_W_FP8_E4M3) {
+    if (!w->w13_scale || !w->w2_scale || !w->a1_scale || !w->a2_scale) return MOE_ERR_INVALID_ARG;
+  }
+  if (p.wdtype == MOE_W_INT4_G128) {
+    if (!w->w13_scale || !w->w2_scale || !aligned(w->w13_scale, 2) || !aligned(w->w2_scale, 2))
+      return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_problem_t& p, void* ws, size_t ws_bytes, bool full) {
+  if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+  const Layout L = layout_of(p);
+  if (ws_bytes < (full ? L.total : L.scratch_end)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define MOE_TRY(x)                       \
+  do {                                   \
+    const moe_status_t st__ = (x);       \
+    if (st__ != MOE_OK) return st__;     \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_scratch_size(const moe_problem_t* p) {
+  if (validate_problem(p) != MOE_OK) return 0;
+  return layout_of(*p).scratch_end;
+}
+
+size_t moe_workspace_size(const moe_problem_t* p) {
+  if (validate_problem(p) != MOE_OK) return 0;
+  return layout_of(*p).total;
+}
+
+size_t moe_padded_capacity(const moe_problem_t* p, int32_t block) {
+  if (validate_problem(p) != MOE_OK || block < 1) return 0;
+  const size_t S = static_cast<size_t>(p->T) * p->top_k;
+  const size_t cap = S + static_cast<size_t>(p->E) * (block - 1);
+  return (cap + block - 1) / block * block;
+}
+
+moe_status_t moe_gate_topk(const moe_problem_t* p, const float* logits, const float* bias,
+                           int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  if (p->T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w || !aligned(logits, 4) || !aligned(topk_ids, 4) ||
+      !aligned(topk_w, 4) || (bias && !aligned(bias, 4)))
+    return MOE_ERR_INVALID_ARG;
+  return run_gate(*p, logits, bias, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, const void* x,
+                               const float* a1_scale, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv, void* x_perm, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  MOE_TRY(check_ws(*p, ws, ws_bytes, false));
+  if (!counts || !offsets || !aligned(counts, 4) || !aligned(offsets, 4)) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0) {
+    if (!topk_ids || !x || !perm || !inv || !x_perm || !aligned(x, 16) || !aligned(x_perm, 16) ||
+        !aligned(perm, 4) || !aligned(inv, 4) || !aligned(topk_ids, 4))
+      return MOE_ERR_INVALID_ARG;
+    if (p->wdtype == MOE_W_FP8_E4M3 && !a1_scale) return MOE_ERR_INVALID_ARG;
+  }
+  return run_align(*p, topk_ids, x, a1_scale, counts, offsets, perm, inv, x_perm, ws,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_align_block_size(const moe_problem_t* p, const int32_t* offsets,
+                                  const int32_t* perm, int32_t block, int32_t* sorted_ids,
+                                  int32_t* block_expert, int32_t* total_padded,
+                                  moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  if (block < 1 || block > 1024) return MOE_ERR_INVALID_ARG;
+  if (!offsets || !total_padded || !sorted_ids || !block_expert) return MOE_ERR_INVALID_ARG;
+  if (p->T > 0 && !perm) return MOE_ERR_INVALID_ARG;
+  const size_t cap = moe_padded_capacity(p, block);
+  return cuda_status(launch_align_block_size(offsets, perm, p->E, p->T * p->top_k, block, cap,
+                                             sorted_ids, block_expert, total_padded,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_gemm_swiglu(const moe_problem_t* p, const moe_weights_t* w,
+                                     const void* x_perm, const int32_t* offsets, void* act,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  MOE_TRY(check_weights(*p, w));
+  MOE_TRY(check_ws(*p, ws, ws_bytes, false));
+  if (p->T == 0) return MOE_OK;
+  if (!x_perm || !offsets || !act || !aligned(x_perm, 16) || !aligned(act, 16) || !aligned(offsets, 4))
+    return MOE_ERR_INVALID_ARG;
+  return run_gemm(*p, *w, true, x_perm, offsets, act, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_gemm_down(const moe_problem_t* p, const moe_weights_t* w,
+                                   const void* act, const int32_t* offsets, void* y_perm,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  MOE_TRY(check_weights(*p, w));
+  MOE_TRY(check_ws(*p, ws, ws_bytes, false));
+  if (p->T == 0) return MOE_OK;
+  if (!act || !offsets || !y_perm || !aligned(act, 16) || !aligned(y_perm, 16) || !aligned(offsets, 4))
+    return MOE_ERR_INVALID_ARG;
+  return run_gemm(*p, *w, false, act, offsets, y_perm, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_unpermute_reduce(const moe_problem_t* p, const void* y_perm, const int32_t* inv,
+                                  const float* topk_w, void* out, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  MOE_TRY(check_ws(*p, ws, ws_bytes, false));
+  if (p->T == 0) return MOE_OK;
+  if (!y_perm || !inv || !topk_w || !out || !aligned(y_perm, 16) || !aligned(out, 16) ||
+      !aligned(inv, 4) || !aligned(topk_w, 4))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_unpermute_reduce(y_perm, inv, topk_w, p->T, p->H, p->top_k, out,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const void* x,
+                         const float* logits, const float* bias, void* out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate_problem(p));
+  MOE_TRY(check_weights(*p, w));
+  MOE_TRY(check_ws(*p, ws, ws_bytes, true));
+  if (p->T == 0) return MOE_OK;
+  if (!x || !logits || !out || !aligned(x, 16) || !aligned(out, 16) || !aligned(logits, 4) ||
+      (bias && !aligned(bias, 4)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Layout L = layout_of(*p);
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* tw = at<float>(ws, L.w);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* inv = at<int32_t>(ws, L.inv);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* act = at<void>(ws, L.act);
+  void* y_perm = at<void>(ws, L.y_perm);
+  MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
+  MOE_TRY(run_align(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws, s));
+  MOE_TRY(run_gemm(*p, *w, true, x_perm, offsets, act, ws, s));
+  MOE_TRY(run_gemm(*p, *w, false, act, offsets, y_perm, ws, s));
+  return cuda_status(launch_unpermute_reduce(y_perm, inv, tw, p->T, p->H, p->top_k, out, s));
+}
+
+moe_status_t moe_get_device_error(void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h[0] != 0) {
+    if (cudaMemsetAsync(ws, 0, sizeof(h), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(h[0]);
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported problem";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE_BAD_INDEX: return "expert id outside [0, E) seen on the device";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+moe_status_t moe_get_plan(const moe_problem_t* p, moe_plan_t* plan) {
+  MOE_TRY(validate_problem(p));
+  if (plan == nullptr) return MOE_ERR_INVALID_ARG;
+  DeviceInfo di;
+  if (device_info(&di) != cudaSuccess) return MOE_ERR_CUDA;
+  const GemmPlan u = plan_gemm(*p, true, di.sms);
+  const GemmPlan d = plan_gemm(*p, false, di.sms);
+  plan->bn_max_up = u.bn_max;
+  plan->splits_up = u.P;
+  plan->stages_up = u.stages;
+  plan->bn_max_down = d.bn_max;
+  plan->splits_down = d.P;
+  plan->stages_down = d.stages;
+  plan->num_sms = di.sms;
+  return MOE_OK;
+}
+
+}  // extern "C"

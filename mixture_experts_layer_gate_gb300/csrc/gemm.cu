@@ -1,0 +1,492 @@
+// Stage 3: persistent grouped GEMMs on the 5th-generation tensor cores.
+//
+// Prior art on the pages: Triton fused_moe tuned per batch size ("Optimized
+// fused MoE Kernel, take 2"), split-K ("[kernel] introduce fused_moe_triton_
+// splitk to sglang"), a persistent TMA grouped GEMM (FBGEMM grouped-GEMM blog),
+// int4 dequantisation inside one launch instead of one launch per expert
+// ("[Kernel] add triton fused moe kernel for gptq/awq") and TensorRT-LLM's
+// grouped GEMM without padding ("Add deepseek_v3 fused gate").
+//
+// Design for sm_103a:
+//   * Weights are the MMA's A operand (M = 128 weight rows) and the expert's
+//     token rows are B (N = 16..256 tokens, sized per tile to the tokens the
+//     expert actually has), so a decode step with 1..32 tokens per expert does
+//     not pad to 128 tokens.  D = A * B^T lands in tensor memory (TMEM).
+//   * One CTA per SM loops over work units (expert, 128-row weight block, token
+//     block, K slice).  Units are derived on the device from the expert row
+//     offsets, so no host synchronisation is needed and empty experts cost
+//     nothing.
+//   * Warp roles: warp 0 issues TMA loads into a ring of shared-memory stages,
+//     warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5 drain
+//     the double-buffered accumulator (tcgen05.ld) and run the epilogue while
+//     the next unit accumulates.  For int4 weights warps 6..9 turn packed codes
+//     plus fp16 group scales into bf16 tiles in the 128-byte-swizzled layout
+//     the MMA reads.
+//   * gate_up: the A tile holds 64 gate rows and the 64 matching up rows,
+//     interleaved in blocks of 16 (one 5-D TMA box), so SiLU(gate) * up pairs
+//     lanes l and l + 16 of the same warp in the epilogue.
+//   * Small token counts split K into P slices that write fp32 partial sums;
+//     a separate pass adds them in slice order (no atomics).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kABytes = 16384;   // 128 rows x 128 B
+constexpr int kRawBytes = 4096;  // 128 rows x 32 B of packed int4
+constexpr int kStgBytesPerWarp = 2048;
+constexpr int kStgBytes = 4 * kStgBytesPerWarp;
+constexpr uint32_t kAccCols = 256;
+constexpr uint32_t kTmemCols = 512;
+
+struct SmemLayout {
+  uint32_t a, b, raw, stg, bars, misc, tiles, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages, int E) {
+  SmemLayout L;
+  uint32_t o = 0;
+  L.a = o;
+  o += stages * kABytes;
+  L.b = o;
+  o += stages * bn_max * 128;  // bn_max % 16 == 0 keeps 2 KB granularity
+  L.raw = o;
+  if (wk == kW_INT4) o += stages * kRawBytes;
+  L.stg = o;
+  o += kStgBytes;
+  L.bars = o;
+  o += (3 * stages + 5) * 8;
+  o = (o + 15u) & ~15u;
+  L.misc = o;
+  o += 16;
+  L.tiles = o;
+  o += 2 * (E + 1) * 4;
+  L.total = o + 1024;  // slack to align the dynamic base to 1024 B
+  return L;
+}
+
+struct Unit {
+  int e, fb, row0, nvalid, n, kb0, kb1, sp;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const int* off,
+                                            const GemmParams& p) {
+  Unit t;
+  const int tile = u / p.P;
+  t.sp = u - tile * p.P;
+  int lo = 0, hi = p.E;  // largest e with tile_base[e] <= tile
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_base[mid] <= tile) lo = mid; else hi = mid;
+  }
+  t.e = lo;
+  const int cnt = off[lo + 1] - off[lo];
+  const int nb = (cnt + p.bn_max - 1) / p.bn_max;
+  const int local = tile - tile_base[lo];
+  t.fb = local / nb;
+  const int tb = local - t.fb * nb;
+  t.row0 = off[lo] + tb * p.bn_max;
+  t.nvalid = min(p.bn_max, cnt - tb * p.bn_max);
+  t.n = (t.nvalid + 15) & ~15;
+  t.kb0 = static_cast<int>((static_cast<long long>(t.sp) * p.KB) / p.P);
+  t.kb1 = static_cast<int>((static_cast<long long>(t.sp + 1) * p.KB) / p.P);
+  return t;
+}
+
+// 8 packed int4 codes (low nibble first, two's complement) times a bf16 scale
+// -> 8 bf16.  0x4300 | v is the bf16 value 128 + v for v < 128; XOR 8 turns a
+// two's-complement nibble n into n + 8, so each half holds 136 + n exactly and
+// subtracting 136 recovers n before the scale multiply.
+__device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
+  x ^= 0x88888888u;
+  const uint32_t p04 = (x & 0x000F000Fu) | 0x43004300u;
+  const uint32_t p15 = ((x >> 4) & 0x000F000Fu) | 0x43004300u;
+  const uint32_t p26 = ((x >> 8) & 0x000F000Fu) | 0x43004300u;
+  const uint32_t p37 = ((x >> 12) & 0x000F000Fu) | 0x43004300u;
+  uint32_t o[4];
+  o[0] = __byte_perm(p04, p15, 0x5410);  // k0, k1
+  o[1] = __byte_perm(p26, p37, 0x5410);  // k2, k3
+  o[2] = __byte_perm(p04, p15, 0x7632);  // k4, k5
+  o[3] = __byte_perm(p26, p37, 0x7632);  // k6, k7
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&o[i]);
+    v = __hmul2(__hsub2(v, off), s2);
+    o[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int WK>
+__global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const SmemLayout L = smem_layout(WK, p.bn_max, p.stages, p.E);
+  const uint32_t sA = base_u32 + L.a;
+  const uint32_t sB = base_u32 + L.b;
+  const uint32_t bstage = static_cast<uint32_t>(p.bn_max) * 128u;
+  const uint32_t bars = base_u32 + L.bars;
+  const int ns = p.stages;
+#define FULL(s) (bars + 8u * static_cast<uint32_t>(s))
+#define EMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
+#define RAWFULL(s) (bars + 8u * static_cast<uint32_t>(2 * ns + (s)))
+  const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(3 * ns);
+  const uint32_t tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tfull0 + 32u;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.misc + 4);
+  int* tile_base = reinterpret_cast<int*>(base + L.tiles);
+  int* off = tile_base + (p.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------------- prologue
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(FULL(s), WK == kW_INT4 ? 5u : 1u);  // int4: producer + 4 converter warps
+      mbar_init(EMPTY(s), 1u);
+      if (WK == kW_INT4) mbar_init(RAWFULL(s), 1u);
+    }
+    mbar_init(tfull0, 1u);
+    mbar_init(tfull0 + 8u, 1u);
+    mbar_init(tempty0, 128u);
+    mbar_init(tempty0 + 8u, 128u);
+    mbar_init(drain_bar, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // Work-unit prefix over experts: expert e owns ceil(count_e / bn_max) * FB tiles.
+    const int per = (p.E + 31) / 32;
+    const int e0 = lane * per;
+    int local = 0;
+    for (int j = 0; j < per; ++j) {
+      const int e = e0 + j;
+      if (e < p.E) {
+        const int c = p.offsets[e + 1] - p.offsets[e];
+        local += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; ++j) {
+      const int e = e0 + j;
+      if (e < p.E) {
+        const int o0 = p.offsets[e];
+        const int c = p.offsets[e + 1] - o0;
+        tile_base[e] = run;
+        off[e] = o0;
+        run += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+      }
+    }
+    if (lane == 31) {
+      tile_base[p.E] = incl;
+      off[p.E] = p.offsets[p.E];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = tile_base[p.E] * p.P;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int kelem_b = (WK == kW_FP8) ? 128 : 64;
+      int st = 0;
+      uint32_t ph = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tile_base, off, p);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(EMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
+          if (WK == kW_INT4) {
+            const uint32_t dst = base_u32 + L.raw + st * kRawBytes;
+            mbar_expect_tx(RAWFULL(st), kRawBytes);
+            if (p.is_up)
+              tma_load_5d(dst, &maps.a, RAWFULL(st), kb * 32, 0, 0, t.fb * 4, t.e);
+            else
+              tma_load_3d(dst, &maps.a, RAWFULL(st), kb * 32, t.fb * 128, t.e);
+            mbar_expect_tx(FULL(st), bbytes);
+          } else {
+            const int kelem = (WK == kW_FP8) ? 128 : 64;
+            mbar_expect_tx(FULL(st), kABytes + bbytes);
+            if (p.is_up)
+              tma_load_5d(sA + st * kABytes, &maps.a, FULL(st), kb * kelem, 0, 0, t.fb * 4, t.e);
+            else
+              tma_load_3d(sA + st * kABytes, &maps.a, FULL(st), kb * kelem, t.fb * 128, t.e);
+          }
+          for (int j = 0; j < (t.n >> 4); ++j)
+            tma_load_2d(sB + st * bstage + j * 2048u, &maps.b, FULL(st), kb * kelem_b,
+                        t.row0 + 16 * j);
+          issued |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (ph << st);
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let loads already in flight land before the CTA exits.
+        for (int s = 0; s < ns; ++s)
+          if ((issued >> s) & 1u)
+            mbar_wait(WK == kW_INT4 ? RAWFULL(s) : FULL(s), (issued_par >> s) & 1u, nullptr,
+                      p.err, 0x180u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0;
+      uint32_t acc = 0, aph = 0;
+      bool ok = true, any = false;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tile_base, off, p);
+        if (!mbar_wait(tempty0 + 8u * acc, aph ^ 1u, abort_flag, p.err, 0x200u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccCols;
+        const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), WK == kW_FP8 ? 0u : 1u);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x210u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(sA + st * kABytes);
+          const uint64_t bd = sw128_kmajor_desc(sB + st * bstage);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t accum = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+            if (WK == kW_FP8)
+              mma_f8(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+            else
+              mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+          }
+          mma_commit(EMPTY(st));
+          any = true;
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8u * acc);
+        acc ^= 1u;
+        if (acc == 0u) aph ^= 1u;
+      }
+      if (!ok && any) {
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0u, nullptr, p.err, 0x280u);
+      }
+    }
+  } else if (warp < 6) {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    uint8_t* stg = base + L.stg + q * kStgBytesPerWarp;
+    uint32_t acc = 0, aph = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const Unit t = decode_unit(u, tile_base, off, p);
+      if (!mbar_wait(tfull0 + 8u * acc, aph, abort_flag, p.err, 0x300u)) break;
+      tc_fence_after();
+      float sc = 1.0f;
+      if (WK == kW_FP8) sc = p.a_scale[0] * p.w_scale[t.e];
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      for (int c0 = 0; c0 < t.nvalid; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
+        tmem_ld_wait();
+        const int ntok = min(16, t.nvalid - c0);
+        const size_t row = static_cast<size_t>(t.row0 + c0);
+        if (p.epi == kEpiSwiglu) {
+          // lane l < 16: gate row of feature 16q + l; lane l + 16: its up row.
+          const bool upl = lane >= 16;
+          const int f16 = lane & 15;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float x = __uint_as_float(v[c]) * sc;
+            const float o = __shfl_xor_sync(0xffffffffu, x, 16);
+            if ((c & 1) == static_cast<int>(upl)) {
+              const float g = upl ? o : x;
+              const float uu = upl ? x : o;
+              const float a = silu_f32(g) * uu;
+              if (WK == kW_FP8)
+                stg[c * 16 + f16] =
+                    static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(a, p.q_scale[0]), 0.f) & 0xFF);
+              else
+                reinterpret_cast<__nv_bfloat16*>(stg)[c * 16 + f16] = __float2bfloat16_rn(a);
+            }
+          }
+          __syncwarp();
+          const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16;
+          if (WK == kW_FP8) {
+            if (lane < ntok)
+              *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row + lane) * p.out_ld + col) =
+                  *reinterpret_cast<const uint4*>(stg + lane * 16);
+          } else {
+            const int tok = lane >> 1, half = lane & 1;
+            if (tok < ntok)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
+                                        col + half * 8) =
+                  *reinterpret_cast<const uint4*>(stg + tok * 32 + half * 16);
+          }
+        } else if (p.epi == kEpiStore) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            reinterpret_cast<__nv_bfloat16*>(stg)[c * 32 + lane] =
+                __float2bfloat16_rn(__uint_as_float(v[c]) * sc);
+          __syncwarp();
+          const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32;
+#pragma unroll
+          for (int i = lane; i < 64; i += 32) {
+            const int tok = i >> 2, part = i & 3;
+            if (tok < ntok)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
+                                        col + part * 8) =
+                  *reinterpret_cast<const uint4*>(stg + tok * 64 + part * 16);
+          }
+        } else {  // fp32 split-K partials
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            reinterpret_cast<float*>(stg)[c * 32 + lane] = __uint_as_float(v[c]) * sc;
+          __syncwarp();
+          float* dst0 = static_cast<float*>(p.out) + static_cast<size_t>(t.sp) * p.part_stride;
+#pragma unroll
+          for (int i = lane; i < 128; i += 32) {
+            const int tok = i >> 3, w8 = i & 7;
+            if (tok < ntok) {
+              size_t col;
+              if (p.is_up)
+                col = static_cast<size_t>((w8 >> 2) * p.I) + static_cast<size_t>(t.fb) * 64 + q * 16 +
+                      (w8 & 3) * 4;
+              else
+                col = static_cast<size_t>(t.fb) * 128 + q * 32 + w8 * 4;
+              *reinterpret_cast<float4*>(dst0 + (row + tok) * p.out_ld + col) =
+                  *reinterpret_cast<const float4*>(stg + tok * 128 + w8 * 16);
+            }
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8u * acc);
+      acc ^= 1u;
+      if (acc == 0u) aph ^= 1u;
+    }
+  } else if (WK == kW_INT4) {
+    // --------------------------------------------- int4 -> bf16 tile converters
+    const int m = threadIdx.x - 192;  // A row of the tile, 0..127
+    const uint8_t* rawbase = base + L.raw;
+    uint8_t* abase = base + L.a;
+    const __half* scales = static_cast<const __half*>(p.w4_scale);
+    int st = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit t = decode_unit(u, tile_base, off, p);
+      const int grow = p.is_up ? (((m >> 4) & 1) * p.I + t.fb * 64 + (m >> 5) * 16 + (m & 15))
+                               : (t.fb * 128 + m);
+      const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
+      for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(srow[kb >> 1]));
+        if (!mbar_wait(RAWFULL(st), ph, abort_flag, p.err, 0x400u)) {
+          ok = false;
+          break;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(rawbase + st * kRawBytes + m * 32);
+        const uint4 r0 = src[0], r1 = src[1];
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        uint8_t* arow = abase + st * kABytes + m * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = dequant8(w[j], s2);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(FULL(st));
+        if (++st == ns) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+#undef FULL
+#undef EMPTY
+#undef RAWFULL
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int WK>
+cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                       cudaStream_t s) {
+  static int configured_device = -1;  // attribute set once per device (single-device processes)
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (configured_device != dev) {
+    err = cudaFuncSetAttribute(grouped_gemm_kernel<WK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               232448);
+    if (err != cudaSuccess) return err;
+    configured_device = dev;
+  }
+  grouped_gemm_kernel<WK><<<grid, gemm_threads(WK), smem, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int E) {
+  return smem_layout(wkind, bn_max, stages, E).total;
+}
+
+int gemm_threads(int wkind) { return wkind == kW_INT4 ? 320 : 192; }
+
+cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
+                                size_t smem, cudaStream_t s) {
+  switch (wkind) {
+    case kW_BF16:
+      return launch_one<kW_BF16>(maps, p, grid, smem, s);
+    case kW_FP8:
+      return launch_one<kW_FP8>(maps, p, grid, smem, s);
+    case kW_INT4:
+      return launch_one<kW_INT4>(maps, p, grid, smem, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,96 @@
+// Internal launchers of the MoE kernels (host side).  The C ABI in api.cu
+// validates arguments and lays out the workspace; these functions only launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ------------------------------------------------------------------- gate
+struct GateArgs {
+  const float* logits;  // [T, E]
+  const float* bias;    // [E] or null
+  int32_t* ids;         // [T, k]
+  float* w;             // [T, k]
+  int T, E, k;
+  int sigmoid;          // 0 softmax, 1 sigmoid
+  int renormalize;
+  int n_group, topk_group;
+  float scale;
+};
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------------ align
+constexpr int kAlignSlotsPerCta = 1024;
+inline int align_blocks(int S) { return (S + kAlignSlotsPerCta - 1) / kAlignSlotsPerCta; }
+
+struct AlignArgs {
+  const int32_t* ids;     // [S]
+  int S, E, k, H;
+  int32_t* block_counts;  // [nblk, E] scratch
+  int32_t* counts;        // [E]
+  int32_t* offsets;       // [E + 1]
+  int32_t* perm;          // [S]
+  int32_t* inv;           // [S]
+  const void* x;          // [T, H] bf16
+  void* x_perm;           // [S, H] bf16 or e4m3
+  const float* a1;        // fp8: [1]
+  int fp8;
+  uint32_t* err;
+};
+cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+
+cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm, int E, int S,
+                                    int block, size_t capacity, int32_t* sorted_ids,
+                                    int32_t* block_expert, int32_t* total, cudaStream_t s);
+
+// ----------------------------------------------------------------- reduce
+cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, const float* w,
+                                    int T, int H, int k, void* out, cudaStream_t s);
+
+// Split-K finishing passes (fixed summation order over the P slices).
+cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
+                                 const float* a2, int fp8, void* act, cudaStream_t s);
+cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H,
+                               void* y, cudaStream_t s);
+
+// ------------------------------------------------------------ grouped GEMM
+enum WKind : int { kW_BF16 = 0, kW_FP8 = 1, kW_INT4 = 2 };
+enum EpiKind : int { kEpiSwiglu = 0, kEpiStore = 1, kEpiPartial = 2 };
+
+struct GemmParams {
+  const int32_t* offsets;  // [E + 1]
+  uint32_t* err;
+  void* out;
+  const float* a_scale;    // fp8: activation scale of the B operand (a1 or a2)
+  const float* w_scale;    // fp8: per-expert weight scale [E]
+  const float* q_scale;    // fp8 gate_up: a2, the scale `act` is quantised with
+  const void* w4_scale;    // int4: half [E, R, G]
+  int64_t out_ld;          // elements per output row
+  int64_t part_stride;     // elements between split-K slices
+  int E, S, I;
+  int FB;                  // feature blocks (I/64 for gate_up, H/128 for down)
+  int KB;                  // k blocks of the reduction
+  int P;                   // split-K factor
+  int bn_max;              // token tile limit: multiple of 16, <= 256
+  int stages;
+  int epi;                 // EpiKind
+  int is_up;
+  int R;                   // weight rows per expert (2I or H)
+  int G;                   // int4 groups per weight row
+};
+
+struct GemmMaps {
+  CUtensorMap a;  // weights (bf16/e4m3 swizzled tile, or packed int4 plain tile)
+  CUtensorMap b;  // token rows (x_perm or act)
+};
+
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int E);
+int gemm_threads(int wkind);
+cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
+                                size_t smem, cudaStream_t s);
+
+}  // namespace moe

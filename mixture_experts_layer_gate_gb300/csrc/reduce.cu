@@ -1,0 +1,122 @@
+// Stage 4: unpermute and top-k weighted reduction, plus the split-K finishing
+// passes of the grouped GEMMs.
+//
+// "Add deepseek_v3 fused gate" (sglang) names TensorRT-LLM's
+// unpermute_and_reduce; "[kernel] introduce fused_moe_triton_splitk to sglang"
+// reports that split-K partials added with atomics gave random values.  Every
+// sum here runs in a fixed order in fp32 (j = 0..k-1; slice p = 0..P-1), so the
+// result is the same on every run.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// grid (ceil(H / 2048), T); each thread owns 8 consecutive elements of a row.
+__global__ void __launch_bounds__(256)
+    unpermute_reduce_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ inv,
+                            const float* __restrict__ w, int H, int k, __nv_bfloat16* out) {
+  const int t = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c * 8 >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int r = inv[static_cast<size_t>(t) * k + j];
+    const float wj = w[static_cast<size_t>(t) * k + j];
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(r) * H) + c);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wj, bf16_lo(u[i]), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, bf16_hi(u[i]), acc[2 * i + 1]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
+}
+
+// act[r, i] = silu(sum_p part[p][r][i]) * sum_p part[p][r][I + i]; 4 columns per thread.
+template <bool FP8>
+__global__ void __launch_bounds__(256)
+    swiglu_finish_kernel(const float* __restrict__ part, int P, int64_t pstride, int I,
+                         const float* __restrict__ a2, void* act) {
+  const int r = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c * 4 >= I) return;
+  const float* row = part + static_cast<size_t>(r) * (2 * static_cast<size_t>(I));
+  float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+  for (int p = 0; p < P; ++p) {
+    const float4 gg = __ldg(reinterpret_cast<const float4*>(row + p * pstride) + c);
+    const float4 uu = __ldg(reinterpret_cast<const float4*>(row + p * pstride + I) + c);
+    g.x += gg.x; g.y += gg.y; g.z += gg.z; g.w += gg.w;
+    u.x += uu.x; u.y += uu.y; u.z += uu.z; u.w += uu.w;
+  }
+  const float a0 = silu_f32(g.x) * u.x, a1 = silu_f32(g.y) * u.y;
+  const float a2v = silu_f32(g.z) * u.z, a3 = silu_f32(g.w) * u.w;
+  if (!FP8) {
+    uint2 o = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2v, a3));
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(act) + static_cast<size_t>(r) * I)[c] = o;
+  } else {
+    const float s = a2[0];
+    const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a0, s), __fdiv_rn(a1, s));
+    const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(a2v, s), __fdiv_rn(a3, s));
+    reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(act) + static_cast<size_t>(r) * I)[c] =
+        lo | (hi << 16);
+  }
+}
+
+// y[r, h] = sum_p part[p][r][h] (bf16 out); 4 columns per thread.
+__global__ void __launch_bounds__(256)
+    down_finish_kernel(const float* __restrict__ part, int P, int64_t pstride, int H,
+                       __nv_bfloat16* y) {
+  const int r = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c * 4 >= H) return;
+  const float* row = part + static_cast<size_t>(r) * H;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < P; ++p) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + p * pstride) + c);
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  }
+  reinterpret_cast<uint2*>(y + static_cast<size_t>(r) * H)[c] =
+      make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+}
+
+}  // namespace
+
+cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, const float* w, int T,
+                                    int H, int k, void* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid((H / 8 + 255) / 256, T);
+  unpermute_reduce_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y_perm), inv, w,
+                                              H, k, static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
+                                 const float* a2, int fp8, void* act, cudaStream_t s) {
+  if (S == 0) return cudaSuccess;
+  const dim3 grid((I / 4 + 255) / 256, S);
+  if (fp8)
+    swiglu_finish_kernel<true><<<grid, 256, 0, s>>>(part, P, pstride, I, a2, act);
+  else
+    swiglu_finish_kernel<false><<<grid, 256, 0, s>>>(part, P, pstride, I, a2, act);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H, void* y,
+                               cudaStream_t s) {
+  if (S == 0) return cudaSuccess;
+  const dim3 grid((H / 4 + 255) / 256, S);
+  down_finish_kernel<<<grid, 256, 0, s>>>(part, P, pstride, H, static_cast<__nv_bfloat16*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

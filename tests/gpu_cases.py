@@ -1,0 +1,184 @@
+"""Helpers for the GPU parity tests: run every stage through the C ABI and
+compare against the oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import mixture_experts_layer_gate_gb300 as moe
+import oracle
+from synth import make_tokens, make_weights
+from tests.oracle_io import np_of, oracle_inputs
+
+TOL = {"bf16": 1e-2, "fp8": 3e-2, "int4": 4e-2}
+
+
+def lib_problem(shape, T):
+    return moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
+                       renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
+                       routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                       group_size=shape.group_size)
+
+
+def lib_weights(w, tok):
+    return moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+
+
+@dataclasses.dataclass
+class StageOut:
+    ids: torch.Tensor
+    w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    inv: torch.Tensor
+    x_perm: torch.Tensor
+    act: torch.Tensor
+    y_perm: torch.Tensor
+    out: torch.Tensor
+    out_forward: torch.Tensor
+
+
+def run_stages(shape, T, weights, tok, device) -> StageOut:
+    p = lib_problem(shape, T)
+    wts = lib_weights(weights, tok)
+    k, S, H, I, E = shape.top_k, T * shape.top_k, shape.H, shape.I, shape.E
+    adt = torch.uint8 if shape.wdtype == "fp8" else torch.bfloat16
+    ids = torch.full((T, k), -1, dtype=torch.int32, device=device)
+    w = torch.zeros((T, k), dtype=torch.float32, device=device)
+    counts = torch.full((E,), -1, dtype=torch.int32, device=device)
+    offsets = torch.full((E + 1,), -1, dtype=torch.int32, device=device)
+    perm = torch.full((S,), -1, dtype=torch.int32, device=device)
+    inv = torch.full((S,), -1, dtype=torch.int32, device=device)
+    x_perm = torch.zeros((S, H), dtype=adt, device=device)
+    act = torch.zeros((S, I), dtype=adt, device=device)
+    y_perm = torch.zeros((S, H), dtype=torch.bfloat16, device=device)
+    out = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+    out_f = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+    ws = moe.alloc_workspace(p, device, full=False)
+    moe.gate_topk(p, tok.logits, tok.bias, ids, w)
+    moe.align_permute(p, ids, tok.x, tok.a1_scale, counts, offsets, perm, inv, x_perm, ws)
+    moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws)
+    moe.grouped_gemm_down(p, wts, act, offsets, y_perm, ws)
+    moe.unpermute_reduce(p, y_perm, inv, w, out, ws)
+    assert moe.get_device_error(ws) == 0
+    wsf = moe.alloc_workspace(p, device, full=True)
+    moe.forward(p, wts, tok.x, tok.logits, tok.bias, out_f, wsf)
+    assert moe.get_device_error(wsf) == 0
+    torch.cuda.synchronize()
+    return StageOut(ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, out, out_f)
+
+
+def rel_err(gpu, ref) -> float:
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.abs(ref).max()
+    if scale == 0:
+        return float(np.abs(gpu).max())
+    return float(np.abs(gpu - ref).max() / scale)
+
+
+def to_f64(t: torch.Tensor, wdtype: str, scale=None) -> np.ndarray:
+    """bf16 tensor -> exact float64; e4m3 codes (uint8) -> decoded * scale."""
+    if t.dtype == torch.uint8:
+        v = oracle.decode_e4m3(t.cpu().numpy())
+        return v * (1.0 if scale is None else float(np.float32(scale)))
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_gate(shape, T, tok, g: StageOut):
+    """ids bit-exact except near-ties (where any valid choice is accepted);
+    weights to 1e-5 relative for the GPU's ids.  Returns the ids to use."""
+    p, inp = oracle_inputs(shape, _NoWeights(), tok)
+    ids_o, amb = oracle.gate_select(p, inp["logits"], inp["bias"])
+    ids_g = g.ids.cpu().numpy()
+    assert ids_g.min() >= 0 and ids_g.max() < shape.E
+    for row in ids_g:
+        assert len(set(row.tolist())) == shape.top_k
+    mism = np.any(ids_o != ids_g, axis=1)
+    assert not np.any(mism & ~amb), f"ids differ on unflagged tokens {np.nonzero(mism & ~amb)[0][:10]}"
+    w_o = oracle.gate_weights(p, inp["logits"], ids_g)
+    w_g = g.w.cpu().numpy().astype(np.float64)
+    assert np.allclose(w_g, w_o, rtol=1e-5, atol=1e-7), np.abs(w_g - w_o).max()
+    return ids_g, int(mism.sum()), int(amb.sum())
+
+
+def check_align(shape, ids_g, g: StageOut):
+    counts, offsets, perm, inv = oracle.align(ids_g, shape.E)
+    assert np.array_equal(g.counts.cpu().numpy(), counts)
+    assert np.array_equal(g.offsets.cpu().numpy(), offsets)
+    assert np.array_equal(g.perm.cpu().numpy(), perm)
+    assert np.array_equal(g.inv.cpu().numpy(), inv)
+    return counts, offsets, perm, inv
+
+
+class _NoWeights:
+    w13 = w2 = w13_scale = w2_scale = None
+
+
+def full_check(shape, T, device, seed=0, check_stages=True):
+    """Whole-layer parity on a size the oracle computes completely."""
+    w = make_weights(shape, device, seed)
+    tok = make_tokens(shape, T, device, seed)
+    g = run_stages(shape, T, w, tok, device)
+    assert torch.equal(g.out, g.out_forward), "moe_forward differs from the staged calls"
+    ids_g, n_mism, n_amb = check_gate(shape, T, tok, g)
+    counts, offsets, perm, inv = check_align(shape, ids_g, g)
+    p, inp = oracle_inputs(shape, w, tok)
+    res = oracle.forward(p, inp["x_bits"], inp["logits"], inp["bias"], inp["experts"], inp["a1"],
+                         inp["a2"], ids=ids_g)
+    tol = TOL[shape.wdtype]
+    if check_stages:
+        # x_perm: exact copy (bf16) or exact e4m3 codes of x / a1
+        xg = g.x_perm.cpu()
+        if shape.wdtype == "fp8":
+            codes = oracle.quantize_fp8(oracle.decode_bf16(inp["x_bits"]), inp["a1"])
+            assert np.array_equal(xg.numpy(), codes[perm // shape.top_k])
+        else:
+            assert np.array_equal(to_f64(xg, "bf16"), oracle.decode_bf16(inp["x_bits"])[perm // shape.top_k])
+        # act from the same x_perm
+        act_g = to_f64(g.act, shape.wdtype, inp["a2"])
+        if shape.wdtype == "fp8":
+            # compare in e4m3 steps: neighbours allowed on a small fraction
+            vals = np.sort(oracle.decode_e4m3(np.arange(256, dtype=np.uint8)))
+            vals = vals[np.isfinite(vals)]
+            a2 = float(np.float32(inp["a2"]))
+            idx_g = np.searchsorted(vals, act_g / a2)
+            idx_o = np.searchsorted(vals, res["act"] / a2)
+            diff = np.abs(idx_g - idx_o)
+            assert diff.max() <= 1, diff.max()
+            assert np.mean(diff > 0) < 0.02, np.mean(diff > 0)
+        else:
+            assert rel_err(act_g, res["act"]) <= tol, rel_err(act_g, res["act"])
+        # y_perm from the GPU's act (isolates the down GEMM)
+        y_ref = np.zeros_like(res["y_perm"])
+        for e in range(shape.E):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                _, W2 = inp["experts"](e)
+                y_ref[lo:hi] = oracle.down(act_g[lo:hi], W2)
+        assert rel_err(to_f64(g.y_perm, "bf16"), y_ref) <= 1e-2, rel_err(to_f64(g.y_perm, "bf16"), y_ref)
+    err = rel_err(to_f64(g.out, "bf16"), res["out"])
+    assert err <= tol, f"{shape.name} T={T}: out rel err {err}"
+    return dict(err=err, mism=n_mism, amb=n_amb, counts=counts)
+
+
+def sampled_check(shape, T, device, n_sample=4, seed=0):
+    """Full-size parity: gate and align on every token, output on sampled tokens."""
+    w = make_weights(shape, device, seed)
+    tok = make_tokens(shape, T, device, seed)
+    g = run_stages(shape, T, w, tok, device)
+    assert torch.equal(g.out, g.out_forward)
+    ids_g, n_mism, n_amb = check_gate(shape, T, tok, g)
+    counts, offsets, perm, inv = check_align(shape, ids_g, g)
+    p, inp = oracle_inputs(shape, w, tok)
+    rng = np.random.default_rng(T)
+    rows = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, size=n_sample)]))
+    ref = oracle.token_outputs(p, rows, inp["x_bits"], inp["logits"], inp["bias"], inp["experts"],
+                               inp["a1"], inp["a2"], ids=ids_g)
+    got = to_f64(g.out[torch.as_tensor(rows, device=device)], "bf16")
+    err = rel_err(got, ref)
+    assert err <= TOL[shape.wdtype], f"{shape.name} T={T}: sampled out rel err {err}"
+    return dict(err=err, mism=n_mism, amb=n_amb, counts=counts)

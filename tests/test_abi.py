@@ -1,0 +1,110 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+entry point include/moe.h declares, and rejects bad arguments before touching
+the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_gate_gb300 as moe
+from mixture_experts_layer_gate_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from mixture_experts_layer_gate_gb300 import build
+        build.build()
+    return moe.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ("moe_gate_topk", "moe_align_permute", "moe_grouped_gemm_swiglu", "moe_grouped_gemm_down",
+              "moe_unpermute_reduce", "moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(binding.EXPORTED) | set(names)
+
+
+def test_struct_layout_matches_header():
+    assert ctypes.sizeof(binding.Problem) == 48
+    assert ctypes.sizeof(binding.WeightsStruct) == 48
+    assert ctypes.sizeof(binding.Plan) == 28
+
+
+def test_status_strings(lib):
+    assert moe.status_string(0) == "ok"
+    assert "workspace" in moe.status_string(3)
+    assert moe.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=100), dict(I=96), dict(top_k=9), dict(E=2048), dict(T=-1),
+    dict(scoring="softmax", n_group=2, topk_group=1),
+    dict(scoring="sigmoid", n_group=3, topk_group=1),
+    dict(scoring="sigmoid", n_group=4, topk_group=5),
+    dict(scoring="sigmoid", n_group=4, topk_group=1, top_k=3, E=8),
+    dict(wdtype="int4", group_size=64),
+])
+def test_invalid_problems_rejected(lib, bad):
+    kw = dict(T=4, H=256, I=512, E=8, top_k=2)
+    kw.update(bad)
+    p = moe.problem(**kw)
+    assert moe.workspace_size(p) == 0
+    assert moe.scratch_size(p) == 0
+    st = lib.moe_gate_topk(ctypes.byref(p), None, None, None, None, None)
+    assert st in (1, 2)
+
+
+def test_null_and_misaligned_arguments_rejected(lib):
+    p = moe.problem(4, 256, 512, 8, 2)
+    assert lib.moe_gate_topk(ctypes.byref(p), None, None, None, None, None) == 1
+    assert lib.moe_gate_topk(None, None, None, None, None, None) == 1
+    # workspace too small / missing
+    assert lib.moe_align_permute(ctypes.byref(p), None, None, None, None, None, None, None, None,
+                                 None, 0, None) == 3
+    assert lib.moe_unpermute_reduce(ctypes.byref(p), 16, 16, 16, 16, 256, 8, None) == 3
+    w = binding.WeightsStruct(None, None, None, None, None, None)
+    assert lib.moe_forward(ctypes.byref(p), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    w = binding.WeightsStruct(4096, 4097, None, None, None, None)   # misaligned w2
+    assert lib.moe_forward(ctypes.byref(p), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    pf = moe.problem(4, 256, 512, 8, 2, wdtype="fp8")
+    w = binding.WeightsStruct(4096, 8192, None, None, None, None)   # fp8 needs scales
+    assert lib.moe_forward(ctypes.byref(pf), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+
+
+def test_workspace_sizes_are_monotone_and_cover_intermediates(lib):
+    prev = 0
+    for T in (1, 2, 8, 64, 512, 4096):
+        p = moe.problem(T, 4096, 14336, 8, 2)
+        ws = moe.workspace_size(p)
+        S = 2 * T
+        # at least x_perm + act + y_perm + ids/w/perm/inv
+        assert ws >= S * (4096 * 2 + 14336 * 2 + 4096 * 2) + 4 * S * 4
+        assert moe.scratch_size(p) <= ws
+        prev = ws
+    pe = moe.problem(0, 4096, 14336, 8, 2)
+    assert moe.workspace_size(pe) > 0
+
+
+def test_padded_capacity(lib):
+    p = moe.problem(4, 256, 512, 4, 2)
+    assert moe.padded_capacity(p, 2) == 8 + 4
+    assert moe.padded_capacity(p, 1) == 8
+    assert moe.padded_capacity(p, 0) == 0
