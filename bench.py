@@ -27,6 +27,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s and achieved % of roofline (HBM or tensor) vs batch 1–4096"
 UNIT = "tokens/s"
 CONFIG_NAME = "mixtral"
+WORKLOADS = {"mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
+             "dsv3": "deepseek_v3_moe_layer_int4", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
 
 
 def _peaks():
@@ -136,6 +138,10 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     moe.load()
     shape = SHAPES[args.config]
+    if args.E:
+        # profiling aid: same layer shape with fewer experts (smaller device footprint)
+        import dataclasses
+        shape = dataclasses.replace(shape, E=args.E)
     T = args.T
     hbm, bf16_peak, bf16_sust, peak_src = _peaks()
 
@@ -275,11 +281,15 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "mixtral_8x7b_moe_layer", "T": T, "H": shape.H, "I": shape.I, "E": shape.E,
-                   "top_k": shape.top_k, "gate": "softmax top-2, renormalised", "weights": "bf16 N(0,0.02)",
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "int4": "bf16"}[shape.wdtype],
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS.get(args.config, args.config) + (f"_E{shape.E}" if args.E else ""), "T": T, "H": shape.H, "I": shape.I, "E": shape.E,
+                   "top_k": shape.top_k, "gate": f"{shape.scoring} top-{shape.top_k}" +
+                   (", renormalised" if shape.renormalize else "") +
+                   (f", {shape.n_group} groups keep {shape.topk_group}" if shape.n_group else ""),
+                   "weights": {"bf16": "bf16", "fp8": "e4m3 per-expert scale", "int4": "int4 group-128"}[shape.wdtype],
                    "global_batch": world * T, "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "no flush: expert weights (2.8 GB) exceed L2 every step",
+                   "l2": "no flush: expert weights exceed L2 (129 MB) every step",
                    "cuda_graph": True, "plan": {"bn_max": plan.bn_max_up, "splits_up": plan.splits_up,
                                                 "splits_down": plan.splits_down, "stages_up": plan.stages_up,
                                                 "sms": plan.num_sms}},
@@ -463,9 +473,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=CONFIG_NAME)
     ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling small cases)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=64)
+    ap.add_argument("--cpu-sample", type=int, default=2048)
     ap.add_argument("--ref-sample", type=int, default=16)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -207,14 +207,20 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream);
 /* Static, human-readable name of a status. */
 const char* moe_status_string(moe_status_t s);
 
-/* Tile choices the library makes for a problem (for tests and benchmarks):
- * token tile limit and split-K factor of the two GEMMs on the current device. */
+/* Launch plan the library makes for a problem (for tests and benchmarks): per
+ * GEMM the token tile limit, split-K factor, operand ring depth, converted
+ * weight ring depth (int4 only, else 0) and dynamic shared memory bytes. */
 typedef struct {
-  int32_t bn_max_up, splits_up, stages_up;
-  int32_t bn_max_down, splits_down, stages_down;
+  int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
+  int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
   int32_t num_sms;
 } moe_plan_t;
+
+/* Plan on the current device. */
 moe_status_t moe_get_plan(const moe_problem_t* p, moe_plan_t* plan);
+
+/* Plan for a device with `num_sms` SMs; pure host computation, needs no GPU. */
+moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_plan_t* plan);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ SCORING = {"softmax": 0, "sigmoid": 1}
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "moe_gate_topk",
             "moe_align_permute", "moe_align_block_size", "moe_grouped_gemm_swiglu",
             "moe_grouped_gemm_down", "moe_unpermute_reduce", "moe_forward", "moe_get_device_error",
-            "moe_status_string", "moe_get_plan")
+            "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms")
 
 
 class MoEError(RuntimeError):
@@ -51,9 +51,10 @@ class WeightsStruct(ctypes.Structure):
 
 class Plan(ctypes.Structure):
     _fields_ = [("bn_max_up", ctypes.c_int32), ("splits_up", ctypes.c_int32),
-                ("stages_up", ctypes.c_int32), ("bn_max_down", ctypes.c_int32),
-                ("splits_down", ctypes.c_int32), ("stages_down", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32)]
+                ("stages_up", ctypes.c_int32), ("astages_up", ctypes.c_int32), ("smem_up", ctypes.c_int32),
+                ("bn_max_down", ctypes.c_int32), ("splits_down", ctypes.c_int32),
+                ("stages_down", ctypes.c_int32), ("astages_down", ctypes.c_int32),
+                ("smem_down", ctypes.c_int32), ("num_sms", ctypes.c_int32)]
 
 
 _lib = None
@@ -83,6 +84,7 @@ def load(path: str = LIB_PATH):
         "moe_get_device_error": (st, [vp, vp]),
         "moe_status_string": (ctypes.c_char_p, [st]),
         "moe_get_plan": (st, [P, ctypes.POINTER(Plan)]),
+        "moe_get_plan_for_sms": (st, [P, i32, ctypes.POINTER(Plan)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -197,9 +199,14 @@ def get_device_error(ws, stream=None) -> int:
     return int(load().moe_get_device_error(_ptr(ws), _stream(stream)))
 
 
-def get_plan(p: Problem) -> Plan:
+def get_plan(p: Problem, num_sms: int | None = None) -> Plan:
+    """Launch plan on the current device, or for `num_sms` SMs (no GPU needed)."""
     plan = Plan()
-    _check(load().moe_get_plan(ctypes.byref(p), ctypes.byref(plan)), "moe_get_plan")
+    if num_sms is None:
+        _check(load().moe_get_plan(ctypes.byref(p), ctypes.byref(plan)), "moe_get_plan")
+    else:
+        _check(load().moe_get_plan_for_sms(ctypes.byref(p), int(num_sms), ctypes.byref(plan)),
+               "moe_get_plan_for_sms")
     return plan
 
 

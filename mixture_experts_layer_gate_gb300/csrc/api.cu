@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <mutex>
 
@@ -20,6 +21,7 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxStages = 8;
+constexpr int kMaxStagesInt4 = 16;
 constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
 constexpr size_t kMaxDynSmem = 232448;
 
@@ -111,9 +113,16 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, FB, KB;
+  int bn_max, P, stages, astages, FB, KB;
   size_t smem;
 };
+
+// Tuning overrides (benchmarking only): MOE_BN_MAX, MOE_STAGES, MOE_SPLITS.
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == 0) return dflt;
+  return std::atoi(v);
+}
 
 int wkind_of(const moe_problem_t& p) {
   return p.wdtype == MOE_W_FP8_E4M3 ? kW_FP8 : (p.wdtype == MOE_W_INT4_G128 ? kW_INT4 : kW_BF16);
@@ -162,16 +171,46 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   GemmPlan g;
   const int wk = wkind_of(p);
   g.bn_max = plan_bn_max(p);
+  const int bn_env = env_int("MOE_BN_MAX", 0);
+  if (bn_env >= 16 && bn_env <= 256 && bn_env % 16 == 0) g.bn_max = bn_env;
   g.FB = up ? p.I / 64 : p.H / 128;
   const int K = up ? p.H : p.I;
   g.KB = K / (wk == kW_FP8 ? 128 : 64);
   g.P = plan_splits(p, up, g.bn_max, g.KB, std::min(sms, kSmsForSizing));
-  const size_t per_stage =
-      16384 + static_cast<size_t>(g.bn_max) * 128 + (wk == kW_INT4 ? 4096 : 0) + 24;
-  const size_t fixed = gemm_smem_bytes(wk, g.bn_max, 0, p.E);
-  g.stages = static_cast<int>(std::min<size_t>(kMaxStages, (kMaxDynSmem - fixed) / per_stage));
-  while (g.stages > 2 && gemm_smem_bytes(wk, g.bn_max, g.stages, p.E) > kMaxDynSmem) --g.stages;
-  g.smem = gemm_smem_bytes(wk, g.bn_max, g.stages, p.E);
+  const int p_env = env_int("MOE_SPLITS", 0);
+  if (p_env >= 1 && p_env <= kMaxSplits && p_env <= std::max(1, g.KB / 4)) g.P = p_env;
+  // Ring depth: as many stages as shared memory holds (capped).  int4 keeps a
+  // deep ring of packed weights + token rows and a short ring of converted
+  // bf16 weight tiles.
+  size_t per_stage;
+  int cap;
+  if (wk == kW_INT4) {
+    g.astages = g.bn_max >= 128 ? 2 : 4;
+    const int as_env = env_int("MOE_ASTAGES", 0);
+    if (as_env >= 2 && as_env <= 12) g.astages = as_env;
+    per_stage = static_cast<size_t>(g.bn_max) * 128 + 4096 + 16;
+    cap = kMaxStagesInt4;
+  } else {
+    g.astages = 0;
+    per_stage = 16384 + static_cast<size_t>(g.bn_max) * 128 + 16;
+    cap = kMaxStages;
+  }
+  const size_t fixed = gemm_smem_bytes(wk, g.bn_max, 0, g.astages, p.E);
+  g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed) / per_stage));
+  const int st_env = env_int("MOE_STAGES", 0);
+  if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
+  while (g.stages > 2 && gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E) > kMaxDynSmem)
+    --g.stages;
+  // int4: the converter groups wait on the operand ring with parity waits, so
+  // they must never run more than one ring phase ahead of it: the converted
+  // ring may not be deeper than the operand ring.
+  if (wk == kW_INT4 && g.astages > g.stages) {
+    g.astages = std::max(2, g.stages);
+    const size_t fixed2 = gemm_smem_bytes(wk, g.bn_max, 0, g.astages, p.E);
+    g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed2) / per_stage));
+    // (the kernel refuses a plan that still violates the rule instead of running it)
+  }
+  g.smem = gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E);
   return g;
 }
 
@@ -312,15 +351,18 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   }
   if (!ok) return MOE_ERR_CUDA;
   {
-    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path).
+    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path), three box heights.
     const uint64_t K = up ? H : I;
     const bool f8 = wk == kW_FP8;
     uint64_t dims[2] = {K, static_cast<uint64_t>(S)};
     uint64_t str[1] = {K * (f8 ? 1 : 2)};
-    uint32_t box[2] = {f8 ? 128u : 64u, 16};
-    if (!encode_map(&maps.b, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return MOE_ERR_CUDA;
+    const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap* dst[3] = {&maps.b, &maps.b64, &maps.b16};
+    const uint32_t rows[3] = {static_cast<uint32_t>(g.bn_max), 64u, 16u};
+    for (int i = 0; i < 3; ++i) {
+      uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
+      if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+    }
   }
 
   GemmParams gp;
@@ -338,6 +380,8 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.P = g.P;
   gp.bn_max = g.bn_max;
   gp.stages = g.stages;
+  gp.astages = g.astages;
+  gp.full_box = env_int("MOE_FULL_BOX", 0) != 0 ? 1 : 0;
   gp.is_up = up ? 1 : 0;
   gp.R = up ? 2 * p.I : p.H;
   gp.G = up ? p.H / 128 : p.I / 128;
@@ -543,21 +587,31 @@ const char* moe_status_string(moe_status_t s) {
   }
 }
 
+moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_plan_t* plan) {
+  MOE_TRY(validate_problem(p));
+  if (plan == nullptr || num_sms < 1) return MOE_ERR_INVALID_ARG;
+  const GemmPlan u = plan_gemm(*p, true, num_sms);
+  const GemmPlan d = plan_gemm(*p, false, num_sms);
+  plan->bn_max_up = u.bn_max;
+  plan->splits_up = u.P;
+  plan->stages_up = u.stages;
+  plan->astages_up = u.astages;
+  plan->smem_up = static_cast<int32_t>(u.smem);
+  plan->bn_max_down = d.bn_max;
+  plan->splits_down = d.P;
+  plan->stages_down = d.stages;
+  plan->astages_down = d.astages;
+  plan->smem_down = static_cast<int32_t>(d.smem);
+  plan->num_sms = num_sms;
+  return MOE_OK;
+}
+
 moe_status_t moe_get_plan(const moe_problem_t* p, moe_plan_t* plan) {
   MOE_TRY(validate_problem(p));
   if (plan == nullptr) return MOE_ERR_INVALID_ARG;
   DeviceInfo di;
   if (device_info(&di) != cudaSuccess) return MOE_ERR_CUDA;
-  const GemmPlan u = plan_gemm(*p, true, di.sms);
-  const GemmPlan d = plan_gemm(*p, false, di.sms);
-  plan->bn_max_up = u.bn_max;
-  plan->splits_up = u.P;
-  plan->stages_up = u.stages;
-  plan->bn_max_down = d.bn_max;
-  plan->splits_down = d.P;
-  plan->stages_down = d.stages;
-  plan->num_sms = di.sms;
-  return MOE_OK;
+  return moe_get_plan_for_sms(p, di.sms, plan);
 }
 
 }  // extern "C"

@@ -40,24 +40,40 @@ constexpr int kStgBytesPerWarp = 2048;
 constexpr int kStgBytes = 4 * kStgBytesPerWarp;
 constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kConvGroups = 2;   // int4: converter warp groups, alternating k-blocks
 
+// Shared-memory plan (offsets from a 1024-aligned base).
+//   bf16 / fp8 : ring of `stages` x {A tile 16 KB, B tile bn_max x 128 B}
+//   int4       : ring of `stages` x {B tile bn_max x 128 B, packed A 4 KB}
+//                plus ring of `astages` converted bf16 A tiles (16 KB each)
 struct SmemLayout {
-  uint32_t a, b, raw, stg, bars, misc, tiles, total;
+  uint32_t a, r, r_stride, r_raw, stg, bars, misc, tiles, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages, int E) {
+__host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages, int astages,
+                                                  int E) {
   SmemLayout L;
   uint32_t o = 0;
-  L.a = o;
-  o += stages * kABytes;
-  L.b = o;
-  o += stages * bn_max * 128;  // bn_max % 16 == 0 keeps 2 KB granularity
-  L.raw = o;
-  if (wk == kW_INT4) o += stages * kRawBytes;
+  const uint32_t bbytes = static_cast<uint32_t>(bn_max) * 128u;  // multiple of 2 KB
+  if (wk == kW_INT4) {
+    L.a = o;
+    o += astages * kABytes;
+    L.r = o;
+    L.r_stride = bbytes + kRawBytes;
+    L.r_raw = bbytes;
+    o += stages * L.r_stride;
+  } else {
+    L.a = o;
+    o += stages * kABytes;
+    L.r = o;
+    L.r_stride = bbytes;
+    L.r_raw = 0;
+    o += stages * bbytes;
+  }
   L.stg = o;
   o += kStgBytes;
   L.bars = o;
-  o += (3 * stages + 5) * 8;
+  o += (2 * stages + 2 * astages + 5) * 8;
   o = (o + 15u) & ~15u;
   L.misc = o;
   o += 16;
@@ -120,23 +136,52 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Issues the token-row loads of one k-block: a single box for a full tile,
+// 64- and 16-row boxes for an expert's ragged last tile (few, large TMA
+// requests keep the pipe fed).
+__device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const GemmParams& p,
+                                                const Unit& t, uint32_t dst, uint32_t bar, int kcoord) {
+  if (t.n == p.bn_max || p.full_box) {
+    tma_load_2d(dst, &maps.b, bar, kcoord, t.row0);
+  } else {
+    int r = 0;
+    for (; r + 64 <= t.n; r += 64)
+      tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, t.row0 + r);
+    for (; r < t.n; r += 16)
+      tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, t.row0 + r);
+  }
+}
+
 template <int WK>
-__global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
+__device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const GemmParams& p,
+                                                 const Unit& t, uint32_t dst, uint32_t bar, int kb) {
+  const int kc = (WK == kW_INT4) ? kb * 32 : (WK == kW_FP8 ? kb * 128 : kb * 64);
+  if (p.is_up)
+    tma_load_5d(dst, &maps.a, bar, kc, 0, 0, t.fb * 4, t.e);
+  else
+    tma_load_3d(dst, &maps.a, bar, kc, t.fb * 128, t.e);
+}
+
+template <int WK>
+__global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups : 192, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  const SmemLayout L = smem_layout(WK, p.bn_max, p.stages, p.E);
-  const uint32_t sA = base_u32 + L.a;
-  const uint32_t sB = base_u32 + L.b;
-  const uint32_t bstage = static_cast<uint32_t>(p.bn_max) * 128u;
-  const uint32_t bars = base_u32 + L.bars;
+  constexpr bool kInt4 = (WK == kW_INT4);
   const int ns = p.stages;
+  const int na = kInt4 ? p.astages : 0;
+  const SmemLayout L = smem_layout(WK, p.bn_max, ns, na, p.E);
+  const uint32_t sA = base_u32 + L.a;
+  const uint32_t sR = base_u32 + L.r;
+  const uint32_t bars = base_u32 + L.bars;
+  // ring barriers: FULL/EMPTY over `ns` stages; int4 adds AFULL/AEMPTY over `na`.
 #define FULL(s) (bars + 8u * static_cast<uint32_t>(s))
 #define EMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
-#define RAWFULL(s) (bars + 8u * static_cast<uint32_t>(2 * ns + (s)))
-  const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(3 * ns);
+#define AFULL(s) (bars + 8u * static_cast<uint32_t>(2 * ns + (s)))
+#define AEMPTY(s) (bars + 8u * static_cast<uint32_t>(2 * ns + na + (s)))
+  const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(2 * ns + 2 * na);
   const uint32_t tempty0 = tfull0 + 16u;
   const uint32_t drain_bar = tfull0 + 32u;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L.misc);
@@ -146,13 +191,20 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (kInt4 && (na < 2 || na > ns)) {  // host plans never do this; refuse rather than misbehave
+    if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);
+    return;
+  }
 
   // ---------------------------------------------------------------- prologue
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(FULL(s), WK == kW_INT4 ? 5u : 1u);  // int4: producer + 4 converter warps
+      mbar_init(FULL(s), 1u);
       mbar_init(EMPTY(s), 1u);
-      if (WK == kW_INT4) mbar_init(RAWFULL(s), 1u);
+    }
+    for (int s = 0; s < na; ++s) {
+      mbar_init(AFULL(s), 4u);  // the 4 warps of one converter group
+      mbar_init(AEMPTY(s), 1u);
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
@@ -163,6 +215,8 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
@@ -222,26 +276,17 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
             ok = false;
             break;
           }
-          const uint32_t bbytes = static_cast<uint32_t>(t.n) * 128u;
-          if (WK == kW_INT4) {
-            const uint32_t dst = base_u32 + L.raw + st * kRawBytes;
-            mbar_expect_tx(RAWFULL(st), kRawBytes);
-            if (p.is_up)
-              tma_load_5d(dst, &maps.a, RAWFULL(st), kb * 32, 0, 0, t.fb * 4, t.e);
-            else
-              tma_load_3d(dst, &maps.a, RAWFULL(st), kb * 32, t.fb * 128, t.e);
-            mbar_expect_tx(FULL(st), bbytes);
+          const uint32_t stage = sR + st * L.r_stride;
+          const uint32_t bbytes = static_cast<uint32_t>(p.full_box ? p.bn_max : t.n) * 128u;
+          if (kInt4) {
+            mbar_expect_tx(FULL(st), kRawBytes + bbytes);
+            load_weight_tile<WK>(maps, p, t, stage + L.r_raw, FULL(st), kb);
+            load_token_rows(maps, p, t, stage, FULL(st), kb * kelem_b);
           } else {
-            const int kelem = (WK == kW_FP8) ? 128 : 64;
             mbar_expect_tx(FULL(st), kABytes + bbytes);
-            if (p.is_up)
-              tma_load_5d(sA + st * kABytes, &maps.a, FULL(st), kb * kelem, 0, 0, t.fb * 4, t.e);
-            else
-              tma_load_3d(sA + st * kABytes, &maps.a, FULL(st), kb * kelem, t.fb * 128, t.e);
+            load_weight_tile<WK>(maps, p, t, sA + st * kABytes, FULL(st), kb);
+            load_token_rows(maps, p, t, stage, FULL(st), kb * kelem_b);
           }
-          for (int j = 0; j < (t.n >> 4); ++j)
-            tma_load_2d(sB + st * bstage + j * 2048u, &maps.b, FULL(st), kb * kelem_b,
-                        t.row0 + 16 * j);
           issued |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);
           if (++st == ns) {
@@ -253,21 +298,19 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
       if (!ok) {
         // Let loads already in flight land before the CTA exits.
         for (int s = 0; s < ns; ++s)
-          if ((issued >> s) & 1u)
-            mbar_wait(WK == kW_INT4 ? RAWFULL(s) : FULL(s), (issued_par >> s) & 1u, nullptr,
-                      p.err, 0x180u);
+          if ((issued >> s) & 1u) mbar_wait(FULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      uint32_t acc = 0, aph = 0;
+      int st = 0, as = 0;
+      uint32_t ph = 0, aph = 0;
+      uint32_t acc = 0, accph = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, tile_base, off, p);
-        if (!mbar_wait(tempty0 + 8u * acc, aph ^ 1u, abort_flag, p.err, 0x200u)) {
+        if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
           ok = false;
           break;
         }
@@ -275,13 +318,15 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
         const uint32_t d = tmem_base + acc * kAccCols;
         const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), WK == kW_FP8 ? 0u : 1u);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x210u)) {
+          // int4: the converted tile's barrier also covers the token rows (the
+          // converter group waited for the whole ring stage before converting).
+          if (!mbar_wait(kInt4 ? AFULL(as) : FULL(st), kInt4 ? aph : ph, abort_flag, p.err, 0x210u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(sA + st * kABytes);
-          const uint64_t bd = sw128_kmajor_desc(sB + st * bstage);
+          const uint64_t ad = sw128_kmajor_desc(kInt4 ? sA + as * kABytes : sA + st * kABytes);
+          const uint64_t bd = sw128_kmajor_desc(sR + st * L.r_stride);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kb > t.kb0 || kk > 0) ? 1u : 0u;
@@ -291,6 +336,13 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
               mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
           }
           mma_commit(EMPTY(st));
+          if (kInt4) {
+            mma_commit(AEMPTY(as));
+            if (++as == na) {
+              as = 0;
+              aph ^= 1u;
+            }
+          }
           any = true;
           if (++st == ns) {
             st = 0;
@@ -300,7 +352,7 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
         if (!ok) break;
         mma_commit(tfull0 + 8u * acc);
         acc ^= 1u;
-        if (acc == 0u) aph ^= 1u;
+        if (acc == 0u) accph ^= 1u;
       }
       if (!ok && any) {
         mma_commit(drain_bar);
@@ -311,10 +363,10 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     uint8_t* stg = base + L.stg + q * kStgBytesPerWarp;
-    uint32_t acc = 0, aph = 0;
+    uint32_t acc = 0, accph = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const Unit t = decode_unit(u, tile_base, off, p);
-      if (!mbar_wait(tfull0 + 8u * acc, aph, abort_flag, p.err, 0x300u)) break;
+      if (!mbar_wait(tfull0 + 8u * acc, accph, abort_flag, p.err, 0x300u)) break;
       tc_fence_after();
       float sc = 1.0f;
       if (WK == kW_FP8) sc = p.a_scale[0] * p.w_scale[t.e];
@@ -398,16 +450,18 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
       tc_fence_before();
       mbar_arrive(tempty0 + 8u * acc);
       acc ^= 1u;
-      if (acc == 0u) aph ^= 1u;
+      if (acc == 0u) accph ^= 1u;
     }
-  } else if (WK == kW_INT4) {
+  } else if (kInt4) {
     // --------------------------------------------- int4 -> bf16 tile converters
-    const int m = threadIdx.x - 192;  // A row of the tile, 0..127
-    const uint8_t* rawbase = base + L.raw;
-    uint8_t* abase = base + L.a;
+    // Two groups of 4 warps take alternate k-blocks; each thread owns one of
+    // the tile's 128 weight rows.
+    const int grp = (warp - 6) >> 2;
+    const int m = (threadIdx.x - 192) & 127;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
-    int st = 0;
-    uint32_t ph = 0;
+    int st = 0, as = 0;
+    uint32_t ph = 0, aph = 0;
+    uint32_t kcount = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit(u, tile_base, off, p);
@@ -415,31 +469,40 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 320 : 192, 1)
                                : (t.fb * 128 + m);
       const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
       for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(srow[kb >> 1]));
-        if (!mbar_wait(RAWFULL(st), ph, abort_flag, p.err, 0x400u)) {
-          ok = false;
-          break;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(rawbase + st * kRawBytes + m * 32);
-        const uint4 r0 = src[0], r1 = src[1];
-        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        uint8_t* arow = abase + st * kABytes + m * 128;
+        if (static_cast<int>(kcount & 1u) == grp) {
+          const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(srow[kb >> 1]));
+          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x400u) ||
+              !mbar_wait(AEMPTY(as), aph ^ 1u, abort_flag, p.err, 0x410u)) {
+            ok = false;
+            break;
+          }
+          const uint4* src = reinterpret_cast<const uint4*>(base + L.r + st * L.r_stride + L.r_raw + m * 32);
+          const uint4 r0 = src[0], r1 = src[1];
+          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          uint8_t* arow = base + L.a + as * kABytes + m * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = dequant8(w[j], s2);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(FULL(st));
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = dequant8(w[j], s2);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(AFULL(as));
+        }
+        ++kcount;
         if (++st == ns) {
           st = 0;
           ph ^= 1u;
+        }
+        if (++as == na) {
+          as = 0;
+          aph ^= 1u;
         }
       }
     }
   }
 #undef FULL
 #undef EMPTY
-#undef RAWFULL
+#undef AFULL
+#undef AEMPTY
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
@@ -469,11 +532,11 @@ cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size
 
 }  // namespace
 
-size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int E) {
-  return smem_layout(wkind, bn_max, stages, E).total;
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E) {
+  return smem_layout(wkind, bn_max, stages, astages, E).total;
 }
 
-int gemm_threads(int wkind) { return wkind == kW_INT4 ? 320 : 192; }
+int gemm_threads(int wkind) { return wkind == kW_INT4 ? 64 + 128 + 128 * kConvGroups : 192; }
 
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s) {

@@ -76,7 +76,9 @@ struct GemmParams {
   int KB;                  // k blocks of the reduction
   int P;                   // split-K factor
   int bn_max;              // token tile limit: multiple of 16, <= 256
-  int stages;
+  int stages;              // operand ring depth (int4: ring of packed A + token tiles)
+  int astages;             // int4 only: ring of converted bf16 A tiles
+  int full_box;            // 1: always load bn_max token rows (tuning)
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
@@ -84,11 +86,13 @@ struct GemmParams {
 };
 
 struct GemmMaps {
-  CUtensorMap a;  // weights (bf16/e4m3 swizzled tile, or packed int4 plain tile)
-  CUtensorMap b;  // token rows (x_perm or act)
+  CUtensorMap a;    // weights (bf16/e4m3 swizzled tile, or packed int4 plain tile)
+  CUtensorMap b;    // token rows (x_perm or act), box of bn_max rows: one load per full tile
+  CUtensorMap b64;  // the same rows, 64-row box (ragged last tile of an expert)
+  CUtensorMap b16;  // the same rows, 16-row box (ragged last tile of an expert)
 };
 
-size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int E);
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E);
 int gemm_threads(int wkind);
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s);

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 48
     assert ctypes.sizeof(binding.WeightsStruct) == 48
-    assert ctypes.sizeof(binding.Plan) == 28
+    assert ctypes.sizeof(binding.Plan) == 44
 
 
 def test_status_strings(lib):
@@ -108,3 +108,29 @@ def test_padded_capacity(lib):
     assert moe.padded_capacity(p, 2) == 8 + 4
     assert moe.padded_capacity(p, 1) == 8
     assert moe.padded_capacity(p, 0) == 0
+
+
+def _all_problems():
+    from synth import SHAPES, T_SWEEP
+    for s in SHAPES.values():
+        for T in (0,) + tuple(T_SWEEP) + (3, 37, 1000, 8192):
+            yield s, moe.problem(T, s.H, s.I, s.E, s.top_k, scoring=s.scoring, renormalize=s.renormalize,
+                                 n_group=s.n_group, topk_group=s.topk_group,
+                                 routed_scaling_factor=s.routed_scaling_factor, wdtype=s.wdtype)
+
+
+@pytest.mark.parametrize("sms", [148, 152, 160])
+def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
+    for shape, p in _all_problems():
+        pl = moe.get_plan(p, num_sms=sms)
+        for side in ("up", "down"):
+            bn = getattr(pl, f"bn_max_{side}")
+            assert 16 <= bn <= 256 and bn % 16 == 0
+            assert 1 <= getattr(pl, f"splits_{side}") <= 16
+            st, ast = getattr(pl, f"stages_{side}"), getattr(pl, f"astages_{side}")
+            assert st >= 2
+            assert getattr(pl, f"smem_{side}") <= 232448
+            if shape.wdtype == "int4":
+                assert 2 <= ast <= st      # converter groups never lap the operand ring
+            else:
+                assert ast == 0
