@@ -148,6 +148,28 @@ moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, 
                                int32_t* perm, int32_t* inv, void* x_perm, void* ws,
                                size_t ws_bytes, moe_stream_t stream);
 
+/* moe_align_permute without a workspace, for callers that are not allowed to
+ * allocate device memory: for instance a host framework that hands out no
+ * scratch buffer to a custom operator, or a serving loop that forbids
+ * cudaMalloc after start-up because it synchronises the device.  The pages
+ * have no counterpart: it is a packaging variant of stage 2 only.
+ *   Arguments and results are those of moe_align_permute minus ws/ws_bytes.
+ *   Its scratch (per-CTA expert histograms) is a fixed 256 KiB array in the
+ *   library's device image, one per device that loads the library, held until
+ *   the process exits.  Limit: ceil(T*k / 1024) * E <= 65536 (e.g. E = 256 up
+ *   to T*k = 262144); larger problems return MOE_ERR_UNSUPPORTED and launch
+ *   nothing.  No cudaMalloc/cudaFree or other allocation happens.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array: calls whose GPU work can overlap (e.g. on
+ *   two unsynchronised streams) race; order them.  Expert ids outside [0, E)
+ *   are still routed to expert 0 but are not reported (there is no error
+ *   header). */
+moe_status_t moe_align_permute_noalloc(const moe_problem_t* p, const int32_t* topk_ids,
+                                       const void* x, const float* a1_scale, int32_t* counts,
+                                       int32_t* offsets, int32_t* perm, int32_t* inv,
+                                       void* x_perm, moe_stream_t stream);
+
 /* Padded view of the sorted slots for a GEMM row block of `block` rows (the
  * layout moe_align_block_size produces, "[Kernel] add triton fused moe kernel
  * for gptq/awq", note 1).  Each expert's segment is padded up to a multiple of

@@ -22,7 +22,7 @@ SCORING = {"softmax": 0, "sigmoid": 1}
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "moe_gate_topk",
             "moe_align_permute", "moe_align_block_size", "moe_grouped_gemm_swiglu",
             "moe_grouped_gemm_down", "moe_unpermute_reduce", "moe_forward", "moe_get_device_error",
-            "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms")
+            "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms", "moe_align_permute_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "moe_gate_topk": (st, [P, vp, vp, vp, vp, vp]),
         "moe_align_permute": (st, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_align_block_size": (st, [P, vp, vp, i32, vp, vp, vp, vp]),
+        "moe_align_permute_noalloc": (st, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "moe_grouped_gemm_swiglu": (st, [P, ctypes.POINTER(WeightsStruct), vp, vp, vp, vp, sz, vp]),
         "moe_grouped_gemm_down": (st, [P, ctypes.POINTER(WeightsStruct), vp, vp, vp, vp, sz, vp]),
         "moe_unpermute_reduce": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
@@ -164,6 +165,14 @@ def align_permute(p: Problem, topk_ids, x, a1_scale, counts, offsets, perm, inv,
     _check(load().moe_align_permute(ctypes.byref(p), _ptr(topk_ids), _ptr(x), _ptr(a1_scale), _ptr(counts),
                                     _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm), _ptr(ws),
                                     ws.numel(), _stream(stream)), "moe_align_permute")
+
+
+def align_permute_noalloc(p: Problem, topk_ids, x, a1_scale, counts, offsets, perm, inv, x_perm, stream=None):
+    """moe_align_permute for callers that cannot allocate: no workspace argument;
+    the library's fixed device-side array holds the scratch (see include/moe.h)."""
+    _check(load().moe_align_permute_noalloc(ctypes.byref(p), _ptr(topk_ids), _ptr(x), _ptr(a1_scale),
+                                            _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv), _ptr(x_perm),
+                                            _stream(stream)), "moe_align_permute_noalloc")
 
 
 def align_block_size(p: Problem, offsets, perm, block, sorted_ids, block_expert, total_padded, stream=None):
