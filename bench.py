@@ -227,17 +227,22 @@ def run_ours(args):
     stream.synchronize()
     k_ms = g0.elapsed_time(g1) / reps
     up_flops = 2.0 * S * (2 * shape.I) * shape.H
-    up_bytes = touched * (2 * shape.I * shape.H * 2) + S * shape.H * 2 + S * shape.I * 2
-    t_tensor = up_flops / (bf16_peak * 1e12)
+    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0, "int4": 0.5 + 2.0 / shape.group_size}[shape.wdtype]
+    abytes = 1 if shape.wdtype == "fp8" else 2
+    up_bytes = touched * (2 * shape.I * shape.H * wbytes_per_elem) + S * shape.H * abytes + S * shape.I * abytes
+    tensor_peak = bf16_peak * (2.0 if shape.wdtype == "fp8" else 1.0)  # fp8: nominal 2x the measured bf16
+    t_tensor = up_flops / (tensor_peak * 1e12)
     t_hbm = up_bytes / (hbm * 1e9)
     if t_tensor >= t_hbm:
-        roof = {"bound": "tensor", "achieved": up_flops / (k_ms / 1e3) / 1e12, "peak": bf16_peak,
-                "unit": "TFLOP/s", "peak_kind": f"bf16 dense burst, {peak_src}"}
+        roof = {"bound": "tensor", "achieved": up_flops / (k_ms / 1e3) / 1e12, "peak": tensor_peak,
+                "unit": "TFLOP/s",
+                "peak_kind": ("fp8 dense = 2x bf16 dense burst, " if shape.wdtype == "fp8" else "bf16 dense burst, ")
+                + peak_src}
     else:
         roof = {"bound": "hbm", "achieved": up_bytes / (k_ms / 1e3) / 1e9, "peak": hbm,
                 "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = "grouped_gemm_kernel<bf16> (gate_up + SwiGLU)"
+    roof["kernel"] = ("grouped_gemm_w4_kernel" if shape.wdtype == "int4" else f"grouped_gemm_kernel<{shape.wdtype}>") + " (gate_up + SwiGLU)"
     roof["kernel_ms"] = k_ms
     roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
 

@@ -25,6 +25,8 @@ constexpr int kScatterWarps = kScatterThreads / 32;
 __global__ void __launch_bounds__(512) align_count_kernel(AlignArgs a) {
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int base = blockIdx.x * kAlignSlotsPerCta;
   const int end = min(a.S, base + kAlignSlotsPerCta);
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(kScatterThreads) align_scatter_kernel(AlignArg
   int* warp_sums = ctot + E;            // [32]
   uint16_t* wc = reinterpret_cast<uint16_t*>(warp_sums + 32);  // [warps][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
 
   for (int e = tid; e < E; e += kScatterThreads) {
     int tot = 0, before = 0;
@@ -157,6 +161,8 @@ template <bool FP8>
 __global__ void __launch_bounds__(256) gather_rows_kernel(AlignArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
+  pdl_wait();
+  pdl_trigger();
   if (r >= a.S) return;
   const int t = a.perm[r] / a.k;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
@@ -192,6 +198,8 @@ __global__ void __launch_bounds__(256)
                             int E, int S, int block, int32_t* sorted_ids, int32_t* block_expert,
                             int32_t* total_out) {
   extern __shared__ int poff[];  // [E + 1]
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < E; ++e) {
@@ -227,15 +235,14 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
     return cudaMemsetAsync(a.offsets, 0, sizeof(int32_t) * (a.E + 1), s);
   }
   const int nblk = align_blocks(a.S);
-  align_count_kernel<<<nblk, 512, sizeof(int) * a.E, s>>>(a);
+  cudaError_t err = launch_pdl(align_count_kernel, dim3(nblk), dim3(512), sizeof(int) * a.E, s, a);
+  if (err != cudaSuccess) return err;
   const size_t scatter_smem = sizeof(int) * (3 * a.E + 32) + sizeof(uint16_t) * kScatterWarps * a.E;
-  align_scatter_kernel<<<nblk, kScatterThreads, scatter_smem, s>>>(a, nblk);
+  err = launch_pdl(align_scatter_kernel, dim3(nblk), dim3(kScatterThreads), scatter_smem, s, a, nblk);
+  if (err != cudaSuccess) return err;
   const int gblocks = (a.S + 7) / 8;
-  if (a.fp8)
-    gather_rows_kernel<true><<<gblocks, 256, 0, s>>>(a);
-  else
-    gather_rows_kernel<false><<<gblocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a);
+  return launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm, int E, int S,
@@ -244,9 +251,8 @@ cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm,
   int grid = static_cast<int>((capacity + 255) / 256);
   if (grid < 1) grid = 1;
   if (grid > 1024) grid = 1024;
-  align_block_size_kernel<<<grid, 256, sizeof(int) * (E + 1), s>>>(offsets, perm, E, S, block,
-                                                                   sorted_ids, block_expert, total);
-  return cudaGetLastError();
+  return launch_pdl(align_block_size_kernel, dim3(grid), dim3(256), sizeof(int) * (E + 1), s, offsets,
+                    perm, E, S, block, sorted_ids, block_expert, total);
 }
 
 }  // namespace moe

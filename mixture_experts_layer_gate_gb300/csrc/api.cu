@@ -21,7 +21,7 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxStages = 8;
-constexpr int kMaxStagesInt4 = 16;
+constexpr int kMaxStagesInt4 = 8;
 constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
 constexpr size_t kMaxDynSmem = 232448;
 
@@ -113,7 +113,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, FB, KB;
+  int bn_max, P, stages, astages, conv_groups, acc_cols, FB, KB;
   size_t smem;
 };
 
@@ -130,13 +130,16 @@ int wkind_of(const moe_problem_t& p) {
 
 // Token tile limit: generous enough that one tile usually holds all of an
 // expert's tokens (each extra token block re-reads the expert's weights).
+// int4 keeps two accumulators and its converted weight tiles in TMEM, which
+// caps its token tile at 128 columns.
 int plan_bn_max(const moe_problem_t& p) {
   const long long S = static_cast<long long>(p.T) * p.top_k;
   if (S <= 0) return 16;
   const long long touched = std::max(1ll, std::min<long long>(p.E, S));
   const long long m_avg = (S + touched - 1) / touched;
   long long bn = std::max(3 * m_avg, m_avg + 24);
-  bn = std::min<long long>(256, std::max<long long>(16, bn));
+  const long long cap = (p.wdtype == MOE_W_INT4_G128) ? 128 : 256;
+  bn = std::min<long long>(cap, std::max<long long>(16, bn));
   return roundup16(static_cast<int>(bn));
 }
 
@@ -172,25 +175,26 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   const int wk = wkind_of(p);
   g.bn_max = plan_bn_max(p);
   const int bn_env = env_int("MOE_BN_MAX", 0);
-  if (bn_env >= 16 && bn_env <= 256 && bn_env % 16 == 0) g.bn_max = bn_env;
+  if (bn_env >= 16 && bn_env <= (wk == kW_INT4 ? 128 : 256) && bn_env % 16 == 0) g.bn_max = bn_env;
   g.FB = up ? p.I / 64 : p.H / 128;
   const int K = up ? p.H : p.I;
   g.KB = K / (wk == kW_FP8 ? 128 : 64);
   g.P = plan_splits(p, up, g.bn_max, g.KB, std::min(sms, kSmsForSizing));
   const int p_env = env_int("MOE_SPLITS", 0);
   if (p_env >= 1 && p_env <= kMaxSplits && p_env <= std::max(1, g.KB / 4)) g.P = p_env;
-  // Ring depth: as many stages as shared memory holds (capped).  int4 keeps a
-  // deep ring of packed weights + token rows and a short ring of converted
-  // bf16 weight tiles.
   size_t per_stage;
   int cap;
+  g.conv_groups = 0;
   if (wk == kW_INT4) {
-    g.astages = g.bn_max >= 128 ? 2 : 4;
-    const int as_env = env_int("MOE_ASTAGES", 0);
-    if (as_env >= 2 && as_env <= 12) g.astages = as_env;
-    per_stage = static_cast<size_t>(g.bn_max) * 128 + 4096 + 16;
+    // TMEM: two accumulators of acc_cols columns, then converted slots of 64
+    // columns (two k-blocks); at least 2 per converter group (parity-wait rule).
+    g.conv_groups = env_int("MOE_CONV_GROUPS", 2) == 1 ? 1 : 2;
+    g.acc_cols = (g.bn_max + 31) / 32 * 32;
+    g.astages = std::min(7, (512 - 2 * g.acc_cols) / 64);
+    per_stage = 16384 + 4 * static_cast<size_t>(g.bn_max) * 128 + 16;
     cap = kMaxStagesInt4;
   } else {
+    g.acc_cols = 256;
     g.astages = 0;
     per_stage = 16384 + static_cast<size_t>(g.bn_max) * 128 + 16;
     cap = kMaxStages;
@@ -201,15 +205,9 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
   while (g.stages > 2 && gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E) > kMaxDynSmem)
     --g.stages;
-  // int4: the converter groups wait on the operand ring with parity waits, so
-  // they must never run more than one ring phase ahead of it: the converted
-  // ring may not be deeper than the operand ring.
-  if (wk == kW_INT4 && g.astages > g.stages) {
-    g.astages = std::max(2, g.stages);
-    const size_t fixed2 = gemm_smem_bytes(wk, g.bn_max, 0, g.astages, p.E);
-    g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed2) / per_stage));
-    // (the kernel refuses a plan that still violates the rule instead of running it)
-  }
+  // int4: converter group g takes every conv_groups-th ring stage, so the ring
+  // depth must be a multiple of the group count (parity-wait rule).
+  if (wk == kW_INT4) g.stages -= g.stages % g.conv_groups;
   g.smem = gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E);
   return g;
 }
@@ -335,19 +333,18 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const uint64_t dimK = (wk == kW_BF16) ? H : Kb;
     uint64_t dims[5] = {dimK, 16, 2, I / 16, E};
     uint64_t str[4] = {Kb, I * Kb, 16 * Kb, 2 * I * Kb};
-    uint32_t box[5] = {wk == kW_INT4 ? 32u : (wk == kW_FP8 ? 128u : 64u), 16, 2, 4, 1};
+    // 128 bytes of each row per box: 64 bf16, 128 e4m3, or 256 int4 codes
+    uint32_t box[5] = {wk == kW_BF16 ? 64u : 128u, 16, 2, 4, 1};
     ok = encode_map(&maps.a, wk == kW_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                    5, wt.w13, dims, str, box,
-                    wk == kW_INT4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+                    5, wt.w13, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     const uint64_t Kb = (wk == kW_INT4) ? I / 2 : (wk == kW_FP8 ? I : I * 2);
     const uint64_t dimK = (wk == kW_BF16) ? I : Kb;
     uint64_t dims[3] = {dimK, H, E};
     uint64_t str[2] = {Kb, H * Kb};
-    uint32_t box[3] = {wk == kW_INT4 ? 32u : (wk == kW_FP8 ? 128u : 64u), 128, 1};
+    uint32_t box[3] = {wk == kW_BF16 ? 64u : 128u, 128, 1};
     ok = encode_map(&maps.a, wk == kW_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                    3, wt.w2, dims, str, box,
-                    wk == kW_INT4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
+                    3, wt.w2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (!ok) return MOE_ERR_CUDA;
   {
@@ -362,6 +359,14 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     for (int i = 0; i < 3; ++i) {
       uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
       if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
+    }
+    if (wk == kW_INT4) {
+      // full tiles: the token rows of 4 consecutive k-blocks in one box, viewed
+      // as [K/64][S][64] so each k-block lands as its own 128-byte-swizzled tile
+      uint64_t d3[3] = {64, static_cast<uint64_t>(S), K / 64};
+      uint64_t s3[2] = {K * 2, 128};
+      uint32_t b3[3] = {64, static_cast<uint32_t>(g.bn_max), 4};
+      if (!encode_map(&maps.b, dt, 3, in, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
     }
   }
 
@@ -381,11 +386,18 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.bn_max = g.bn_max;
   gp.stages = g.stages;
   gp.astages = g.astages;
+  gp.conv_groups = g.conv_groups;
+  gp.acc_cols = g.acc_cols;
   gp.full_box = env_int("MOE_FULL_BOX", 0) != 0 ? 1 : 0;
   gp.is_up = up ? 1 : 0;
   gp.R = up ? 2 * p.I : p.H;
   gp.G = up ? p.H / 128 : p.I / 128;
   float* part = at<float>(ws, L.partial);
+  {
+    const size_t N = up ? 2 * static_cast<size_t>(p.I) : static_cast<size_t>(p.H);
+    const size_t need = static_cast<size_t>(g.P) * S * N * sizeof(float);
+    if (g.P > 1 && need > L.scratch_end - L.partial) return MOE_ERR_UNSUPPORTED;  // plan/size mismatch
+  }
   if (g.P == 1) {
     gp.epi = up ? kEpiSwiglu : kEpiStore;
     gp.out = out;

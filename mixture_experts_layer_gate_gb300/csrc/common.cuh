@@ -10,6 +10,8 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
 
 // Sticky error word layout at the start of the workspace (256 bytes reserved):
@@ -69,13 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false if the
-// CTA-wide abort flag is raised or the wait runs past kWaitLimitNs (then it
-// raises the flag and records kErrTimeout with `info`).  A null abort flag makes
-// the wait ignore aborts (used while draining after an abort).
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       uint32_t* err, uint32_t info) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait (kept out of line so the fast path stays small).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag, uint32_t* err,
+                                                   uint32_t info) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -88,6 +87,17 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
       }
     }
   }
+}
+
+// Waits for the phase with the given parity to complete.  Returns false if the
+// CTA-wide abort flag is raised or the wait runs past kWaitLimitNs (then it
+// raises the flag and records kErrTimeout with `info`).  A null abort flag makes
+// the wait ignore aborts (used while draining after an abort).  The first probe
+// is inline: when the phase is already complete no call is made.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* err, uint32_t info) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, err, info);
 }
 
 // ----------------------------------------------------------------------- TMA
@@ -181,6 +191,35 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// Same as mma_f16 with the A operand read from tensor memory (row m in lane m,
+// two bf16 per 32-bit column, lower K index in the low half).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+      " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -225,9 +264,23 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it may start while the previous kernel on the stream is still
+// running.  It does only private set-up (shared memory, barriers, TMEM) before
+// pdl_wait(), which returns once the previous grid has completed and its
+// writes are visible; no global memory is read or written before that.
+// pdl_trigger() lets the next kernel start launching early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ numerics
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU with the hardware exponential and a fast (approximate) division: the
+// result is rounded to bf16 / e4m3 afterwards, far coarser than their error.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // Two floats -> two e4m3 codes (round to nearest even, saturate at +-448).
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
@@ -241,6 +294,23 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Launches `kernel` on `stream` with programmatic stream serialisation.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kGateWarps * 32) gate_topk_kernel(GateArgs a) 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kGateWarps + warp;
+  pdl_wait();
+  pdl_trigger();
   if (t >= a.T) return;  // whole warp leaves together
 
   const float* lrow = a.logits + static_cast<size_t>(t) * a.E;
@@ -183,13 +185,9 @@ cudaError_t launch_gate(const GateArgs& a, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
   const dim3 grid((a.T + kGateWarps - 1) / kGateWarps);
   const dim3 block(kGateWarps * 32);
-  if (a.E <= 64)
-    gate_topk_kernel<2><<<grid, block, 0, s>>>(a);
-  else if (a.E <= 256)
-    gate_topk_kernel<8><<<grid, block, 0, s>>>(a);
-  else
-    gate_topk_kernel<32><<<grid, block, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.E <= 64) return launch_pdl(gate_topk_kernel<2>, grid, block, 0, s, a);
+  if (a.E <= 256) return launch_pdl(gate_topk_kernel<8>, grid, block, 0, s, a);
+  return launch_pdl(gate_topk_kernel<32>, grid, block, 0, s, a);
 }
 
 }  // namespace moe

@@ -19,9 +19,13 @@
 //   * Warp roles: warp 0 issues TMA loads into a ring of shared-memory stages,
 //     warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5 drain
 //     the double-buffered accumulator (tcgen05.ld) and run the epilogue while
-//     the next unit accumulates.  For int4 weights warps 6..9 turn packed codes
-//     plus fp16 group scales into bf16 tiles in the 128-byte-swizzled layout
-//     the MMA reads.
+//     the next unit accumulates.
+//   * int4 weights (grouped_gemm_w4_kernel): each ring stage holds 4 k-blocks
+//     of packed codes (128 bytes per weight row, one TMA row request per 256
+//     K values) plus the 4 matching token tiles; converter warp groups turn the
+//     codes and fp16 group scales into bf16 and write them straight into TMEM
+//     (tcgen05.st), and the MMA reads its A operand from TMEM.  No converted
+//     tile passes through shared memory.
 //   * gate_up: the A tile holds 64 gate rows and the 64 matching up rows,
 //     interleaved in blocks of 16 (one 5-D TMA box), so SiLU(gate) * up pairs
 //     lanes l and l + 16 of the same warp in the epilogue.
@@ -34,20 +38,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kABytes = 16384;   // 128 rows x 128 B
-constexpr int kRawBytes = 4096;  // 128 rows x 32 B of packed int4
+constexpr int kABytes = 16384;    // 128 rows x 128 B (bf16 / e4m3 weight tile)
+constexpr int kRawBytes = 16384;  // int4: 128 rows x 128 B of packed codes = 4 k-blocks
+constexpr int kSuper = 4;         // int4: k-blocks per ring stage
 constexpr int kStgBytesPerWarp = 2048;
 constexpr int kStgBytes = 4 * kStgBytesPerWarp;
-constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kConvGroups = 2;   // int4: converter warp groups, alternating k-blocks
 
 // Shared-memory plan (offsets from a 1024-aligned base).
-//   bf16 / fp8 : ring of `stages` x {A tile 16 KB, B tile bn_max x 128 B}
-//   int4       : ring of `stages` x {B tile bn_max x 128 B, packed A 4 KB}
-//                plus ring of `astages` converted bf16 A tiles (16 KB each)
+//   bf16 / fp8 : ring of `stages` x {A tile 16 KB} then `stages` x {B tile bn_max x 128 B}
+//   int4       : ring of `stages` x {packed A 16 KB, 4 B tiles of bn_max x 128 B}
 struct SmemLayout {
-  uint32_t a, r, r_stride, r_raw, stg, bars, misc, tiles, total;
+  uint32_t a, r, r_stride, stg, bars, misc, tiles, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages, int astages,
@@ -56,18 +58,15 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
   uint32_t o = 0;
   const uint32_t bbytes = static_cast<uint32_t>(bn_max) * 128u;  // multiple of 2 KB
   if (wk == kW_INT4) {
-    L.a = o;
-    o += astages * kABytes;
+    L.a = 0;
     L.r = o;
-    L.r_stride = bbytes + kRawBytes;
-    L.r_raw = bbytes;
+    L.r_stride = kRawBytes + kSuper * bbytes;
     o += stages * L.r_stride;
   } else {
     L.a = o;
     o += stages * kABytes;
     L.r = o;
     L.r_stride = bbytes;
-    L.r_raw = 0;
     o += stages * bbytes;
   }
   L.stg = o;
@@ -111,6 +110,42 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   return t;
 }
 
+// Work-unit prefix over experts (run by one full warp): expert e owns
+// ceil(count_e / bn_max) * FB tiles; tile_base[E] is the total.
+__device__ void build_tile_table(const GemmParams& p, int lane, int* tile_base, int* off) {
+  const int per = (p.E + 31) / 32;
+  const int e0 = lane * per;
+  int local = 0;
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < p.E) {
+      const int c = p.offsets[e + 1] - p.offsets[e];
+      local += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - local;
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < p.E) {
+      const int o0 = p.offsets[e];
+      const int c = p.offsets[e + 1] - o0;
+      tile_base[e] = run;
+      off[e] = o0;
+      run += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+    }
+  }
+  if (lane == 31) {
+    tile_base[p.E] = incl;
+    off[p.E] = p.offsets[p.E];
+  }
+}
+
 // 8 packed int4 codes (low nibble first, two's complement) times a bf16 scale
 // -> 8 bf16.  0x4300 | v is the bf16 value 128 + v for v < 128; XOR 8 turns a
 // two's-complement nibble n into n + 8, so each half holds 136 + n exactly and
@@ -136,7 +171,7 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Issues the token-row loads of one k-block: a single box for a full tile,
+// Token-row loads of one k-block into a B tile: a single box for a full tile,
 // 64- and 16-row boxes for an expert's ragged last tile (few, large TMA
 // requests keep the pipe fed).
 __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const GemmParams& p,
@@ -152,6 +187,7 @@ __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const Gemm
   }
 }
 
+// Weight tile of k-block kb (bf16 / e4m3: 64 / 128 K) or super-block at kb (int4: 256 K).
 template <int WK>
 __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const GemmParams& p,
                                                  const Unit& t, uint32_t dst, uint32_t bar, int kb) {
@@ -162,23 +198,286 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
     tma_load_3d(dst, &maps.a, bar, kc, t.fb * 128, t.e);
 }
 
+// Epilogue role (warps 2..5): drains each unit's accumulator from TMEM and
+// writes act (SwiGLU), y_perm, or fp32 split-K partials.
 template <int WK>
-__global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups : 192, 1)
+__device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
+                                             int units, uint32_t tmem_base, uint32_t tfull0,
+                                             uint32_t tempty0, volatile int* abort_flag, uint8_t* stg_all,
+                                             int warp, int lane) {
+  const int q = warp & 3;  // TMEM lane quarter this warp may read
+  uint8_t* stg = stg_all + q * kStgBytesPerWarp;
+  uint32_t acc = 0, accph = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const Unit t = decode_unit(u, tile_base, off, p);
+    if (!mbar_wait(tfull0 + 8u * acc, accph, abort_flag, p.err, 0x300u)) break;
+    tc_fence_after();
+    float sc = 1.0f, inv_q = 1.0f;
+    if (WK == kW_FP8) {
+      sc = p.a_scale[0] * p.w_scale[t.e];
+      inv_q = 1.0f / p.q_scale[0];
+    }
+    const uint32_t tbase =
+        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_cols);
+    for (int c0 = 0; c0 < t.nvalid; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
+      tmem_ld_wait();
+      const int ntok = min(16, t.nvalid - c0);
+      const size_t row = static_cast<size_t>(t.row0 + c0);
+      if (p.epi == kEpiSwiglu) {
+        // lane l < 16: gate row of feature 16q + l; lane l + 16: its up row.
+        const bool upl = lane >= 16;
+        const int f16 = lane & 15;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float x = __uint_as_float(v[c]) * sc;
+          const float o = __shfl_xor_sync(0xffffffffu, x, 16);
+          if ((c & 1) == static_cast<int>(upl)) {
+            const float g = upl ? o : x;
+            const float uu = upl ? x : o;
+            const float a = silu_f32(g) * uu;
+            if (WK == kW_FP8)
+              stg[c * 16 + f16] = static_cast<uint8_t>(f32x2_to_e4m3x2(a * inv_q, 0.f) & 0xFF);
+            else
+              reinterpret_cast<__nv_bfloat16*>(stg)[c * 16 + f16] = __float2bfloat16_rn(a);
+          }
+        }
+        __syncwarp();
+        const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16;
+        if (WK == kW_FP8) {
+          if (lane < ntok)
+            *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row + lane) * p.out_ld + col) =
+                *reinterpret_cast<const uint4*>(stg + lane * 16);
+        } else {
+          const int tok = lane >> 1, half = lane & 1;
+          if (tok < ntok)
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
+                                      col + half * 8) =
+                *reinterpret_cast<const uint4*>(stg + tok * 32 + half * 16);
+        }
+      } else if (p.epi == kEpiStore) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          reinterpret_cast<__nv_bfloat16*>(stg)[c * 32 + lane] =
+              __float2bfloat16_rn(__uint_as_float(v[c]) * sc);
+        __syncwarp();
+        const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32;
+#pragma unroll
+        for (int i = lane; i < 64; i += 32) {
+          const int tok = i >> 2, part = i & 3;
+          if (tok < ntok)
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
+                                      col + part * 8) =
+                *reinterpret_cast<const uint4*>(stg + tok * 64 + part * 16);
+        }
+      } else {  // fp32 split-K partials
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          reinterpret_cast<float*>(stg)[c * 32 + lane] = __uint_as_float(v[c]) * sc;
+        __syncwarp();
+        float* dst0 = static_cast<float*>(p.out) + static_cast<size_t>(t.sp) * p.part_stride;
+#pragma unroll
+        for (int i = lane; i < 128; i += 32) {
+          const int tok = i >> 3, w8 = i & 7;
+          if (tok < ntok) {
+            size_t col;
+            if (p.is_up)
+              col = static_cast<size_t>((w8 >> 2) * p.I) + static_cast<size_t>(t.fb) * 64 + q * 16 +
+                    (w8 & 3) * 4;
+            else
+              col = static_cast<size_t>(t.fb) * 128 + q * 32 + w8 * 4;
+            *reinterpret_cast<float4*>(dst0 + (row + tok) * p.out_ld + col) =
+                *reinterpret_cast<const float4*>(stg + tok * 128 + w8 * 16);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    tc_fence_before();
+    mbar_arrive(tempty0 + 8u * acc);
+    acc ^= 1u;
+    if (acc == 0u) accph ^= 1u;
+  }
+}
+
+// ------------------------------------------------------------------ bf16 / fp8
+
+template <int WK>
+__global__ void __launch_bounds__(192, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  constexpr bool kInt4 = (WK == kW_INT4);
   const int ns = p.stages;
-  const int na = kInt4 ? p.astages : 0;
-  const SmemLayout L = smem_layout(WK, p.bn_max, ns, na, p.E);
+  const SmemLayout L = smem_layout(WK, p.bn_max, ns, 0, p.E);
   const uint32_t sA = base_u32 + L.a;
   const uint32_t sR = base_u32 + L.r;
   const uint32_t bars = base_u32 + L.bars;
-  // ring barriers: FULL/EMPTY over `ns` stages; int4 adds AFULL/AEMPTY over `na`.
 #define FULL(s) (bars + 8u * static_cast<uint32_t>(s))
 #define EMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
+  const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(2 * ns);
+  const uint32_t tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tfull0 + 32u;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.misc + 4);
+  int* tile_base = reinterpret_cast<int*>(base + L.tiles);
+  int* off = tile_base + (p.E + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(FULL(s), 1u);
+      mbar_init(EMPTY(s), 1u);
+    }
+    mbar_init(tfull0, 1u);
+    mbar_init(tfull0 + 8u, 1u);
+    mbar_init(tempty0, 128u);
+    mbar_init(tempty0 + 8u, 128u);
+    mbar_init(drain_bar, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b16);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish();
+  }
+  pdl_wait();  // offsets, tokens and (for gate_up) x_perm come from earlier kernels
+  if (warp == 2) build_tile_table(p, lane, tile_base, off);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = tile_base[p.E] * p.P;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int kelem_b = (WK == kW_FP8) ? 128 : 64;
+      int st = 0;
+      uint32_t ph = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tile_base, off, p);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(EMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bbytes = static_cast<uint32_t>(p.full_box ? p.bn_max : t.n) * 128u;
+          mbar_expect_tx(FULL(st), kABytes + bbytes);
+          load_weight_tile<WK>(maps, p, t, sA + st * kABytes, FULL(st), kb);
+          load_token_rows(maps, p, t, sR + st * L.r_stride, FULL(st), kb * kelem_b);
+          issued |= 1u << st;
+          issued_par = (issued_par & ~(1u << st)) | (ph << st);
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let loads already in flight land before the CTA exits.
+        for (int s = 0; s < ns; ++s)
+          if ((issued >> s) & 1u) mbar_wait(FULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t ph = 0, acc = 0, accph = 0;
+      bool ok = true, any = false;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, tile_base, off, p);
+        if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * static_cast<uint32_t>(p.acc_cols);
+        const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), WK == kW_FP8 ? 0u : 1u);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x210u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(sA + st * kABytes);
+          const uint64_t bd = sw128_kmajor_desc(sR + st * L.r_stride);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t accum = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+            if (WK == kW_FP8)
+              mma_f8(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+            else
+              mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+          }
+          mma_commit(EMPTY(st));
+          any = true;
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8u * acc);
+        acc ^= 1u;
+        if (acc == 0u) accph ^= 1u;
+      }
+      if (!ok && any) {
+        mma_commit(drain_bar);
+        mbar_wait(drain_bar, 0u, nullptr, p.err, 0x280u);
+      }
+    }
+  } else {
+    run_epilogue<WK>(p, tile_base, off, units, tmem_base, tfull0, tempty0, abort_flag, base + L.stg,
+                     warp, lane);
+  }
+#undef FULL
+#undef EMPTY
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------ int4
+//
+// Rings and the parity-wait rules they obey (a parity wait is unambiguous only
+// if the waiter is never two phases ahead of the barrier):
+//   RFULL/REMPTY over `stages` ring stages of 4 k-blocks (packed codes + token
+//   tiles).  Converter group g takes every CG-th stage; `stages` is a multiple
+//   of CG, so the previous use of a slot was by the same group.
+//   AFULL/AEMPTY over `astages` TMEM slots of 128 x 128 bf16 (64 columns),
+//   one per pair of k-blocks (one wait and one commit per 8 MMAs);
+//   astages >= 2*CG, so a group that filled its previous slot is at most one
+//   phase ahead of any slot it waits on.
+template <int CG>
+__global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
+    grouped_gemm_w4_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const int ns = p.stages;
+  const int na = p.astages;
+  const SmemLayout L = smem_layout(kW_INT4, p.bn_max, ns, na, p.E);
+  const uint32_t sR = base_u32 + L.r;
+  const uint32_t btile = static_cast<uint32_t>(p.bn_max) * 128u;
+  const uint32_t bars = base_u32 + L.bars;
+#define RFULL(s) (bars + 8u * static_cast<uint32_t>(s))
+#define REMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
 #define AFULL(s) (bars + 8u * static_cast<uint32_t>(2 * ns + (s)))
 #define AEMPTY(s) (bars + 8u * static_cast<uint32_t>(2 * ns + na + (s)))
   const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(2 * ns + 2 * na);
@@ -188,19 +487,19 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.misc + 4);
   int* tile_base = reinterpret_cast<int*>(base + L.tiles);
   int* off = tile_base + (p.E + 1);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (kInt4 && (na < 2 || na > ns)) {  // host plans never do this; refuse rather than misbehave
-    if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);
+  const uint32_t acc_cols = static_cast<uint32_t>(p.acc_cols);
+  const uint32_t a_col0 = 2u * acc_cols;  // TMEM column of converted slot 0
+  if (na < 2 * CG || ns % CG != 0 || a_col0 + 64u * static_cast<uint32_t>(na) > kTmemCols) {
+    if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
     return;
   }
 
-  // ---------------------------------------------------------------- prologue
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(FULL(s), 1u);
-      mbar_init(EMPTY(s), 1u);
+      mbar_init(RFULL(s), 1u);
+      mbar_init(REMPTY(s), 1u);
     }
     for (int s = 0; s < na; ++s) {
       mbar_init(AFULL(s), 4u);  // the 4 warps of one converter group
@@ -222,70 +521,48 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 2) {
-    // Work-unit prefix over experts: expert e owns ceil(count_e / bn_max) * FB tiles.
-    const int per = (p.E + 31) / 32;
-    const int e0 = lane * per;
-    int local = 0;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
-      if (e < p.E) {
-        const int c = p.offsets[e + 1] - p.offsets[e];
-        local += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
-      }
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
-      if (e < p.E) {
-        const int o0 = p.offsets[e];
-        const int c = p.offsets[e + 1] - o0;
-        tile_base[e] = run;
-        off[e] = o0;
-        run += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
-      }
-    }
-    if (lane == 31) {
-      tile_base[p.E] = incl;
-      off[p.E] = p.offsets[p.E];
-    }
-  }
+  pdl_wait();
+  if (warp == 2) build_tile_table(p, lane, tile_base, off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const int units = tile_base[p.E] * p.P;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int kelem_b = (WK == kW_FP8) ? 128 : 64;
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, tile_base, off, p);
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!mbar_wait(EMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
+        for (int kbs = t.kb0; kbs < t.kb1; kbs += kSuper) {
+          const int nk = min(kSuper, t.kb1 - kbs);
+          if (!mbar_wait(REMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
             ok = false;
             break;
           }
           const uint32_t stage = sR + st * L.r_stride;
-          const uint32_t bbytes = static_cast<uint32_t>(p.full_box ? p.bn_max : t.n) * 128u;
-          if (kInt4) {
-            mbar_expect_tx(FULL(st), kRawBytes + bbytes);
-            load_weight_tile<WK>(maps, p, t, stage + L.r_raw, FULL(st), kb);
-            load_token_rows(maps, p, t, stage, FULL(st), kb * kelem_b);
+          const bool full = (t.n == p.bn_max);
+          const uint32_t bbytes = full ? kSuper * btile : static_cast<uint32_t>(nk * t.n) * 128u;
+          mbar_expect_tx(RFULL(st), kRawBytes + bbytes);
+          load_weight_tile<kW_INT4>(maps, p, t, stage, RFULL(st), kbs);
+          if (full) {
+            tma_load_3d(stage + kRawBytes, &maps.b, RFULL(st), 0, t.row0, kbs);
           } else {
-            mbar_expect_tx(FULL(st), kABytes + bbytes);
-            load_weight_tile<WK>(maps, p, t, sA + st * kABytes, FULL(st), kb);
-            load_token_rows(maps, p, t, stage, FULL(st), kb * kelem_b);
+            // ragged last tile of an expert: 64- and 16-row boxes per k-block
+            for (int j = 0; j < nk; ++j) {
+              const uint32_t dst = stage + kRawBytes + j * btile;
+              int r = 0;
+              for (; r + 64 <= t.n; r += 64)
+                tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, RFULL(st), (kbs + j) * 64,
+                            t.row0 + r);
+              for (; r < t.n; r += 16)
+                tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, RFULL(st), (kbs + j) * 64,
+                            t.row0 + r);
+            }
           }
           issued |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -296,17 +573,15 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
         }
       }
       if (!ok) {
-        // Let loads already in flight land before the CTA exits.
         for (int s = 0; s < ns; ++s)
-          if ((issued >> s) & 1u) mbar_wait(FULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
+          if ((issued >> s) & 1u) mbar_wait(RFULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int st = 0, as = 0;
-      uint32_t ph = 0, aph = 0;
-      uint32_t acc = 0, accph = 0;
+      uint32_t ph = 0, aph = 0, acc = 0, accph = 0;
       bool ok = true, any = false;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, tile_base, off, p);
@@ -315,35 +590,38 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * kAccCols;
-        const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), WK == kW_FP8 ? 0u : 1u);
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          // int4: the converted tile's barrier also covers the token rows (the
-          // converter group waited for the whole ring stage before converting).
-          if (!mbar_wait(kInt4 ? AFULL(as) : FULL(st), kInt4 ? aph : ph, abort_flag, p.err, 0x210u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t ad = sw128_kmajor_desc(kInt4 ? sA + as * kABytes : sA + st * kABytes);
-          const uint64_t bd = sw128_kmajor_desc(sR + st * L.r_stride);
+        const uint32_t d = tmem_base + acc * acc_cols;
+        const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), 1u);
+        for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
+          const int nk = min(kSuper, t.kb1 - kbs);
+          const uint32_t bstage = sR + st * L.r_stride + kRawBytes;
+          for (int jp = 0; jp < nk; jp += 2) {
+            // the converted slot's barrier also covers the stage's token rows:
+            // its converter group waited for the whole stage before converting
+            if (!mbar_wait(AFULL(as), aph, abort_flag, p.err, 0x210u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_tmem = tmem_base + a_col0 + 64u * static_cast<uint32_t>(as);
+            for (int jj = 0; jj < 2 && jp + jj < nk; ++jj) {
+              const int j = jp + jj;
+              const uint64_t bd = sw128_kmajor_desc(bstage + j * btile);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t accum = (kb > t.kb0 || kk > 0) ? 1u : 0u;
-            if (WK == kW_FP8)
-              mma_f8(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
-            else
-              mma_f16(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
-          }
-          mma_commit(EMPTY(st));
-          if (kInt4) {
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t accum = (kbs + j > t.kb0 || kk > 0) ? 1u : 0u;
+                mma_f16_tmem_a(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
+              }
+            }
             mma_commit(AEMPTY(as));
+            any = true;
             if (++as == na) {
               as = 0;
               aph ^= 1u;
             }
           }
-          any = true;
+          if (!ok) break;
+          mma_commit(REMPTY(st));
           if (++st == ns) {
             st = 0;
             ph ^= 1u;
@@ -360,151 +638,93 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
       }
     }
   } else if (warp < 6) {
-    // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    uint8_t* stg = base + L.stg + q * kStgBytesPerWarp;
-    uint32_t acc = 0, accph = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const Unit t = decode_unit(u, tile_base, off, p);
-      if (!mbar_wait(tfull0 + 8u * acc, accph, abort_flag, p.err, 0x300u)) break;
-      tc_fence_after();
-      float sc = 1.0f;
-      if (WK == kW_FP8) sc = p.a_scale[0] * p.w_scale[t.e];
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-      for (int c0 = 0; c0 < t.nvalid; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
-        tmem_ld_wait();
-        const int ntok = min(16, t.nvalid - c0);
-        const size_t row = static_cast<size_t>(t.row0 + c0);
-        if (p.epi == kEpiSwiglu) {
-          // lane l < 16: gate row of feature 16q + l; lane l + 16: its up row.
-          const bool upl = lane >= 16;
-          const int f16 = lane & 15;
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float x = __uint_as_float(v[c]) * sc;
-            const float o = __shfl_xor_sync(0xffffffffu, x, 16);
-            if ((c & 1) == static_cast<int>(upl)) {
-              const float g = upl ? o : x;
-              const float uu = upl ? x : o;
-              const float a = silu_f32(g) * uu;
-              if (WK == kW_FP8)
-                stg[c * 16 + f16] =
-                    static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(a, p.q_scale[0]), 0.f) & 0xFF);
-              else
-                reinterpret_cast<__nv_bfloat16*>(stg)[c * 16 + f16] = __float2bfloat16_rn(a);
-            }
-          }
-          __syncwarp();
-          const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16;
-          if (WK == kW_FP8) {
-            if (lane < ntok)
-              *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row + lane) * p.out_ld + col) =
-                  *reinterpret_cast<const uint4*>(stg + lane * 16);
-          } else {
-            const int tok = lane >> 1, half = lane & 1;
-            if (tok < ntok)
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
-                                        col + half * 8) =
-                  *reinterpret_cast<const uint4*>(stg + tok * 32 + half * 16);
-          }
-        } else if (p.epi == kEpiStore) {
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            reinterpret_cast<__nv_bfloat16*>(stg)[c * 32 + lane] =
-                __float2bfloat16_rn(__uint_as_float(v[c]) * sc);
-          __syncwarp();
-          const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32;
-#pragma unroll
-          for (int i = lane; i < 64; i += 32) {
-            const int tok = i >> 2, part = i & 3;
-            if (tok < ntok)
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
-                                        col + part * 8) =
-                  *reinterpret_cast<const uint4*>(stg + tok * 64 + part * 16);
-          }
-        } else {  // fp32 split-K partials
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            reinterpret_cast<float*>(stg)[c * 32 + lane] = __uint_as_float(v[c]) * sc;
-          __syncwarp();
-          float* dst0 = static_cast<float*>(p.out) + static_cast<size_t>(t.sp) * p.part_stride;
-#pragma unroll
-          for (int i = lane; i < 128; i += 32) {
-            const int tok = i >> 3, w8 = i & 7;
-            if (tok < ntok) {
-              size_t col;
-              if (p.is_up)
-                col = static_cast<size_t>((w8 >> 2) * p.I) + static_cast<size_t>(t.fb) * 64 + q * 16 +
-                      (w8 & 3) * 4;
-              else
-                col = static_cast<size_t>(t.fb) * 128 + q * 32 + w8 * 4;
-              *reinterpret_cast<float4*>(dst0 + (row + tok) * p.out_ld + col) =
-                  *reinterpret_cast<const float4*>(stg + tok * 128 + w8 * 16);
-            }
-          }
-        }
-        __syncwarp();
-      }
-      tc_fence_before();
-      mbar_arrive(tempty0 + 8u * acc);
-      acc ^= 1u;
-      if (acc == 0u) accph ^= 1u;
-    }
-  } else if (kInt4) {
-    // --------------------------------------------- int4 -> bf16 tile converters
-    // Two groups of 4 warps take alternate k-blocks; each thread owns one of
-    // the tile's 128 weight rows.
+    run_epilogue<kW_INT4>(p, tile_base, off, units, tmem_base, tfull0, tempty0, abort_flag,
+                          base + L.stg, warp, lane);
+  } else {
+    // --------------------------------------------- int4 -> bf16 converters
+    // Group g (4 warps) converts ring stages g, g + CG, ...; the thread owns
+    // weight row m of the tile, which is TMEM lane m of the converted tile.
     const int grp = (warp - 6) >> 2;
-    const int m = (threadIdx.x - 192) & 127;
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
+    const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
     int st = 0, as = 0;
     uint32_t ph = 0, aph = 0;
-    uint32_t kcount = 0;
+    uint32_t scount = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit(u, tile_base, off, p);
       const int grow = p.is_up ? (((m >> 4) & 1) * p.I + t.fb * 64 + (m >> 5) * 16 + (m & 15))
                                : (t.fb * 128 + m);
       const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
-      for (int kb = t.kb0; kb < t.kb1; ++kb) {
-        if (static_cast<int>(kcount & 1u) == grp) {
-          const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(srow[kb >> 1]));
-          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x400u) ||
-              !mbar_wait(AEMPTY(as), aph ^ 1u, abort_flag, p.err, 0x410u)) {
+      for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
+        const int nk = min(kSuper, t.kb1 - kbs);
+        if (static_cast<int>(scount % CG) == grp) {
+          __half sc[kSuper];
+#pragma unroll
+          for (int j = 0; j < kSuper; ++j) sc[j] = srow[min(kbs + j, t.kb1 - 1) >> 1];
+          if (!mbar_wait(RFULL(st), ph, abort_flag, p.err, 0x400u)) {
             ok = false;
             break;
           }
-          const uint4* src = reinterpret_cast<const uint4*>(base + L.r + st * L.r_stride + L.r_raw + m * 32);
-          const uint4 r0 = src[0], r1 = src[1];
-          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-          uint8_t* arow = base + L.a + as * kABytes + m * 128;
+          const uint8_t* rrow = base + L.r + st * L.r_stride + m * 128;
+          int a = as;
+          uint32_t ap = aph;
+          for (int jp = 0; jp < nk; jp += 2) {
+            if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int jj = 0; jj < 2 && jp + jj < nk; ++jj) {
+              const int j = jp + jj;
+              const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
+              // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
+              const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
+              const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
+              const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+              uint32_t outv[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(arow + ((j ^ (m & 7)) << 4)) = dequant8(w[j], s2);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(AFULL(as));
+              for (int i = 0; i < 8; ++i) {
+                const uint4 o = dequant8(w[i], s2);
+                outv[4 * i + 0] = o.x;
+                outv[4 * i + 1] = o.y;
+                outv[4 * i + 2] = o.z;
+                outv[4 * i + 3] = o.w;
+              }
+              tmem_st32(tmem_base + tlane + a_col0 + 64u * static_cast<uint32_t>(a) + 32u * jj, outv);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(AFULL(a));
+            if (++a == na) {
+              a = 0;
+              ap ^= 1u;
+            }
+          }
         }
-        ++kcount;
+        // every group keeps the same ring and slot counters
+        for (int jp = 0; jp < nk; jp += 2) {
+          if (++as == na) {
+            as = 0;
+            aph ^= 1u;
+          }
+        }
+        ++scount;
         if (++st == ns) {
           st = 0;
           ph ^= 1u;
         }
-        if (++as == na) {
-          as = 0;
-          aph ^= 1u;
-        }
       }
     }
   }
-#undef FULL
-#undef EMPTY
+#undef RFULL
+#undef REMPTY
 #undef AFULL
 #undef AEMPTY
 
-  // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -513,21 +733,36 @@ __global__ void __launch_bounds__(WK == kW_INT4 ? 64 + 128 + 128 * kConvGroups :
   }
 }
 
-template <int WK>
-cudaError_t launch_one(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
-                       cudaStream_t s) {
-  static int configured_device = -1;  // attribute set once per device (single-device processes)
+template <typename K>
+cudaError_t set_smem_attr(K kernel, int* configured_device) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (configured_device != dev) {
-    err = cudaFuncSetAttribute(grouped_gemm_kernel<WK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               232448);
+  if (*configured_device != dev) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (err != cudaSuccess) return err;
-    configured_device = dev;
+    *configured_device = dev;
   }
-  grouped_gemm_kernel<WK><<<grid, gemm_threads(WK), smem, s>>>(maps, p);
-  return cudaGetLastError();
+  return cudaSuccess;
+}
+
+template <int WK>
+cudaError_t launch_dense(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                         cudaStream_t s) {
+  static int configured = -1;  // attribute set once per device (single-device processes)
+  cudaError_t err = set_smem_attr(grouped_gemm_kernel<WK>, &configured);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(grouped_gemm_kernel<WK>, dim3(grid), dim3(192), smem, s, maps, p);
+}
+
+template <int CG>
+cudaError_t launch_w4(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                      cudaStream_t s) {
+  static int configured = -1;
+  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG>, &configured);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(grouped_gemm_w4_kernel<CG>, dim3(grid), dim3(gemm_threads(kW_INT4, CG)), smem, s,
+                    maps, p);
 }
 
 }  // namespace
@@ -536,17 +771,21 @@ size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E) {
   return smem_layout(wkind, bn_max, stages, astages, E).total;
 }
 
-int gemm_threads(int wkind) { return wkind == kW_INT4 ? 64 + 128 + 128 * kConvGroups : 192; }
+int gemm_threads(int wkind, int conv_groups) {
+  return wkind == kW_INT4 ? 64 + 128 + 128 * conv_groups : 192;
+}
 
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s) {
   switch (wkind) {
     case kW_BF16:
-      return launch_one<kW_BF16>(maps, p, grid, smem, s);
+      return launch_dense<kW_BF16>(maps, p, grid, smem, s);
     case kW_FP8:
-      return launch_one<kW_FP8>(maps, p, grid, smem, s);
+      return launch_dense<kW_FP8>(maps, p, grid, smem, s);
     case kW_INT4:
-      return launch_one<kW_INT4>(maps, p, grid, smem, s);
+      if (p.conv_groups == 2) return launch_w4<2>(maps, p, grid, smem, s);
+      if (p.conv_groups == 1) return launch_w4<1>(maps, p, grid, smem, s);
+      return cudaErrorInvalidValue;
     default:
       return cudaErrorInvalidValue;
   }

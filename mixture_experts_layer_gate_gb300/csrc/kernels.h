@@ -79,6 +79,8 @@ struct GemmParams {
   int stages;              // operand ring depth (int4: ring of packed A + token tiles)
   int astages;             // int4 only: ring of converted bf16 A tiles
   int full_box;            // 1: always load bn_max token rows (tuning)
+  int conv_groups;         // int4 only: converter warp groups (2 or 4)
+  int acc_cols;            // TMEM columns per accumulator buffer
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
@@ -86,14 +88,16 @@ struct GemmParams {
 };
 
 struct GemmMaps {
-  CUtensorMap a;    // weights (bf16/e4m3 swizzled tile, or packed int4 plain tile)
+  CUtensorMap a;    // weights: bf16/e4m3 tile of 128 rows x 128 B, or for int4 128 rows x
+                    // 128 B of packed codes (4 k-blocks); 128-byte swizzle
   CUtensorMap b;    // token rows (x_perm or act), box of bn_max rows: one load per full tile
+                    // (int4: 3-D view [k-block][row][64], box of 4 k-blocks)
   CUtensorMap b64;  // the same rows, 64-row box (ragged last tile of an expert)
   CUtensorMap b16;  // the same rows, 16-row box (ragged last tile of an expert)
 };
 
 size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E);
-int gemm_threads(int wkind);
+int gemm_threads(int wkind, int conv_groups);
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s);
 

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256)
                             const float* __restrict__ w, int H, int k, __nv_bfloat16* out) {
   const int t = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (c * 8 >= H) return;
   float acc[8];
 #pragma unroll
@@ -49,6 +51,8 @@ __global__ void __launch_bounds__(256)
                          const float* __restrict__ a2, void* act) {
   const int r = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (c * 4 >= I) return;
   const float* row = part + static_cast<size_t>(r) * (2 * static_cast<size_t>(I));
   float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
@@ -78,6 +82,8 @@ __global__ void __launch_bounds__(256)
                        __nv_bfloat16* y) {
   const int r = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (c * 4 >= H) return;
   const float* row = part + static_cast<size_t>(r) * H;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -95,28 +101,25 @@ cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, cons
                                     int H, int k, void* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const dim3 grid((H / 8 + 255) / 256, T);
-  unpermute_reduce_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(y_perm), inv, w,
-                                              H, k, static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+  return launch_pdl(unpermute_reduce_kernel, grid, dim3(256), 0, s,
+                    static_cast<const __nv_bfloat16*>(y_perm), inv, w, H, k,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
                                  const float* a2, int fp8, void* act, cudaStream_t s) {
   if (S == 0) return cudaSuccess;
   const dim3 grid((I / 4 + 255) / 256, S);
-  if (fp8)
-    swiglu_finish_kernel<true><<<grid, 256, 0, s>>>(part, P, pstride, I, a2, act);
-  else
-    swiglu_finish_kernel<false><<<grid, 256, 0, s>>>(part, P, pstride, I, a2, act);
-  return cudaGetLastError();
+  if (fp8) return launch_pdl(swiglu_finish_kernel<true>, grid, dim3(256), 0, s, part, P, pstride, I, a2, act);
+  return launch_pdl(swiglu_finish_kernel<false>, grid, dim3(256), 0, s, part, P, pstride, I, a2, act);
 }
 
 cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H, void* y,
                                cudaStream_t s) {
   if (S == 0) return cudaSuccess;
   const dim3 grid((H / 4 + 255) / 256, S);
-  down_finish_kernel<<<grid, 256, 0, s>>>(part, P, pstride, H, static_cast<__nv_bfloat16*>(y));
-  return cudaGetLastError();
+  return launch_pdl(down_finish_kernel, grid, dim3(256), 0, s, part, P, pstride, H,
+                    static_cast<__nv_bfloat16*>(y));
 }
 
 }  // namespace moe

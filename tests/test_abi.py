@@ -131,6 +131,10 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             assert st >= 2
             assert getattr(pl, f"smem_{side}") <= 232448
             if shape.wdtype == "int4":
-                assert 2 <= ast <= st      # converter groups never lap the operand ring
+                # TMEM holds two accumulators and >= 4 converted tiles per converter
+                # group (2 groups); the ring depth is a multiple of the group count
+                assert bn <= 128
+                assert 4 <= ast <= 7 and 2 * ((bn + 31) // 32 * 32) + 64 * ast <= 512
+                assert st % 2 == 0
             else:
                 assert ast == 0
