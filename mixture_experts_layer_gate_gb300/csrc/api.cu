@@ -20,7 +20,7 @@ namespace {
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 8;  // bf16 / fp8 operand ring
 constexpr int kMaxStagesInt4 = 8;
 constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
 constexpr size_t kMaxDynSmem = 232448;
@@ -113,7 +113,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, conv_groups, acc_cols, FB, KB;
+  int bn_max, P, stages, astages, conv_groups, acc_cols, pair, FB, KB;
   size_t smem;
 };
 
@@ -185,6 +185,12 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   size_t per_stage;
   int cap;
   g.conv_groups = 0;
+  // bf16 / fp8: CTA pairs (M = 256 per MMA) whenever the weight blocks pair up.
+  g.pair = 0;
+  if (wk != kW_INT4 && g.FB % 2 == 0 && env_int("MOE_PAIR", 1) != 0) {
+    g.pair = 1;
+    g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
+  }
   if (wk == kW_INT4) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of 64
     // columns (two k-blocks); at least 2 per converter group (parity-wait rule).
@@ -196,19 +202,21 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   } else {
     g.acc_cols = 256;
     g.astages = 0;
-    per_stage = 16384 + static_cast<size_t>(g.bn_max) * 128 + 16;
+    per_stage = 16384 + static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStages;
   }
-  const size_t fixed = gemm_smem_bytes(wk, g.bn_max, 0, g.astages, p.E);
+  // rows of token tile each CTA stages per K step
+  const int brows = g.pair ? g.bn_max / 2 : g.bn_max;
+  const size_t fixed = gemm_smem_bytes(wk, brows, 0, g.astages, p.E);
   g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed) / per_stage));
   const int st_env = env_int("MOE_STAGES", 0);
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
-  while (g.stages > 2 && gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E) > kMaxDynSmem)
+  while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E) > kMaxDynSmem)
     --g.stages;
   // int4: converter group g takes every conv_groups-th ring stage, so the ring
   // depth must be a multiple of the group count (parity-wait rule).
   if (wk == kW_INT4) g.stages -= g.stages % g.conv_groups;
-  g.smem = gemm_smem_bytes(wk, g.bn_max, g.stages, g.astages, p.E);
+  g.smem = gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E);
   return g;
 }
 
@@ -355,7 +363,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     uint64_t str[1] = {K * (f8 ? 1 : 2)};
     const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap* dst[3] = {&maps.b, &maps.b64, &maps.b16};
-    const uint32_t rows[3] = {static_cast<uint32_t>(g.bn_max), 64u, 16u};
+    const uint32_t rows[3] = {static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 64u, 16u};
     for (int i = 0; i < 3; ++i) {
       uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
       if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
@@ -380,7 +388,8 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.E = p.E;
   gp.S = S;
   gp.I = p.I;
-  gp.FB = g.FB;
+  gp.FB = g.pair ? g.FB / 2 : g.FB;
+  gp.pair = g.pair;
   gp.KB = g.KB;
   gp.P = g.P;
   gp.bn_max = g.bn_max;

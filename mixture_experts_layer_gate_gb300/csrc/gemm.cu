@@ -175,41 +175,48 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
 // 64- and 16-row boxes for an expert's ragged last tile (few, large TMA
 // requests keep the pipe fed).
 __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const GemmParams& p,
-                                                const Unit& t, uint32_t dst, uint32_t bar, int kcoord) {
+                                                const Unit& t, uint32_t dst, uint32_t bar, int kcoord,
+                                                uint64_t pol) {
   if (t.n == p.bn_max || p.full_box) {
-    tma_load_2d(dst, &maps.b, bar, kcoord, t.row0);
+    tma_load_2d_hint(dst, &maps.b, bar, kcoord, t.row0, pol);
   } else {
     int r = 0;
     for (; r + 64 <= t.n; r += 64)
-      tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, t.row0 + r);
+      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, t.row0 + r, pol);
     for (; r < t.n; r += 16)
-      tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, t.row0 + r);
+      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, t.row0 + r, pol);
   }
 }
 
 // Weight tile of k-block kb (bf16 / e4m3: 64 / 128 K) or super-block at kb (int4: 256 K).
 template <int WK>
 __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const GemmParams& p,
-                                                 const Unit& t, uint32_t dst, uint32_t bar, int kb) {
+                                                 const Unit& t, uint32_t dst, uint32_t bar, int kb,
+                                                 uint64_t pol) {
   const int kc = (WK == kW_INT4) ? kb * 32 : (WK == kW_FP8 ? kb * 128 : kb * 64);
   if (p.is_up)
-    tma_load_5d(dst, &maps.a, bar, kc, 0, 0, t.fb * 4, t.e);
+    tma_load_5d_hint(dst, &maps.a, bar, kc, 0, 0, t.fb * 4, t.e, pol);
   else
-    tma_load_3d(dst, &maps.a, bar, kc, t.fb * 128, t.e);
+    tma_load_3d_hint(dst, &maps.a, bar, kc, t.fb * 128, t.e, pol);
 }
 
 // Epilogue role (warps 2..5): drains each unit's accumulator from TMEM and
 // writes act (SwiGLU), y_perm, or fp32 split-K partials.
+// Units are taken from `first` in steps of `stride`; `pair_rank` >= 0 marks a
+// CTA-pair kernel (this CTA's rows are weight block 2*fb + rank); the arrival
+// that frees an accumulator goes, one per warp, to the shared::cluster address
+// `tempty_cl0` (+8 for buffer 1).
 template <int WK>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
-                                             int units, uint32_t tmem_base, uint32_t tfull0,
-                                             uint32_t tempty0, volatile int* abort_flag, uint8_t* stg_all,
-                                             int warp, int lane) {
+                                             int units, int first, int stride, int pair_rank,
+                                             uint32_t tmem_base, uint32_t tfull0, uint32_t tempty_cl0,
+                                             volatile int* abort_flag, uint8_t* stg_all, int warp, int lane) {
   const int q = warp & 3;  // TMEM lane quarter this warp may read
   uint8_t* stg = stg_all + q * kStgBytesPerWarp;
   uint32_t acc = 0, accph = 0;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const Unit t = decode_unit(u, tile_base, off, p);
+  for (int u = first; u < units; u += stride) {
+    Unit t = decode_unit(u, tile_base, off, p);
+    if (pair_rank >= 0) t.fb = 2 * t.fb + pair_rank;
     if (!mbar_wait(tfull0 + 8u * acc, accph, abort_flag, p.err, 0x300u)) break;
     tc_fence_after();
     float sc = 1.0f, inv_q = 1.0f;
@@ -295,7 +302,8 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       __syncwarp();
     }
     tc_fence_before();
-    mbar_arrive(tempty0 + 8u * acc);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(tempty_cl0 + 8u * acc);
     acc ^= 1u;
     if (acc == 0u) accph ^= 1u;
   }
@@ -334,8 +342,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
-    mbar_init(tempty0, 128u);
-    mbar_init(tempty0 + 8u, 128u);
+    mbar_init(tempty0, 4u);  // one arrival per epilogue warp
+    mbar_init(tempty0 + 8u, 4u);
     mbar_init(drain_bar, 1u);
     *abort_flag = 0;
     fence_mbar_init();
@@ -361,6 +369,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int kelem_b = (WK == kW_FP8) ? 128 : 64;
+      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
@@ -373,8 +382,8 @@ __global__ void __launch_bounds__(192, 1)
           }
           const uint32_t bbytes = static_cast<uint32_t>(p.full_box ? p.bn_max : t.n) * 128u;
           mbar_expect_tx(FULL(st), kABytes + bbytes);
-          load_weight_tile<WK>(maps, p, t, sA + st * kABytes, FULL(st), kb);
-          load_token_rows(maps, p, t, sR + st * L.r_stride, FULL(st), kb * kelem_b);
+          load_weight_tile<WK>(maps, p, t, sA + st * kABytes, FULL(st), kb, pol_w);
+          load_token_rows(maps, p, t, sR + st * L.r_stride, FULL(st), kb * kelem_b, pol_t);
           issued |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);
           if (++st == ns) {
@@ -438,8 +447,8 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    run_epilogue<WK>(p, tile_base, off, units, tmem_base, tfull0, tempty0, abort_flag, base + L.stg,
-                     warp, lane);
+    run_epilogue<WK>(p, tile_base, off, units, blockIdx.x, gridDim.x, -1, tmem_base, tfull0,
+                     map_to_rank(tempty0, cluster_ctarank()), abort_flag, base + L.stg, warp, lane);
   }
 #undef FULL
 #undef EMPTY
@@ -449,6 +458,187 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------- bf16 / fp8, CTA pairs
+//
+// A cluster of two CTAs shares one tcgen05.mma.cta_group::2 per K step: each
+// CTA stages its own 128 weight rows (A) and half of the tile's token rows (B),
+// the leader (rank 0) issues M = 256 MMAs over both CTAs' shared memory, and
+// each CTA's TMEM receives its 128 rows of the accumulator.  Per CTA the
+// operand traffic per K step falls from 16 KB + N x 128 B to 16 KB + N x 64 B.
+//   FULL (leader only): both CTAs' TMA loads count on the leader's barrier, the
+//   leader's producer posts the expected bytes of both.
+//   EMPTY (both): the leader's commit arrives on both CTAs' barrier.
+//   tfull (both) / tempty (leader, one arrival per epilogue warp of each CTA).
+template <int WK>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const int ns = p.stages;
+  const int half_max = p.bn_max / 2;  // token rows per CTA of a full tile
+  const SmemLayout L = smem_layout(WK, half_max, ns, 0, p.E);
+  const uint32_t sA = base_u32 + L.a;
+  const uint32_t sR = base_u32 + L.r;
+  const uint32_t bars = base_u32 + L.bars;
+#define FULL(s) (bars + 8u * static_cast<uint32_t>(s))
+#define EMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
+  const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(2 * ns);
+  const uint32_t tempty0 = tfull0 + 16u;
+  const uint32_t drain_bar = tfull0 + 32u;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.misc + 4);
+  int* tile_base = reinterpret_cast<int*>(base + L.tiles);
+  int* off = tile_base + (p.E + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(FULL(s), 1u);
+      mbar_init(EMPTY(s), 1u);
+    }
+    mbar_init(tfull0, 1u);
+    mbar_init(tfull0 + 8u, 1u);
+    mbar_init(tempty0, 8u);  // 4 epilogue warps in each CTA of the pair
+    mbar_init(tempty0 + 8u, 8u);
+    mbar_init(drain_bar, 1u);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&maps.a);
+    tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b16);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  pdl_wait();
+  if (warp == 2) build_tile_table(p, lane, tile_base, off);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = tile_base[p.E] * p.P;
+  const int first = static_cast<int>(cluster_id_x());
+  const int stride = static_cast<int>(num_clusters_x());
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const int kelem = (WK == kW_FP8) ? 128 : 64;
+      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = first; u < units && ok; u += stride) {
+        Unit t = decode_unit(u, tile_base, off, p);
+        const int fb = 2 * t.fb + static_cast<int>(rank);
+        const int n = (t.nvalid + 31) & ~31;
+        const int half = n >> 1;
+        const int r0 = t.row0 + static_cast<int>(rank) * half;
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(EMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_cl = map_to_rank(FULL(st), 0);
+          if (leader) mbar_expect_tx(FULL(st), 2u * (kABytes + static_cast<uint32_t>(half) * 128u));
+          const uint32_t adst = sA + st * kABytes;
+          if (p.is_up)
+            tma_load_5d_pair(adst, &maps.a, full_cl, kb * kelem, 0, 0, fb * 4, t.e, pol_w);
+          else
+            tma_load_3d_pair(adst, &maps.a, full_cl, kb * kelem, fb * 128, t.e, pol_w);
+          const uint32_t bdst = sR + st * L.r_stride;
+          if (half == half_max) {
+            tma_load_2d_pair(bdst, &maps.b, full_cl, kb * kelem, r0, pol_t);
+          } else {
+            int r = 0;
+            for (; r + 64 <= half; r += 64)
+              tma_load_2d_pair(bdst + static_cast<uint32_t>(r) * 128u, &maps.b64, full_cl, kb * kelem, r0 + r, pol_t);
+            for (; r < half; r += 16)
+              tma_load_2d_pair(bdst + static_cast<uint32_t>(r) * 128u, &maps.b16, full_cl, kb * kelem, r0 + r, pol_t);
+          }
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // (after an abort, loads already issued complete into this CTA's own
+      // shared memory; the final cluster barrier keeps both CTAs resident)
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      int st = 0;
+      uint32_t ph = 0, acc = 0, accph = 0;
+      bool ok = true, any = false;
+      for (int u = first; u < units && ok; u += stride) {
+        const Unit t = decode_unit(u, tile_base, off, p);
+        const int n = (t.nvalid + 31) & ~31;
+        if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * static_cast<uint32_t>(p.acc_cols);
+        const uint32_t idesc = make_idesc(256u, static_cast<uint32_t>(n), WK == kW_FP8 ? 0u : 1u);
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+          if (!mbar_wait(FULL(st), ph, abort_flag, p.err, 0x210u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_kmajor_desc(sA + st * kABytes);
+          const uint64_t bd = sw128_kmajor_desc(sR + st * L.r_stride);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t accum = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+            if (WK == kW_FP8)
+              mma_f8_pair(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+            else
+              mma_f16_pair(d, ad + 2u * kk, bd + 2u * kk, idesc, accum);
+          }
+          mma_commit_pair(EMPTY(st), 0x3);
+          any = true;
+          if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull0 + 8u * acc, 0x3);
+        acc ^= 1u;
+        if (acc == 0u) accph ^= 1u;
+      }
+      if (!ok && any) {
+        mma_commit_pair(drain_bar, 0x1);
+        mbar_wait(drain_bar, 0u, nullptr, p.err, 0x280u);
+      }
+    }
+  } else {
+    run_epilogue<WK>(p, tile_base, off, units, first, stride, static_cast<int>(rank), tmem_base, tfull0,
+                     map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
+  }
+#undef FULL
+#undef EMPTY
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no signals into either CTA remain in flight
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -507,8 +697,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
-    mbar_init(tempty0, 128u);
-    mbar_init(tempty0 + 8u, 128u);
+    mbar_init(tempty0, 4u);  // one arrival per epilogue warp
+    mbar_init(tempty0 + 8u, 4u);
     mbar_init(drain_bar, 1u);
     *abort_flag = 0;
     fence_mbar_init();
@@ -533,6 +723,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
@@ -548,20 +739,20 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           const bool full = (t.n == p.bn_max);
           const uint32_t bbytes = full ? kSuper * btile : static_cast<uint32_t>(nk * t.n) * 128u;
           mbar_expect_tx(RFULL(st), kRawBytes + bbytes);
-          load_weight_tile<kW_INT4>(maps, p, t, stage, RFULL(st), kbs);
+          load_weight_tile<kW_INT4>(maps, p, t, stage, RFULL(st), kbs, pol_w);
           if (full) {
-            tma_load_3d(stage + kRawBytes, &maps.b, RFULL(st), 0, t.row0, kbs);
+            tma_load_3d_hint(stage + kRawBytes, &maps.b, RFULL(st), 0, t.row0, kbs, pol_t);
           } else {
             // ragged last tile of an expert: 64- and 16-row boxes per k-block
             for (int j = 0; j < nk; ++j) {
               const uint32_t dst = stage + kRawBytes + j * btile;
               int r = 0;
               for (; r + 64 <= t.n; r += 64)
-                tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, RFULL(st), (kbs + j) * 64,
-                            t.row0 + r);
+                tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, RFULL(st),
+                                 (kbs + j) * 64, t.row0 + r, pol_t);
               for (; r < t.n; r += 16)
-                tma_load_2d(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, RFULL(st), (kbs + j) * 64,
-                            t.row0 + r);
+                tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, RFULL(st),
+                                 (kbs + j) * 64, t.row0 + r, pol_t);
             }
           }
           issued |= 1u << st;
@@ -638,8 +829,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       }
     }
   } else if (warp < 6) {
-    run_epilogue<kW_INT4>(p, tile_base, off, units, tmem_base, tfull0, tempty0, abort_flag,
-                          base + L.stg, warp, lane);
+    run_epilogue<kW_INT4>(p, tile_base, off, units, blockIdx.x, gridDim.x, -1, tmem_base, tfull0,
+                          map_to_rank(tempty0, cluster_ctarank()), abort_flag, base + L.stg, warp, lane);
   } else {
     // --------------------------------------------- int4 -> bf16 converters
     // Group g (4 warps) converts ring stages g, g + CG, ...; the thread owns
@@ -755,6 +946,15 @@ cudaError_t launch_dense(const GemmMaps& maps, const GemmParams& p, int grid, si
   return launch_pdl(grouped_gemm_kernel<WK>, dim3(grid), dim3(192), smem, s, maps, p);
 }
 
+template <int WK>
+cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                        cudaStream_t s) {
+  static int configured = -1;
+  cudaError_t err = set_smem_attr(grouped_gemm_pair_kernel<WK>, &configured);
+  if (err != cudaSuccess) return err;
+  return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
+}
+
 template <int CG>
 cudaError_t launch_w4(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
                       cudaStream_t s) {
@@ -779,9 +979,9 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
                                 size_t smem, cudaStream_t s) {
   switch (wkind) {
     case kW_BF16:
-      return launch_dense<kW_BF16>(maps, p, grid, smem, s);
+      return p.pair ? launch_pair<kW_BF16>(maps, p, grid, smem, s) : launch_dense<kW_BF16>(maps, p, grid, smem, s);
     case kW_FP8:
-      return launch_dense<kW_FP8>(maps, p, grid, smem, s);
+      return p.pair ? launch_pair<kW_FP8>(maps, p, grid, smem, s) : launch_dense<kW_FP8>(maps, p, grid, smem, s);
     case kW_INT4:
       if (p.conv_groups == 2) return launch_w4<2>(maps, p, grid, smem, s);
       if (p.conv_groups == 1) return launch_w4<1>(maps, p, grid, smem, s);

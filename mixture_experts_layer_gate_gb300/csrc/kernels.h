@@ -81,6 +81,7 @@ struct GemmParams {
   int full_box;            // 1: always load bn_max token rows (tuning)
   int conv_groups;         // int4 only: converter warp groups (2 or 4)
   int acc_cols;            // TMEM columns per accumulator buffer
+  int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
