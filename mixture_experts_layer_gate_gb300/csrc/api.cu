@@ -390,6 +390,16 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.I = p.I;
   gp.FB = g.pair ? g.FB / 2 : g.FB;
   gp.pair = g.pair;
+  {
+    // weights are streamed (read once) when one token tile is expected to hold
+    // all of an expert's rows; otherwise several tiles reuse them through L2
+    const long long Sl = static_cast<long long>(p.T) * p.top_k;
+    const long long touched = std::max(1ll, std::min<long long>(p.E, Sl));
+    const long long m_avg = (Sl + touched - 1) / touched;
+    gp.w_stream = (m_avg <= g.bn_max) ? 1 : 0;
+    const int ws_env = env_int("MOE_W_STREAM", -1);
+    if (ws_env == 0 || ws_env == 1) gp.w_stream = ws_env;
+  }
   gp.KB = g.KB;
   gp.P = g.P;
   gp.bn_max = g.bn_max;

@@ -226,10 +226,18 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
     }
     const uint32_t tbase =
         tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_cols);
-    for (int c0 = 0; c0 < t.nvalid; c0 += 16) {
-      uint32_t v[16];
-      tmem_ld16(tbase + static_cast<uint32_t>(c0), v);
+    for (int cb = 0; cb < t.nvalid; cb += 32) {
+      // two 16-column loads in flight, one wait
+      uint32_t vv[2][16];
+      const bool two = cb + 16 < t.nvalid;  // warp-uniform
+      tmem_ld16(tbase + static_cast<uint32_t>(cb), vv[0]);
+      if (two) tmem_ld16(tbase + static_cast<uint32_t>(cb + 16), vv[1]);
       tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+      if (h == 1 && !two) break;
+      const int c0 = cb + 16 * h;
+      const uint32_t (&v)[16] = vv[h];
       const int ntok = min(16, t.nvalid - c0);
       const size_t row = static_cast<size_t>(t.row0 + c0);
       if (p.epi == kEpiSwiglu) {
@@ -301,6 +309,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       }
       __syncwarp();
     }
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(tempty_cl0 + 8u * acc);
@@ -369,7 +378,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int kelem_b = (WK == kW_FP8) ? 128 : 64;
-      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
+      const uint64_t pol_w = p.w_stream ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_t = l2_policy_evict_last();
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
@@ -536,7 +546,8 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       const int kelem = (WK == kW_FP8) ? 128 : 64;
-      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
+      const uint64_t pol_w = p.w_stream ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_t = l2_policy_evict_last();
       int st = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -723,7 +734,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first(), pol_t = l2_policy_evict_last();
+      const uint64_t pol_w = p.w_stream ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_t = l2_policy_evict_last();
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;

@@ -82,6 +82,7 @@ struct GemmParams {
   int conv_groups;         // int4 only: converter warp groups (2 or 4)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
+  int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
