@@ -187,17 +187,20 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   g.conv_groups = 0;
   // bf16 / fp8: CTA pairs (M = 256 per MMA) whenever the weight blocks pair up.
   g.pair = 0;
-  if (wk != kW_INT4 && g.FB % 2 == 0 && env_int("MOE_PAIR", 1) != 0) {
+  if (g.FB % 2 == 0 && env_int("MOE_PAIR", 1) != 0) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
   if (wk == kW_INT4) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of 64
     // columns (two k-blocks); at least 2 per converter group (parity-wait rule).
-    g.conv_groups = env_int("MOE_CONV_GROUPS", 2) == 1 ? 1 : 2;
     g.acc_cols = (g.bn_max + 31) / 32 * 32;
     g.astages = std::min(7, (512 - 2 * g.acc_cols) / 64);
-    per_stage = 16384 + 4 * static_cast<size_t>(g.bn_max) * 128 + 16;
+    // three converter groups (CTA pairs) when TMEM holds >= 6 converted slots
+    g.conv_groups = (g.pair && g.astages >= 6) ? 3 : 2;
+    const int cg_env = env_int("MOE_CONV_GROUPS", 0);
+    if (cg_env == 1 || cg_env == 2 || (cg_env == 3 && g.pair && g.astages >= 6)) g.conv_groups = cg_env;
+    per_stage = 16384 + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStagesInt4;
   } else {
     g.acc_cols = 256;
@@ -373,7 +376,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
       // as [K/64][S][64] so each k-block lands as its own 128-byte-swizzled tile
       uint64_t d3[3] = {64, static_cast<uint64_t>(S), K / 64};
       uint64_t s3[2] = {K * 2, 128};
-      uint32_t b3[3] = {64, static_cast<uint32_t>(g.bn_max), 4};
+      uint32_t b3[3] = {64, static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 4};
       if (!encode_map(&maps.b, dt, 3, in, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
     }
   }

@@ -147,20 +147,21 @@ __device__ void build_tile_table(const GemmParams& p, int lane, int* tile_base, 
 }
 
 // 8 packed int4 codes (low nibble first, two's complement) times a bf16 scale
-// -> 8 bf16.  0x4300 | v is the bf16 value 128 + v for v < 128; XOR 8 turns a
-// two's-complement nibble n into n + 8, so each half holds 136 + n exactly and
-// subtracting 136 recovers n before the scale multiply.
+// -> 8 bf16 in k order.  One byte permute of (x, x >> 4) puts the nibbles of
+// k = 2i and 2i + 1 at the bottom of the low and high halves; masking those
+// nibbles and flipping bit 3 gives v + 8 there, and OR-ing the bf16 pattern
+// 0x4300 (= 128) makes each half the exact bf16 value 136 + v (mask, flip and
+// OR fold into one three-input logic op).  Subtracting 136 recovers v
+// exactly; the scale multiply rounds once.  Integer-pipe work is the cost that
+// matters here (bf16x2 arithmetic is far cheaper), hence 9 integer ops per
+// 8 codes.
 __device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
-  x ^= 0x88888888u;
-  const uint32_t p04 = (x & 0x000F000Fu) | 0x43004300u;
-  const uint32_t p15 = ((x >> 4) & 0x000F000Fu) | 0x43004300u;
-  const uint32_t p26 = ((x >> 8) & 0x000F000Fu) | 0x43004300u;
-  const uint32_t p37 = ((x >> 12) & 0x000F000Fu) | 0x43004300u;
+  const uint32_t xs = x >> 4;
   uint32_t o[4];
-  o[0] = __byte_perm(p04, p15, 0x5410);  // k0, k1
-  o[1] = __byte_perm(p26, p37, 0x5410);  // k2, k3
-  o[2] = __byte_perm(p04, p15, 0x7632);  // k4, k5
-  o[3] = __byte_perm(p26, p37, 0x7632);  // k6, k7
+  o[0] = (__byte_perm(x, xs, 0x4400) & 0x000F000Fu) ^ 0x43084308u;  // k0, k1
+  o[1] = (__byte_perm(x, xs, 0x5511) & 0x000F000Fu) ^ 0x43084308u;  // k2, k3
+  o[2] = (__byte_perm(x, xs, 0x6622) & 0x000F000Fu) ^ 0x43084308u;  // k4, k5
+  o[3] = (__byte_perm(x, xs, 0x7733) & 0x000F000Fu) ^ 0x43084308u;  // k6, k7
   const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -664,7 +665,11 @@ __global__ void __launch_bounds__(192, 1)
 //   one per pair of k-blocks (one wait and one commit per 8 MMAs);
 //   astages >= 2*CG, so a group that filled its previous slot is at most one
 //   phase ahead of any slot it waits on.
-template <int CG>
+// PAIR: the kernel runs as clusters of two CTAs sharing M = 256 MMAs, each CTA
+// converting its own 128 weight rows into its own TMEM and staging half of the
+// token rows; converter groups of both CTAs report to the leader's AFULL, the
+// leader's commits are multicast to both CTAs.
+template <int CG, bool PAIR>
 __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     grouped_gemm_w4_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -673,9 +678,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const int ns = p.stages;
   const int na = p.astages;
-  const SmemLayout L = smem_layout(kW_INT4, p.bn_max, ns, na, p.E);
+  const int brows = PAIR ? p.bn_max / 2 : p.bn_max;  // token rows this CTA stages per k-block
+  const SmemLayout L = smem_layout(kW_INT4, brows, ns, na, p.E);
   const uint32_t sR = base_u32 + L.r;
-  const uint32_t btile = static_cast<uint32_t>(p.bn_max) * 128u;
+  const uint32_t btile = static_cast<uint32_t>(brows) * 128u;
   const uint32_t bars = base_u32 + L.bars;
 #define RFULL(s) (bars + 8u * static_cast<uint32_t>(s))
 #define REMPTY(s) (bars + 8u * static_cast<uint32_t>(ns + (s)))
@@ -692,6 +698,9 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t acc_cols = static_cast<uint32_t>(p.acc_cols);
   const uint32_t a_col0 = 2u * acc_cols;  // TMEM column of converted slot 0
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = (rank == 0);
+  constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   if (na < 2 * CG || ns % CG != 0 || a_col0 + 64u * static_cast<uint32_t>(na) > kTmemCols) {
     if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
     return;
@@ -703,13 +712,13 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       mbar_init(REMPTY(s), 1u);
     }
     for (int s = 0; s < na; ++s) {
-      mbar_init(AFULL(s), 4u);  // the 4 warps of one converter group
+      mbar_init(AFULL(s), 4u * kCtas);  // the 4 warps of one converter group (in each CTA)
       mbar_init(AEMPTY(s), 1u);
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
-    mbar_init(tempty0, 4u);  // one arrival per epilogue warp
-    mbar_init(tempty0 + 8u, 4u);
+    mbar_init(tempty0, 4u * kCtas);  // one arrival per epilogue warp (of each CTA)
+    mbar_init(tempty0 + 8u, 4u * kCtas);
     mbar_init(drain_bar, 1u);
     *abort_flag = 0;
     fence_mbar_init();
@@ -719,17 +728,25 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+      tmem_relinquish();
+    }
   }
   pdl_wait();
   if (warp == 2) build_tile_table(p, lane, tile_base, off);
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const int units = tile_base[p.E] * p.P;
+  const int first = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int stride = PAIR ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -739,8 +756,15 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       int st = 0;
       uint32_t ph = 0, issued = 0, issued_par = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, tile_base, off, p);
+      for (int u = first; u < units && ok; u += stride) {
+        Unit t = decode_unit(u, tile_base, off, p);
+        if (PAIR) {
+          // this CTA: weight block 2*fb + rank, token rows [row0 + rank*n/2, + n/2)
+          t.fb = 2 * t.fb + static_cast<int>(rank);
+          const int n = (t.nvalid + 31) & ~31;
+          t.n = n >> 1;
+          t.row0 += static_cast<int>(rank) * t.n;
+        }
         for (int kbs = t.kb0; kbs < t.kb1; kbs += kSuper) {
           const int nk = min(kSuper, t.kb1 - kbs);
           if (!mbar_wait(REMPTY(st), ph ^ 1u, abort_flag, p.err, 0x100u)) {
@@ -748,7 +772,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             break;
           }
           const uint32_t stage = sR + st * L.r_stride;
-          const bool full = (t.n == p.bn_max);
+          const bool full = (t.n == brows);
           const uint32_t bbytes = full ? kSuper * btile : static_cast<uint32_t>(nk * t.n) * 128u;
           mbar_expect_tx(RFULL(st), kRawBytes + bbytes);
           load_weight_tile<kW_INT4>(maps, p, t, stage, RFULL(st), kbs, pol_w);
@@ -782,11 +806,11 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int st = 0, as = 0;
       uint32_t ph = 0, aph = 0, acc = 0, accph = 0;
       bool ok = true, any = false;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = first; u < units && ok; u += stride) {
         const Unit t = decode_unit(u, tile_base, off, p);
         if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
           ok = false;
@@ -794,7 +818,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * acc_cols;
-        const uint32_t idesc = make_idesc(128u, static_cast<uint32_t>(t.n), 1u);
+        const uint32_t n_mma = PAIR ? static_cast<uint32_t>((t.nvalid + 31) & ~31) : static_cast<uint32_t>(t.n);
+        const uint32_t idesc = make_idesc(PAIR ? 256u : 128u, n_mma, 1u);
         for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
           const int nk = min(kSuper, t.kb1 - kbs);
           const uint32_t bstage = sR + st * L.r_stride + kRawBytes;
@@ -813,10 +838,13 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t accum = (kbs + j > t.kb0 || kk > 0) ? 1u : 0u;
-                mma_f16_tmem_a(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
+                if (PAIR)
+                  mma_f16_tmem_a_pair(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
+                else
+                  mma_f16_tmem_a(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
               }
             }
-            mma_commit(AEMPTY(as));
+            if (PAIR) mma_commit_pair(AEMPTY(as), 0x3); else mma_commit(AEMPTY(as));
             any = true;
             if (++as == na) {
               as = 0;
@@ -824,25 +852,25 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             }
           }
           if (!ok) break;
-          mma_commit(REMPTY(st));
+          if (PAIR) mma_commit_pair(REMPTY(st), 0x3); else mma_commit(REMPTY(st));
           if (++st == ns) {
             st = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(tfull0 + 8u * acc);
+        if (PAIR) mma_commit_pair(tfull0 + 8u * acc, 0x3); else mma_commit(tfull0 + 8u * acc);
         acc ^= 1u;
         if (acc == 0u) accph ^= 1u;
       }
       if (!ok && any) {
-        mma_commit(drain_bar);
+        if (PAIR) mma_commit_pair(drain_bar, 0x1); else mma_commit(drain_bar);
         mbar_wait(drain_bar, 0u, nullptr, p.err, 0x280u);
       }
     }
   } else if (warp < 6) {
-    run_epilogue<kW_INT4>(p, tile_base, off, units, blockIdx.x, gridDim.x, -1, tmem_base, tfull0,
-                          map_to_rank(tempty0, cluster_ctarank()), abort_flag, base + L.stg, warp, lane);
+    run_epilogue<kW_INT4>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
+                          tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
   } else {
     // --------------------------------------------- int4 -> bf16 converters
     // Group g (4 warps) converts ring stages g, g + CG, ...; the thread owns
@@ -856,8 +884,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     uint32_t ph = 0, aph = 0;
     uint32_t scount = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit t = decode_unit(u, tile_base, off, p);
+    const uint32_t afull_cl0 = map_to_rank(AFULL(0), 0);  // leader's AFULL(0)
+    for (int u = first; u < units && ok; u += stride) {
+      Unit t = decode_unit(u, tile_base, off, p);
+      if (PAIR) t.fb = 2 * t.fb + static_cast<int>(rank);
       const int grow = p.is_up ? (((m >> 4) & 1) * p.I + t.fb * 64 + (m >> 5) * 16 + (m & 15))
                                : (t.fb * 128 + m);
       const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
@@ -901,7 +931,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(AFULL(a));
+            if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
             if (++a == na) {
               a = 0;
               ap ^= 1u;
@@ -930,9 +960,13 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // no signals into either CTA remain in flight
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -967,14 +1001,14 @@ cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, siz
   return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
 }
 
-template <int CG>
+template <int CG, bool PAIR>
 cudaError_t launch_w4(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
                       cudaStream_t s) {
   static int configured = -1;
-  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG>, &configured);
+  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG, PAIR>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl(grouped_gemm_w4_kernel<CG>, dim3(grid), dim3(gemm_threads(kW_INT4, CG)), smem, s,
-                    maps, p);
+  return launch_pdl_cluster(grouped_gemm_w4_kernel<CG, PAIR>, dim3(PAIR ? (grid & ~1) : grid),
+                            dim3(gemm_threads(kW_INT4, CG)), smem, s, PAIR ? 2u : 1u, maps, p);
 }
 
 }  // namespace
@@ -995,8 +1029,14 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_FP8:
       return p.pair ? launch_pair<kW_FP8>(maps, p, grid, smem, s) : launch_dense<kW_FP8>(maps, p, grid, smem, s);
     case kW_INT4:
-      if (p.conv_groups == 2) return launch_w4<2>(maps, p, grid, smem, s);
-      if (p.conv_groups == 1) return launch_w4<1>(maps, p, grid, smem, s);
+      if (p.pair) {
+        if (p.conv_groups == 3) return launch_w4<3, true>(maps, p, grid, smem, s);
+        if (p.conv_groups == 2) return launch_w4<2, true>(maps, p, grid, smem, s);
+        if (p.conv_groups == 1) return launch_w4<1, true>(maps, p, grid, smem, s);
+      } else {
+        if (p.conv_groups == 2) return launch_w4<2, false>(maps, p, grid, smem, s);
+        if (p.conv_groups == 1) return launch_w4<1, false>(maps, p, grid, smem, s);
+      }
       return cudaErrorInvalidValue;
     default:
       return cudaErrorInvalidValue;
