@@ -208,9 +208,16 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t ran
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA)
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the
+// peer CTA), with the default (CTA-scope release) semantics.  Every caller
+// signals completion of tensor-memory work (tcgen05.st completed by
+// tcgen05.wait::st, or tcgen05.ld results consumed) followed by
+// tcgen05.fence::before_thread_sync; no generic-proxy data is published
+// through these barriers, so a cluster-scope release (a cluster-wide memory
+// fence on every arrival, measured at ~12% of the int4 GEMM's time) buys
+// nothing.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA load into this CTA's shared memory whose completion is counted on an

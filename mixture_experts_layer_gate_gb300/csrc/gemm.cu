@@ -172,6 +172,22 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Moves a ring cursor to entry `target` (>= idx) of a ring of n entries:
+// pos = target mod n, phase flips once per wrap.
+__device__ __forceinline__ void ring_advance(int& pos, uint32_t& phase, int& idx, int target, int n) {
+  int d = target - idx;
+  idx = target;
+  while (d >= n) {
+    d -= n;
+    phase ^= 1u;
+  }
+  pos += d;
+  if (pos >= n) {
+    pos -= n;
+    phase ^= 1u;
+  }
+}
+
 // Token-row loads of one k-block into a B tile: a single box for a full tile,
 // 64- and 16-row boxes for an expert's ragged last tile (few, large TMA
 // requests keep the pipe fed).
@@ -873,45 +889,60 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
                           tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
   } else {
     // --------------------------------------------- int4 -> bf16 converters
-    // Group g (4 warps) converts ring stages g, g + CG, ...; the thread owns
-    // weight row m of the tile, which is TMEM lane m of the converted tile.
+    // The CTA's stages are numbered i = 0, 1, ... in (unit, k) order; a stage of
+    // nk k-blocks fills ceil(nk / 2) TMEM slots, numbered the same way.  Group
+    // g (4 warps) converts the stages with i % CG == g and jumps straight from
+    // one to the next: stepping through the other groups' stages one by one
+    // costs hundreds of cycles each while the other groups saturate the
+    // integer pipe.  The thread owns weight row m of the tile, which is TMEM
+    // lane m of the converted tile.
     const int grp = (warp - 6) >> 2;
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
-    int st = 0, as = 0;
-    uint32_t ph = 0, aph = 0;
-    uint32_t scount = 0;
+    int ci = 0, cst = 0, cs = 0, ca = 0;  // stage / slot index and their ring positions
+    uint32_t cph = 0, cap = 0;
+    int ui = 0, us = 0;                   // first stage / slot index of the current unit
     bool ok = true;
     const uint32_t afull_cl0 = map_to_rank(AFULL(0), 0);  // leader's AFULL(0)
     for (int u = first; u < units && ok; u += stride) {
       Unit t = decode_unit(u, tile_base, off, p);
       if (PAIR) t.fb = 2 * t.fb + static_cast<int>(rank);
+      const int nkb = t.kb1 - t.kb0;
+      const int nst = (nkb + kSuper - 1) / kSuper;
       const int grow = p.is_up ? (((m >> 4) & 1) * p.I + t.fb * 64 + (m >> 5) * 16 + (m & 15))
                                : (t.fb * 128 + m);
       const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
-      for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
+      int l = grp - ui % CG;
+      if (l < 0) l += CG;
+      for (; l < nst && ok; l += CG) {
+        ring_advance(cst, cph, ci, ui + l, ns);
+        ring_advance(ca, cap, cs, us + 2 * l, na);  // every earlier stage of the unit is full
+        const int kbs = t.kb0 + kSuper * l;
         const int nk = min(kSuper, t.kb1 - kbs);
-        if (static_cast<int>(scount % CG) == grp) {
-          __half sc[kSuper];
+        __half sc[kSuper];
 #pragma unroll
-          for (int j = 0; j < kSuper; ++j) sc[j] = srow[min(kbs + j, t.kb1 - 1) >> 1];
-          if (!mbar_wait(RFULL(st), ph, abort_flag, p.err, 0x400u)) {
+        for (int j = 0; j < kSuper; ++j) sc[j] = srow[min(kbs + j, t.kb1 - 1) >> 1];
+        if (!mbar_wait(RFULL(cst), cph, abort_flag, p.err, 0x400u)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* rrow = base + L.r + cst * L.r_stride + m * 128;
+        int a = ca;
+        uint32_t ap = cap;
+#pragma unroll
+        for (int jp = 0; jp < kSuper; jp += 2) {
+          if (jp >= nk) break;
+          if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
             ok = false;
             break;
           }
-          const uint8_t* rrow = base + L.r + st * L.r_stride + m * 128;
-          int a = as;
-          uint32_t ap = aph;
-          for (int jp = 0; jp < nk; jp += 2) {
-            if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            for (int jj = 0; jj < 2 && jp + jj < nk; ++jj) {
-              const int j = jp + jj;
+          tc_fence_after();
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = jp + jj;
+            if (j < nk) {
               const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
               // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
               const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
@@ -928,28 +959,20 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
               }
               tmem_st32(tmem_base + tlane + a_col0 + 64u * static_cast<uint32_t>(a) + 32u * jj, outv);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
-            if (++a == na) {
-              a = 0;
-              ap ^= 1u;
-            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
+          if (++a == na) {
+            a = 0;
+            ap ^= 1u;
           }
         }
-        // every group keeps the same ring and slot counters
-        for (int jp = 0; jp < nk; jp += 2) {
-          if (++as == na) {
-            as = 0;
-            aph ^= 1u;
-          }
-        }
-        ++scount;
-        if (++st == ns) {
-          st = 0;
-          ph ^= 1u;
-        }
+      }
+      if (nst > 0) {
+        ui += nst;
+        us += 2 * (nst - 1) + (nkb - kSuper * (nst - 1) + 1) / 2;
       }
     }
   }
