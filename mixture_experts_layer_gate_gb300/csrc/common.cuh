@@ -290,6 +290,49 @@ __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uin
 }
 // Arrives on the mbarrier at this shared offset in every CTA of `mask` once all
 // prior MMAs of the pair complete.
+// The four MMAs of one k-block (K = 64) with A in TMEM, in one asm block:
+// A columns a, a + 8, a + 16, a + 24; B descriptors whose low word (start
+// address >> 4 and leading offset) is b_lo, b_lo + 2, + 4, + 6 over the high
+// word b_hi.  The operand arithmetic is plain adds and the accumulate
+// predicate is set once, which keeps the single issuing thread short of
+// integer-pipe work when converter warps saturate that pipe.
+template <bool PAIR>
+__device__ __forceinline__ void mma_kblock_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                                  uint32_t b_hi, uint32_t idesc,
+                                                  uint32_t accumulate_first) {
+  if (PAIR) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 t, l;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %3, %3;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], b, %4, p;\n\t"
+        "add.u32 t, %1, 8;\n\tadd.u32 l, %2, 2;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %4, q;\n\t"
+        "add.u32 t, %1, 16;\n\tadd.u32 l, %2, 4;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %4, q;\n\t"
+        "add.u32 t, %1, 24;\n\tadd.u32 l, %2, 6;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %4, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate_first)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b64 b;\n\t.reg .b32 t, l;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %3, %3;\n\t"
+        "mov.b64 b, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t"
+        "add.u32 t, %1, 8;\n\tadd.u32 l, %2, 2;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %4, q;\n\t"
+        "add.u32 t, %1, 16;\n\tadd.u32 l, %2, 4;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %4, q;\n\t"
+        "add.u32 t, %1, 24;\n\tadd.u32 l, %2, 6;\n\tmov.b64 b, {l, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %4, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate_first)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),

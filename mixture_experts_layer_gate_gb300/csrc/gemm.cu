@@ -826,6 +826,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       int st = 0, as = 0;
       uint32_t ph = 0, aph = 0, acc = 0, accph = 0;
       bool ok = true, any = false;
+      const uint64_t bd0 = sw128_kmajor_desc(0u);
+      const uint32_t bd_lo0 = static_cast<uint32_t>(bd0), bd_hi = static_cast<uint32_t>(bd0 >> 32);
+      const uint32_t btile16 = btile >> 4;
+      const uint32_t a_tmem0 = tmem_base + a_col0;
       for (int u = first; u < units && ok; u += stride) {
         const Unit t = decode_unit(u, tile_base, off, p);
         if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
@@ -838,7 +842,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         const uint32_t idesc = make_idesc(PAIR ? 256u : 128u, n_mma, 1u);
         for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
           const int nk = min(kSuper, t.kb1 - kbs);
-          const uint32_t bstage = sR + st * L.r_stride + kRawBytes;
+          // low descriptor word of the stage's first token tile
+          const uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRawBytes) >> 4);
           for (int jp = 0; jp < nk; jp += 2) {
             // the converted slot's barrier also covers the stage's token rows:
             // its converter group waited for the whole stage before converting
@@ -847,19 +852,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_tmem = tmem_base + a_col0 + 64u * static_cast<uint32_t>(as);
-            for (int jj = 0; jj < 2 && jp + jj < nk; ++jj) {
-              const int j = jp + jj;
-              const uint64_t bd = sw128_kmajor_desc(bstage + j * btile);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t accum = (kbs + j > t.kb0 || kk > 0) ? 1u : 0u;
-                if (PAIR)
-                  mma_f16_tmem_a_pair(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
-                else
-                  mma_f16_tmem_a(d, a_tmem + 32u * jj + 8u * kk, bd + 2u * kk, idesc, accum);
-              }
-            }
+            const uint32_t a_tmem = a_tmem0 + 64u * static_cast<uint32_t>(as);
+            const uint32_t b0 = b_lo + static_cast<uint32_t>(jp) * btile16;
+            mma_kblock_tmem_a<PAIR>(d, a_tmem, b0, bd_hi, idesc, kbs + jp > t.kb0 ? 1u : 0u);
+            if (jp + 1 < nk) mma_kblock_tmem_a<PAIR>(d, a_tmem + 32u, b0 + btile16, bd_hi, idesc, 1u);
             if (PAIR) mma_commit_pair(AEMPTY(as), 0x3); else mma_commit(AEMPTY(as));
             any = true;
             if (++as == na) {
