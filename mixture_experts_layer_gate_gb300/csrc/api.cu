@@ -22,6 +22,8 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxStages = 8;  // bf16 / fp8 operand ring
 constexpr int kMaxStagesInt4 = 8;
+constexpr int kMaxSlotsInt4 = 7;  // int4: converted weight tiles in TMEM
+constexpr int kSuper = 4;         // int4: k-blocks per ring stage
 constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
 constexpr size_t kMaxDynSmem = 232448;
 
@@ -113,7 +115,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, conv_groups, acc_cols, pair, FB, KB;
+  int bn_max, P, stages, astages, slot_kb, conv_groups, acc_cols, pair, FB, KB;
   size_t smem;
 };
 
@@ -192,19 +194,33 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
   if (wk == kW_INT4) {
-    // TMEM: two accumulators of acc_cols columns, then converted slots of 64
-    // columns (two k-blocks); at least 2 per converter group (parity-wait rule).
+    // TMEM: two accumulators of acc_cols columns, then converted slots of
+    // slot_kb k-blocks (32 columns each).  A converter group that fills the
+    // 4 / slot_kb slots of its stage jumps (groups - 1) * 4 / slot_kb slots
+    // ahead, so the slot ring needs one more than that (parity-wait rule).
+    // Whole-stage slots (one wait and one commit per 16 MMAs) when TMEM holds
+    // one per group; else two-k-block slots.
     g.acc_cols = (g.bn_max + 31) / 32 * 32;
-    g.astages = std::min(7, (512 - 2 * g.acc_cols) / 64);
-    // three converter groups (CTA pairs) when TMEM holds >= 6 converted slots
-    g.conv_groups = (g.pair && g.astages >= 6) ? 3 : 2;
+    const int free_cols = 512 - 2 * g.acc_cols;
     const int cg_env = env_int("MOE_CONV_GROUPS", 0);
-    if (cg_env == 1 || cg_env == 2 || (cg_env == 3 && g.pair && g.astages >= 6)) g.conv_groups = cg_env;
+    const int sk_env = env_int("MOE_SLOT_KB", 0);
+    // Two converter groups: the single MMA-issuing thread, not conversion, sets
+    // the pace once slots hold whole stages (three groups measured no faster);
+    // three are available with CTA pairs for tuning.
+    g.conv_groups = 2;
+    if (cg_env == 3 && g.pair) g.conv_groups = 3;
+    auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
+    auto slots_fit = [&](int sk) { return std::min(kMaxSlotsInt4, free_cols / (32 * sk)); };
+    g.slot_kb = (slots_fit(4) >= slots_needed(4)) ? 4 : 2;
+    if ((sk_env == 2 || sk_env == 4) && slots_fit(sk_env) >= slots_needed(sk_env)) g.slot_kb = sk_env;
+    if (slots_fit(g.slot_kb) < slots_needed(g.slot_kb)) g.conv_groups = 2;  // 3 groups do not fit
+    g.astages = slots_fit(g.slot_kb);
     per_stage = 16384 + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStagesInt4;
   } else {
     g.acc_cols = 256;
     g.astages = 0;
+    g.slot_kb = 0;
     per_stage = 16384 + static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStages;
   }
@@ -408,6 +424,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.bn_max = g.bn_max;
   gp.stages = g.stages;
   gp.astages = g.astages;
+  gp.slot_kb = g.slot_kb;
   gp.conv_groups = g.conv_groups;
   gp.acc_cols = g.acc_cols;
   gp.full_box = env_int("MOE_FULL_BOX", 0) != 0 ? 1 : 0;
@@ -637,6 +654,8 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->astages_down = d.astages;
   plan->smem_down = static_cast<int32_t>(d.smem);
   plan->num_sms = num_sms;
+  plan->slot_kb_up = u.slot_kb;
+  plan->slot_kb_down = d.slot_kb;
   return MOE_OK;
 }
 

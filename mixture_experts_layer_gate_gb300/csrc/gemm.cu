@@ -677,15 +677,17 @@ __global__ void __launch_bounds__(192, 1)
 //   RFULL/REMPTY over `stages` ring stages of 4 k-blocks (packed codes + token
 //   tiles).  Converter group g takes every CG-th stage; `stages` is a multiple
 //   of CG, so the previous use of a slot was by the same group.
-//   AFULL/AEMPTY over `astages` TMEM slots of 128 x 128 bf16 (64 columns),
-//   one per pair of k-blocks (one wait and one commit per 8 MMAs);
-//   astages >= 2*CG, so a group that filled its previous slot is at most one
-//   phase ahead of any slot it waits on.
+//   AFULL/AEMPTY over `astages` TMEM slots of slot_kb (2 or 4) converted
+//   k-blocks, 128 rows x 32 * slot_kb columns each: one wait and one commit
+//   per 4 * slot_kb MMAs.  A group fills the 4 / slot_kb slots of its stage
+//   and jumps (CG - 1) * 4 / slot_kb slots ahead; astages is at least one more
+//   than that jump, so a group is at most one phase ahead of any slot it
+//   waits on.
 // PAIR: the kernel runs as clusters of two CTAs sharing M = 256 MMAs, each CTA
 // converting its own 128 weight rows into its own TMEM and staging half of the
 // token rows; converter groups of both CTAs report to the leader's AFULL, the
 // leader's commits are multicast to both CTAs.
-template <int CG, bool PAIR>
+template <int CG, bool PAIR, int SK>
 __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     grouped_gemm_w4_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -717,7 +719,9 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
-  if (na < 2 * CG || ns % CG != 0 || a_col0 + 64u * static_cast<uint32_t>(na) > kTmemCols) {
+  static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
+  if (p.slot_kb != SK || na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0 ||
+      a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
     if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
     return;
   }
@@ -830,6 +834,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       const uint32_t bd_lo0 = static_cast<uint32_t>(bd0), bd_hi = static_cast<uint32_t>(bd0 >> 32);
       const uint32_t btile16 = btile >> 4;
       const uint32_t a_tmem0 = tmem_base + a_col0;
+      const uint32_t slot_cols = 32u * static_cast<uint32_t>(SK);
       for (int u = first; u < units && ok; u += stride) {
         const Unit t = decode_unit(u, tile_base, off, p);
         if (!mbar_wait(tempty0 + 8u * acc, accph ^ 1u, abort_flag, p.err, 0x200u)) {
@@ -844,7 +849,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           const int nk = min(kSuper, t.kb1 - kbs);
           // low descriptor word of the stage's first token tile
           const uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRawBytes) >> 4);
-          for (int jp = 0; jp < nk; jp += 2) {
+          for (int jp = 0; jp < nk; jp += SK) {
             // the converted slot's barrier also covers the stage's token rows:
             // its converter group waited for the whole stage before converting
             if (!mbar_wait(AFULL(as), aph, abort_flag, p.err, 0x210u)) {
@@ -852,10 +857,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_tmem = a_tmem0 + 64u * static_cast<uint32_t>(as);
+            const uint32_t a_tmem = a_tmem0 + slot_cols * static_cast<uint32_t>(as);
             const uint32_t b0 = b_lo + static_cast<uint32_t>(jp) * btile16;
             mma_kblock_tmem_a<PAIR>(d, a_tmem, b0, bd_hi, idesc, kbs + jp > t.kb0 ? 1u : 0u);
-            if (jp + 1 < nk) mma_kblock_tmem_a<PAIR>(d, a_tmem + 32u, b0 + btile16, bd_hi, idesc, 1u);
+            const int jn = min(SK, nk - jp);
+            for (int jj = 1; jj < jn; ++jj)
+              mma_kblock_tmem_a<PAIR>(d, a_tmem + 32u * jj, b0 + btile16 * jj, bd_hi, idesc, 1u);
             if (PAIR) mma_commit_pair(AEMPTY(as), 0x3); else mma_commit(AEMPTY(as));
             any = true;
             if (++as == na) {
@@ -902,6 +909,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     int ui = 0, us = 0;                   // first stage / slot index of the current unit
     bool ok = true;
     const uint32_t afull_cl0 = map_to_rank(AFULL(0), 0);  // leader's AFULL(0)
+    const int spp = kSuper / SK;                            // slots per full stage
     for (int u = first; u < units && ok; u += stride) {
       Unit t = decode_unit(u, tile_base, off, p);
       if (PAIR) t.fb = 2 * t.fb + static_cast<int>(rank);
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       if (l < 0) l += CG;
       for (; l < nst && ok; l += CG) {
         ring_advance(cst, cph, ci, ui + l, ns);
-        ring_advance(ca, cap, cs, us + 2 * l, na);  // every earlier stage of the unit is full
+        ring_advance(ca, cap, cs, us + spp * l, na);  // every earlier stage of the unit is full
         const int kbs = t.kb0 + kSuper * l;
         const int nk = min(kSuper, t.kb1 - kbs);
         __half sc[kSuper];
@@ -928,47 +936,46 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         int a = ca;
         uint32_t ap = cap;
 #pragma unroll
-        for (int jp = 0; jp < kSuper; jp += 2) {
-          if (jp >= nk) break;
-          if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const int j = jp + jj;
-            if (j < nk) {
-              const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
-              // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
-              const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
-              const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
-              const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-              uint32_t outv[32];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const uint4 o = dequant8(w[i], s2);
-                outv[4 * i + 0] = o.x;
-                outv[4 * i + 1] = o.y;
-                outv[4 * i + 2] = o.z;
-                outv[4 * i + 3] = o.w;
-              }
-              tmem_st32(tmem_base + tlane + a_col0 + 64u * static_cast<uint32_t>(a) + 32u * jj, outv);
+        for (int j = 0; j < kSuper; ++j) {
+          if (j >= nk) break;
+          const int js = j & (SK - 1);  // k-block within the slot
+          if (js == 0) {
+            if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
           }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
-          if (++a == na) {
-            a = 0;
-            ap ^= 1u;
+          const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
+          // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
+          const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
+          const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
+          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          uint32_t outv[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 o = dequant8(w[i], s2);
+            outv[4 * i + 0] = o.x;
+            outv[4 * i + 1] = o.y;
+            outv[4 * i + 2] = o.z;
+            outv[4 * i + 3] = o.w;
+          }
+          tmem_st32(tmem_base + tlane + a_col0 + 32u * static_cast<uint32_t>(SK * a + js), outv);
+          if (js == SK - 1 || j == nk - 1) {
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
+            if (++a == na) {
+              a = 0;
+              ap ^= 1u;
+            }
           }
         }
       }
       if (nst > 0) {
         ui += nst;
-        us += 2 * (nst - 1) + (nkb - kSuper * (nst - 1) + 1) / 2;
+        us += spp * (nst - 1) + (nkb - kSuper * (nst - 1) + SK - 1) / SK;
       }
     }
   }
@@ -1020,13 +1027,13 @@ cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, siz
   return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
 }
 
-template <int CG, bool PAIR>
+template <int CG, bool PAIR, int SK>
 cudaError_t launch_w4(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
                       cudaStream_t s) {
   static int configured = -1;
-  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG, PAIR>, &configured);
+  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG, PAIR, SK>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl_cluster(grouped_gemm_w4_kernel<CG, PAIR>, dim3(PAIR ? (grid & ~1) : grid),
+  return launch_pdl_cluster(grouped_gemm_w4_kernel<CG, PAIR, SK>, dim3(PAIR ? (grid & ~1) : grid),
                             dim3(gemm_threads(kW_INT4, CG)), smem, s, PAIR ? 2u : 1u, maps, p);
 }
 
@@ -1048,13 +1055,14 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_FP8:
       return p.pair ? launch_pair<kW_FP8>(maps, p, grid, smem, s) : launch_dense<kW_FP8>(maps, p, grid, smem, s);
     case kW_INT4:
-      if (p.pair) {
-        if (p.conv_groups == 3) return launch_w4<3, true>(maps, p, grid, smem, s);
-        if (p.conv_groups == 2) return launch_w4<2, true>(maps, p, grid, smem, s);
-        if (p.conv_groups == 1) return launch_w4<1, true>(maps, p, grid, smem, s);
-      } else {
-        if (p.conv_groups == 2) return launch_w4<2, false>(maps, p, grid, smem, s);
-        if (p.conv_groups == 1) return launch_w4<1, false>(maps, p, grid, smem, s);
+      if (p.slot_kb == 4) {
+        if (p.pair && p.conv_groups == 3) return launch_w4<3, true, 4>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 2) return launch_w4<2, true, 4>(maps, p, grid, smem, s);
+        if (!p.pair && p.conv_groups == 2) return launch_w4<2, false, 4>(maps, p, grid, smem, s);
+      } else if (p.slot_kb == 2) {
+        if (p.pair && p.conv_groups == 3) return launch_w4<3, true, 2>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 2) return launch_w4<2, true, 2>(maps, p, grid, smem, s);
+        if (!p.pair && p.conv_groups == 2) return launch_w4<2, false, 2>(maps, p, grid, smem, s);
       }
       return cudaErrorInvalidValue;
     default:

@@ -78,6 +78,7 @@ struct GemmParams {
   int bn_max;              // token tile limit: multiple of 16, <= 256
   int stages;              // operand ring depth (int4: ring of packed A + token tiles)
   int astages;             // int4 only: ring of converted bf16 A tiles
+  int slot_kb;             // int4 only: k-blocks per converted tile (2 or 4)
   int full_box;            // 1: always load bn_max token rows (tuning)
   int conv_groups;         // int4 only: converter warp groups (2 or 4)
   int acc_cols;            // TMEM columns per accumulator buffer

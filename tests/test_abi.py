@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 48
     assert ctypes.sizeof(binding.WeightsStruct) == 48
-    assert ctypes.sizeof(binding.Plan) == 44
+    assert ctypes.sizeof(binding.Plan) == 52
 
 
 def test_status_strings(lib):
@@ -131,10 +131,13 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             assert st >= 2
             assert getattr(pl, f"smem_{side}") <= 232448
             if shape.wdtype == "int4":
-                # TMEM holds two accumulators and >= 4 converted tiles per converter
-                # group (2 groups); the ring depth is a multiple of the group count
-                assert bn <= 128
-                assert 4 <= ast <= 7 and 2 * ((bn + 31) // 32 * 32) + 64 * ast <= 512
+                # TMEM holds two accumulators and the converted-weight slot ring
+                sk = getattr(pl, f"slot_kb_{side}")
+                assert bn <= 128 and sk in (2, 4)
+                assert 2 <= ast <= 7 and 2 * ((bn + 31) // 32 * 32) + 32 * sk * ast <= 512
+                # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
+                # stage count that is a multiple of g; g = 2 always satisfies both here
+                assert ast >= 4 // sk + 1
                 assert st % 2 == 0 or st % 3 == 0
             else:
-                assert ast == 0
+                assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0
