@@ -259,21 +259,25 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       const size_t row = static_cast<size_t>(t.row0 + c0);
       if (p.epi == kEpiSwiglu) {
         // lane l < 16: gate row of feature 16q + l; lane l + 16: its up row.
+        // Columns go in pairs with every lane busy and no branch: the gate lane
+        // sends its odd-column gate value and gets the even-column up value,
+        // the up lane the reverse, so one exchange gives each lane the operands
+        // of one output (even column on gate lanes, odd on up lanes).
         const bool upl = lane >= 16;
         const int f16 = lane & 15;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float x = __uint_as_float(v[c]) * sc;
-          const float o = __shfl_xor_sync(0xffffffffu, x, 16);
-          if ((c & 1) == static_cast<int>(upl)) {
-            const float g = upl ? o : x;
-            const float uu = upl ? x : o;
-            const float a = silu_f32(g) * uu;
-            if (WK == kW_FP8)
-              stg[c * 16 + f16] = static_cast<uint8_t>(f32x2_to_e4m3x2(a * inv_q, 0.f) & 0xFF);
-            else
-              reinterpret_cast<__nv_bfloat16*>(stg)[c * 16 + f16] = __float2bfloat16_rn(a);
-          }
+        for (int c = 0; c < 16; c += 2) {
+          const float x0 = __uint_as_float(v[c]) * sc;
+          const float x1 = __uint_as_float(v[c + 1]) * sc;
+          const float recv = __shfl_xor_sync(0xffffffffu, upl ? x0 : x1, 16);
+          const float g = upl ? recv : x0;
+          const float uu = upl ? x1 : recv;
+          const float a = silu_f32(g) * uu;
+          const int col = c + (upl ? 1 : 0);
+          if (WK == kW_FP8)
+            stg[col * 16 + f16] = static_cast<uint8_t>(f32x2_to_e4m3x2(a * inv_q, 0.f) & 0xFF);
+          else
+            reinterpret_cast<__nv_bfloat16*>(stg)[col * 16 + f16] = __float2bfloat16_rn(a);
         }
         __syncwarp();
         const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16;
