@@ -20,6 +20,7 @@ namespace moe {
 namespace {
 
 constexpr int kScatterThreads = 512;
+constexpr int kGatherThreads = 128;
 constexpr int kScatterWarps = kScatterThreads / 32;
 
 __global__ void __launch_bounds__(512) align_count_kernel(AlignArgs a) {
@@ -156,14 +157,13 @@ __global__ void __launch_bounds__(kScatterThreads) align_scatter_kernel(AlignArg
   }
 }
 
-// One warp per permuted row; 16-byte vectors along H.
+// One CTA of 128 threads per permuted row; 16-byte vectors along H.  (A warp
+// per row left small batches latency-bound on the per-element divisions.)
 template <bool FP8>
-__global__ void __launch_bounds__(256) gather_rows_kernel(AlignArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(AlignArgs a) {
+  const int r = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  if (r >= a.S) return;
   const int t = a.perm[r] / a.k;
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
                                                     static_cast<size_t>(t) * a.H);
@@ -171,12 +171,12 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(AlignArgs a) {
   if (!FP8) {
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.x_perm) +
                                           static_cast<size_t>(r) * a.H);
-    for (int c = lane; c < nvec; c += 32) dst[c] = __ldg(src + c);
+    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) dst[c] = __ldg(src + c);
   } else {
     const float s = a.a1[0];
     uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.x_perm) +
                                           static_cast<size_t>(r) * a.H);
-    for (int c = lane; c < nvec; c += 32) {
+    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) {
       const uint4 v = __ldg(src + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t q[2];
@@ -240,9 +240,8 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
   const size_t scatter_smem = sizeof(int) * (3 * a.E + 32) + sizeof(uint16_t) * kScatterWarps * a.E;
   err = launch_pdl(align_scatter_kernel, dim3(nblk), dim3(kScatterThreads), scatter_smem, s, a, nblk);
   if (err != cudaSuccess) return err;
-  const int gblocks = (a.S + 7) / 8;
-  if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(gblocks), dim3(256), 0, s, a);
-  return launch_pdl(gather_rows_kernel<false>, dim3(gblocks), dim3(256), 0, s, a);
+  if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
+  return launch_pdl(gather_rows_kernel<false>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
 }
 
 cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm, int E, int S,

@@ -339,8 +339,16 @@ moe_status_t run_align(const moe_problem_t& p, const int32_t* ids, const void* x
   return cuda_status(launch_align(a, s));
 }
 
+// Split-K partials of the down GEMM left for the caller's reduce to finish.
+struct DeferredFinish {
+  const float* part = nullptr;
+  int P = 1;
+  int64_t pstride = 0;
+};
+
 moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, const void* in,
-                      const int32_t* offsets, void* out, void* ws, cudaStream_t s) {
+                      const int32_t* offsets, void* out, void* ws, cudaStream_t s,
+                      DeferredFinish* defer = nullptr) {
   const int S = p.T * p.top_k;
   if (S == 0) return MOE_OK;
   DeviceInfo di;
@@ -451,10 +459,15 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   cudaError_t err = launch_grouped_gemm(wk, maps, gp, di.sms, g.smem, s);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (g.P > 1) {
-    if (up)
+    if (up) {
       err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8, out, s);
-    else
+    } else if (defer != nullptr) {
+      defer->part = part;  // the caller folds the slice sum into its reduce
+      defer->P = g.P;
+      defer->pstride = gp.part_stride;
+    } else {
       err = launch_down_finish(part, g.P, gp.part_stride, S, p.H, out, s);
+    }
   }
   return cuda_status(err);
 }
@@ -608,7 +621,11 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
   MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
   MOE_TRY(run_align(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws, s));
   MOE_TRY(run_gemm(*p, *w, true, x_perm, offsets, act, ws, s));
-  MOE_TRY(run_gemm(*p, *w, false, act, offsets, y_perm, ws, s));
+  DeferredFinish df;
+  MOE_TRY(run_gemm(*p, *w, false, act, offsets, y_perm, ws, s, &df));
+  if (df.part != nullptr)
+    return cuda_status(launch_unpermute_reduce_splitk(df.part, df.P, df.pstride, inv, tw, p->T, p->H,
+                                                      p->top_k, out, s));
   return cuda_status(launch_unpermute_reduce(y_perm, inv, tw, p->T, p->H, p->top_k, out, s));
 }
 

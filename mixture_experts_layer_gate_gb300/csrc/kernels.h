@@ -56,6 +56,9 @@ cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int 
                                  const float* a2, int fp8, void* act, cudaStream_t s);
 cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H,
                                void* y, cudaStream_t s);
+// down_finish + unpermute_reduce in one pass, bit-identical to the pair.
+cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pstride, const int32_t* inv,
+                                           const float* w, int T, int H, int k, void* out, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
 enum WKind : int { kW_BF16 = 0, kW_FP8 = 1, kW_INT4 = 2 };
