@@ -235,6 +235,9 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   // int4: converter group g takes every conv_groups-th ring stage, so the ring
   // depth must be a multiple of the group count (parity-wait rule).
   if (wk == kW_INT4) g.stages -= g.stages % g.conv_groups;
+  // int4 whole-stage slots: converters wait on the stage ring for slot reuse,
+  // which needs at least as many ring stages as slots (parity-wait rule)
+  if (wk == kW_INT4 && g.slot_kb == kSuper && g.astages > g.stages) g.astages = g.stages;
   g.smem = gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E);
   return g;
 }

@@ -686,7 +686,10 @@ __global__ void __launch_bounds__(192, 1)
 //   per 4 * slot_kb MMAs.  A group fills the 4 / slot_kb slots of its stage
 //   and jumps (CG - 1) * 4 / slot_kb slots ahead; astages is at least one more
 //   than that jump, so a group is at most one phase ahead of any slot it
-//   waits on.
+//   waits on.  With whole-stage slots (slot_kb = 4) slot i is ring stage i's,
+//   so the MMA commits once per stage (REMPTY) and a converter about to refill
+//   slot i mod astages waits for REMPTY of stage i - astages instead; stages >=
+//   astages keeps that barrier from running a phase past the one awaited.
 // PAIR: the kernel runs as clusters of two CTAs sharing M = 256 MMAs, each CTA
 // converting its own 128 weight rows into its own TMEM and staging half of the
 // token rows; converter groups of both CTAs report to the leader's AFULL, the
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
-  if (p.slot_kb != SK || na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0 ||
+  if (p.slot_kb != SK || (SK == kSuper && ns < na) || na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0 ||
       a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
     if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
     return;
@@ -867,7 +870,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             const int jn = min(SK, nk - jp);
             for (int jj = 1; jj < jn; ++jj)
               mma_kblock_tmem_a<PAIR>(d, a_tmem + 32u * jj, b0 + btile16 * jj, bd_hi, idesc, 1u);
-            if (PAIR) mma_commit_pair(AEMPTY(as), 0x3); else mma_commit(AEMPTY(as));
+            // whole-stage slots: the stage's REMPTY commit below also frees the slot
+            if (SK != kSuper) {
+              if (PAIR) mma_commit_pair(AEMPTY(as), 0x3); else mma_commit(AEMPTY(as));
+            }
             any = true;
             if (++as == na) {
               as = 0;
@@ -910,6 +916,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
     int ci = 0, cst = 0, cs = 0, ca = 0;  // stage / slot index and their ring positions
     uint32_t cph = 0, cap = 0;
+    int pi = 0, pst = 0;                  // ring position of stage i - astages (whole-stage slots)
+    uint32_t pph = 0;
     int ui = 0, us = 0;                   // first stage / slot index of the current unit
     bool ok = true;
     const uint32_t afull_cl0 = map_to_rank(AFULL(0), 0);  // leader's AFULL(0)
@@ -936,6 +944,16 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           ok = false;
           break;
         }
+        if (SK == kSuper && ui + l >= na) {
+          // whole-stage slots: slot (i mod astages) is free once stage i - astages
+          // has been consumed, i.e. after that stage's REMPTY completion
+          ring_advance(pst, pph, pi, ui + l - na, ns);
+          if (!mbar_wait(REMPTY(pst), pph, abort_flag, p.err, 0x410u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         const uint8_t* rrow = base + L.r + cst * L.r_stride + m * 128;
         int a = ca;
         uint32_t ap = cap;
@@ -943,7 +961,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         for (int j = 0; j < kSuper; ++j) {
           if (j >= nk) break;
           const int js = j & (SK - 1);  // k-block within the slot
-          if (js == 0) {
+          if (SK != kSuper && js == 0) {
             if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
               ok = false;
               break;
