@@ -188,3 +188,27 @@ FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), 
 def test_full_size_sampled(dev, name, T):
     r = gc.sampled_check(SHAPES[name], T, dev, n_sample=3)
     print(f"{name} T={T}: err={r['err']:.3e} near-ties={r['amb']} mismatched={r['mism']}")
+
+
+# Kernel variants the planner does not pick for these shapes, forced through the
+# library's tuning knobs (read from the environment at every plan): the single-CTA
+# bf16/fp8 kernel (no CTA pairs), and the int4 kernel's non-pair, two-k-block-slot and
+# three-converter-group instantiations.
+@pytest.mark.parametrize("name,knobs", [
+    ("mixtral", {"MOE_PAIR": "0"}),
+    ("qwen2", {"MOE_PAIR": "0"}),
+    ("dsv3", {"MOE_PAIR": "0"}),
+    ("dsv3", {"MOE_SLOT_KB": "2"}),
+    ("dsv3", {"MOE_CONV_GROUPS": "3"}),
+    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
+])
+def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
+    for k, v in knobs.items():
+        monkeypatch.setenv(k, v)
+    shape = small(name)
+    plan = moe.get_plan(gc.lib_problem(shape, 300))
+    if "MOE_SLOT_KB" in knobs:
+        assert plan.slot_kb_up == int(knobs["MOE_SLOT_KB"])
+    for T in (37, 300):
+        gc.full_check(shape, T, dev)
