@@ -472,6 +472,36 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def measure_tensor_peaks():
+    """Dense GEMM throughput of the vendor library on this GPU, for the roofline
+    denominators: cuBLASLt bf16 and e4m3 (per-tensor scales) n x n x n GEMMs,
+    CUDA events around 20 back-to-back launches after 5 warm-up ones."""
+    import torch
+    dev = torch.device("cuda:0")
+    res = {}
+    for n in (8192, 16384):
+        a8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        a16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+        b16 = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+        row = {}
+        for name, fn in (("e4m3", lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)),
+                         ("bf16", lambda: a16 @ b16)):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(20):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            row[name + "_tflops"] = 2.0 * n ** 3 / (e0.elapsed_time(e1) / 20 / 1e3) / 1e12
+        res[str(n)] = row
+    print(json.dumps({"tensor_peaks": res}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -485,9 +515,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=2048)
     ap.add_argument("--ref-sample", type=int, default=16)
+    ap.add_argument("--measure-tensor-peaks", action="store_true",
+                    help="print the library's dense bf16 / e4m3 GEMM throughput and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.measure_tensor_peaks:
+        measure_tensor_peaks()
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
