@@ -240,6 +240,11 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
   const size_t scatter_smem = sizeof(int) * (3 * a.E + 32) + sizeof(uint16_t) * kScatterWarps * a.E;
   err = launch_pdl(align_scatter_kernel, dim3(nblk), dim3(kScatterThreads), scatter_smem, s, a, nblk);
   if (err != cudaSuccess) return err;
+  return launch_gather(a, s);
+}
+
+cudaError_t launch_gather(const AlignArgs& a, cudaStream_t s) {
+  if (a.S == 0) return cudaSuccess;
   if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
   return launch_pdl(gather_rows_kernel<false>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
 }

@@ -301,8 +301,8 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 // ----------------------------------------------------------------- stages
 
-moe_status_t run_gate(const moe_problem_t& p, const float* logits, const float* bias, int32_t* ids,
-                      float* w, cudaStream_t s) {
+GateArgs gate_args(const moe_problem_t& p, const float* logits, const float* bias, int32_t* ids,
+                   float* w) {
   GateArgs a;
   a.logits = logits;
   a.bias = (p.scoring == MOE_SCORE_SIGMOID) ? bias : nullptr;
@@ -316,12 +316,17 @@ moe_status_t run_gate(const moe_problem_t& p, const float* logits, const float* 
   a.n_group = p.n_group;
   a.topk_group = p.topk_group;
   a.scale = p.routed_scaling_factor;
-  return cuda_status(launch_gate(a, s));
+  return a;
 }
 
-moe_status_t run_align(const moe_problem_t& p, const int32_t* ids, const void* x, const float* a1,
-                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
-                       void* x_perm, void* ws, cudaStream_t s) {
+moe_status_t run_gate(const moe_problem_t& p, const float* logits, const float* bias, int32_t* ids,
+                      float* w, cudaStream_t s) {
+  return cuda_status(launch_gate(gate_args(p, logits, bias, ids, w), s));
+}
+
+AlignArgs align_args(const moe_problem_t& p, const int32_t* ids, const void* x, const float* a1,
+                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, void* x_perm,
+                     void* ws) {
   const Layout L = layout_of(p);
   AlignArgs a;
   a.ids = ids;
@@ -339,7 +344,14 @@ moe_status_t run_align(const moe_problem_t& p, const int32_t* ids, const void* x
   a.a1 = a1;
   a.fp8 = p.wdtype == MOE_W_FP8_E4M3;
   a.err = at<uint32_t>(ws, L.hdr);
-  return cuda_status(launch_align(a, s));
+  return a;
+}
+
+moe_status_t run_align(const moe_problem_t& p, const int32_t* ids, const void* x, const float* a1,
+                       int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                       void* x_perm, void* ws, cudaStream_t s) {
+  return cuda_status(
+      launch_align(align_args(p, ids, x, a1, counts, offsets, perm, inv, x_perm, ws), s));
 }
 
 // Split-K partials of the down GEMM left for the caller's reduce to finish.
@@ -621,8 +633,16 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
   void* x_perm = at<void>(ws, L.x_perm);
   void* act = at<void>(ws, L.act);
   void* y_perm = at<void>(ws, L.y_perm);
-  MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
-  MOE_TRY(run_align(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws, s));
+  if (p->T * p->top_k <= kRouteMaxSlots) {
+    // small batch: gate, histogram, offsets and permutation in one CTA (results
+    // identical to the two-step path below), then the row gather
+    const AlignArgs aa = align_args(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws);
+    MOE_TRY(cuda_status(launch_route_small(gate_args(*p, logits, bias, ids, tw), aa, s)));
+    MOE_TRY(cuda_status(launch_gather(aa, s)));
+  } else {
+    MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
+    MOE_TRY(run_align(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws, s));
+  }
   MOE_TRY(run_gemm(*p, *w, true, x_perm, offsets, act, ws, s));
   DeferredFinish df;
   MOE_TRY(run_gemm(*p, *w, false, act, offsets, y_perm, ws, s, &df));

@@ -42,6 +42,14 @@ struct AlignArgs {
   uint32_t* err;
 };
 cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
+// x_perm rows only (perm must be ready).
+cudaError_t launch_gather(const AlignArgs& a, cudaStream_t s);
+
+// Gate + histogram + offsets + stable permutation in one CTA, for batches of
+// at most kRouteMaxSlots (token, expert) slots; ids / w / counts / offsets /
+// perm / inv are bit-identical to launch_gate followed by launch_align.
+constexpr int kRouteMaxSlots = 1024;
+cudaError_t launch_route_small(const GateArgs& g, const AlignArgs& a, cudaStream_t s);
 
 cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm, int E, int S,
                                     int block, size_t capacity, int32_t* sorted_ids,
