@@ -248,36 +248,58 @@ def run_ours(args):
     roof["kernel_ms"] = k_ms
     roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
 
-    # end to end through the public call with host buffers
+    # end to end through the public call with host buffers: every step uploads its
+    # inputs (x, logits) from pinned host memory, runs moe_forward and reads its
+    # output back.  Steps are pipelined the way a serving loop would run them:
+    # step i's upload overlaps step i-1's forward and step i-1's download overlaps
+    # step i's forward (two device buffer sets; copies on their own streams).
     x_h = tok.x.cpu().pin_memory()
     l_h = tok.logits.cpu().pin_memory()
-    o_h = torch.empty((T, shape.H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(tok.x)
-    l_d = torch.empty_like(tok.logits)
+    o_h = [torch.empty((T, shape.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_d = [torch.empty_like(tok.x) for _ in range(2)]
+    l_d = [torch.empty_like(tok.logits) for _ in range(2)]
+    o_d = [torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "comp", "out")}
+    started = [False, False]
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            x_d.copy_(x_h, non_blocking=True)
-            l_d.copy_(l_h, non_blocking=True)
-            moe.forward(p, wts, x_d, l_d, tok.bias, out, ws, stream.cuda_stream)
-            o_h.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if started[b]:
+                s_in.wait_event(ev["comp"][b])  # step i-2's forward has read x_d[b]
+            x_d[b].copy_(x_h, non_blocking=True)
+            l_d[b].copy_(l_h, non_blocking=True)
+            ev["in"][b].record(s_in)
+        stream.wait_event(ev["in"][b])
+        if started[b]:
+            stream.wait_event(ev["out"][b])  # step i-2's download has read o_d[b]
+        moe.forward(p, wts, x_d[b], l_d[b], tok.bias, o_d[b], ws, stream.cuda_stream)
+        ev["comp"][b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][b])
+            o_h[b].copy_(o_d[b], non_blocking=True)
+            ev["out"][b].record(s_out)
+        started[b] = True
 
-    for _ in range(2):
-        e2e_step()
-    stream.synchronize()
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    stream.synchronize()
+    e0.record(s_in)
+    for i in range(args.steps):
+        e2e_step(2 + i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1) / args.steps
     if dist is not None:
         t = torch.tensor([e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e_ms = float(t.item())
+    torch.cuda.synchronize()
+    e2e_ok = bool(torch.equal(o_h[(2 + args.steps - 1) & 1], out.cpu()))  # same inputs -> same output
 
     launches_per_step = 7 + (plan.splits_up > 1) + (plan.splits_down > 1)
 
@@ -305,7 +327,9 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": world * T / (e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + l_h.numel() * 4),
-                "d2h_bytes_per_step": int(o_h.numel() * 2), "ms_per_step": e_ms},
+                "d2h_bytes_per_step": int(o_h[0].numel() * 2), "ms_per_step": e_ms,
+                "pipelined": "step i's upload and step i-1's download overlap forwards",
+                "output_matches_device_run": e2e_ok},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
