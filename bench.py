@@ -40,6 +40,33 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def init_replicas(backend="nccl"):
+    """Process group of a torchrun launch (one rank per GPU, independent
+    replicas: no collective touches the data path), or None for one process."""
+    world = _env_int("WORLD_SIZE", 1)
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend)
+    return dist
+
+
+def max_over_ranks(dist, value, device):
+    """The slowest rank's value (the job finishes when every replica has)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, tokens_per_rank, ms_max):
+    """Whole-job tokens/s: every replica's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 def _env_int(name, default):
     try:
         return int(os.environ.get(name, default))
@@ -130,10 +157,7 @@ def run_ours(args):
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local = _env_int("LOCAL_RANK", 0)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    dist = init_replicas("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     moe.load()
@@ -189,12 +213,8 @@ def run_ours(args):
         time.sleep(0.05)
     if dist is not None:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / args.steps, dev)
+    value = job_throughput(world, T, ms)
 
     # routing facts for the roofline
     counts = ws[0:0]  # placeholder keep-alive
@@ -293,11 +313,7 @@ def run_ours(args):
         e2e_step(2 + i)
     e1.record(s_out)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
     torch.cuda.synchronize()
     e2e_ok = bool(torch.equal(o_h[(2 + args.steps - 1) & 1], out.cpu()))  # same inputs -> same output
 
@@ -325,7 +341,7 @@ def run_ours(args):
         "layer_roofline": {"t_roof_us": t_roof * 1e6, "frac": layer_frac, "touched_experts": touched,
                            "bytes": B, "flops": F},
         "roofline": roof,
-        "e2e": {"value": world * T / (e_ms / 1e3), "unit": UNIT,
+        "e2e": {"value": job_throughput(world, T, e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + l_h.numel() * 4),
                 "d2h_bytes_per_step": int(o_h[0].numel() * 2), "ms_per_step": e_ms,
                 "pipelined": "step i's upload and step i-1's download overlap forwards",
@@ -485,10 +501,12 @@ def run_reference(args):
         n += k
     wall = time.perf_counter() - t0
     v = n / total
-    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT,
+            "n_gpus": _env_int("WORLD_SIZE", 1), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "mixtral_8x7b_moe_layer", "T": args.T, "sample_tokens_per_step": len(r.rows)},
+            "config": {"workload": WORKLOADS.get(args.config, args.config), "T": args.T,
+                       "sample_tokens_per_step": len(r.rows)},
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{len(r.rows)} of {args.T} tokens per step, fp64 numpy, expert decode excluded"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
