@@ -852,6 +852,44 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         const uint32_t d = tmem_base + acc * acc_cols;
         const uint32_t n_mma = PAIR ? static_cast<uint32_t>((t.nvalid + 31) & ~31) : static_cast<uint32_t>(t.n);
         const uint32_t idesc = make_idesc(PAIR ? 256u : 128u, n_mma, 1u);
+        if (SK == kSuper) {
+          // Whole-stage slots: one wait, the stage's MMAs, one commit.  The next
+          // stage's ring positions, barrier addresses and descriptor words are
+          // worked out between this stage's first and remaining MMAs, so the
+          // thread goes from the commit straight to the next wait (the tensor
+          // pipe idles while this single thread does bookkeeping).
+          uint32_t afull = AFULL(as), rempty = REMPTY(st);
+          uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRawBytes) >> 4);
+          uint32_t a_tm = a_tmem0 + slot_cols * static_cast<uint32_t>(as);
+          for (int kbs = t.kb0; kbs < t.kb1; kbs += kSuper) {
+            const int nk = min(kSuper, t.kb1 - kbs);
+            if (!mbar_wait(afull, aph, abort_flag, p.err, 0x210u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_kblock_tmem_a<PAIR>(d, a_tm, b_lo, bd_hi, idesc, kbs > t.kb0 ? 1u : 0u);
+            const int st_n = (st + 1 == ns) ? 0 : st + 1;
+            const uint32_t ph_n = (st + 1 == ns) ? (ph ^ 1u) : ph;
+            const int as_n = (as + 1 == na) ? 0 : as + 1;
+            const uint32_t aph_n = (as + 1 == na) ? (aph ^ 1u) : aph;
+            const uint32_t afull_n = AFULL(as_n), rempty_n = REMPTY(st_n);
+            const uint32_t b_lo_n = bd_lo0 + ((sR + st_n * L.r_stride + kRawBytes) >> 4);
+            const uint32_t a_tm_n = a_tmem0 + slot_cols * static_cast<uint32_t>(as_n);
+            for (int jj = 1; jj < nk; ++jj)
+              mma_kblock_tmem_a<PAIR>(d, a_tm + 32u * jj, b_lo + btile16 * jj, bd_hi, idesc, 1u);
+            if (PAIR) mma_commit_pair(rempty, 0x3); else mma_commit(rempty);
+            any = true;
+            st = st_n;
+            ph = ph_n;
+            as = as_n;
+            aph = aph_n;
+            afull = afull_n;
+            rempty = rempty_n;
+            b_lo = b_lo_n;
+            a_tm = a_tm_n;
+          }
+        } else
         for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
           const int nk = min(kSuper, t.kb1 - kbs);
           // low descriptor word of the stage's first token tile
