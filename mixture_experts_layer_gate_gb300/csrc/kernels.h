@@ -91,7 +91,7 @@ struct GemmParams {
   int astages;             // int4 only: ring of converted bf16 A tiles
   int slot_kb;             // int4 only: k-blocks per converted tile (2 or 4)
   int full_box;            // 1: always load bn_max token rows (tuning)
-  int conv_groups;         // int4 only: converter warp groups (2 or 4)
+  int conv_groups;         // int4 only: converter warp groups (2, or 3 with CTA pairs)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
