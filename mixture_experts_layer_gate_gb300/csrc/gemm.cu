@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kABytes = 16384;    // 128 rows x 128 B (bf16 / e4m3 weight tile)
 constexpr int kRawBytes = 16384;  // int4: 128 rows x 128 B of packed codes = 4 k-blocks
-constexpr int kSuper = 4;         // int4: k-blocks per ring stage
+constexpr int kSuper = kInt4StageKb;  // int4: k-blocks per ring stage
 constexpr int kStgBytesPerWarp = 2048;
 constexpr int kStgBytes = 4 * kStgBytesPerWarp;
 constexpr uint32_t kTmemCols = 512;

@@ -69,6 +69,9 @@ cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pst
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
+// int4: k-blocks (64 reduction elements each) per operand ring stage.
+constexpr int kInt4StageKb = 4;
+
 enum WKind : int { kW_BF16 = 0, kW_FP8 = 1, kW_INT4 = 2 };
 enum EpiKind : int { kEpiSwiglu = 0, kEpiStore = 1, kEpiPartial = 2 };
 
