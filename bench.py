@@ -27,7 +27,9 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s and achieved % of roofline (HBM or tensor) vs batch 1–4096"
 UNIT = "tokens/s"
 CONFIG_NAME = "mixtral"
-WORKLOADS = {"mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
+WORKLOADS = {"mixtral_tp2": "mixtral_8x7b_moe_layer_tp2_slice", "qwen2_tp4": "qwen2_57b_a14b_moe_layer_fp8_tp4_slice",
+             "dsv3_tp8": "deepseek_v3_moe_layer_int4_tp8_slice", "scout_tp8": "llama4_scout_moe_layer_tp8_slice",
+             "mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
              "dsv3": "deepseek_v3_moe_layer_int4", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
 
 

@@ -67,6 +67,14 @@ SHAPES = {
                       routing="half_to_expert0"),
 }
 
+# Tensor-parallel slices of the same layers as the pages run them (the expert
+# intermediate size split over the TP ranks; one rank's share on one GPU):
+# Mixtral-8x7B TP2, Qwen2-57B-A14B TP4, DeepSeek-V3 TP8, Llama-4-Scout TP8.
+for _base, _tp in (("mixtral", 2), ("qwen2", 4), ("dsv3", 8), ("scout", 8)):
+    _s = SHAPES[_base]
+    SHAPES[f"{_base}_tp{_tp}"] = dataclasses.replace(_s, name=f"{_base}_tp{_tp}", I=_s.I // _tp)
+del _base, _tp, _s
+
 T_SWEEP = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 
 

@@ -181,7 +181,11 @@ def test_align_block_size_matches_oracle(dev):
 # ----------------------------------------------------------------- full sizes
 
 FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), ("qwen2", 700),
-              ("dsv3", 2), ("dsv3", 129), ("scout", 3), ("scout", 1024)]
+              ("dsv3", 2), ("dsv3", 129), ("scout", 3), ("scout", 1024),
+              # tensor-parallel slices (I split over 2..8 ranks): short K in the down GEMM,
+              # few weight blocks per expert
+              ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
+              ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("scout_tp8", 32), ("scout_tp8", 4096)]
 
 
 @pytest.mark.parametrize("name,T", FULL_CASES)
