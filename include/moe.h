@@ -194,7 +194,11 @@ size_t moe_padded_capacity(const moe_problem_t* p, int32_t block);
  *                          int4: codes times group scales, rounded to bf16)
  *   act[r, i] = silu(h[i]) * h[I + i],  silu(z) = z / (1 + exp(-z))
  * act is bf16 [S, I], or for fp8 the e4m3 code of act / a2.
- * Uses ws for split-K partial sums when the expert row counts are small. */
+ * Uses ws for split-K partial sums when the expert row counts are small.
+ * offsets need not come from moe_align_permute: any nondecreasing int32
+ * [E + 1] with offsets[0] = 0 and offsets[E] = S works, e.g. rows an
+ * expert-parallel dispatch delivered for a rank's E local experts (then set
+ * T = rows received and top_k = 1 in p).  Same for moe_grouped_gemm_down. */
 moe_status_t moe_grouped_gemm_swiglu(const moe_problem_t* p, const moe_weights_t* w,
                                      const void* x_perm, const int32_t* offsets, void* act,
                                      void* ws, size_t ws_bytes, moe_stream_t stream);
