@@ -102,6 +102,29 @@ def unpack_int4(packed: np.ndarray) -> np.ndarray:
     return out
 
 
+def unpack_uint4(packed: np.ndarray) -> np.ndarray:
+    """uint8 [..., K/2] -> int64 codes [..., K] in [0, 15]; low nibble = even k
+    (the unsigned codes of the zero-point format)."""
+    p = np.asarray(packed).astype(np.int64)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.int64)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = (p >> 4) & 0xF
+    return out
+
+
+def decode_int4_grouped_zp(packed: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+                           group_size: int) -> np.ndarray:
+    """Asymmetric int4 (AWQ / GPTQ style): unsigned codes q in [0, 15], one fp16
+    scale s and one integer zero point z in [0, 15] per group of `group_size`
+    along K; w = (q - z) * s."""
+    q = unpack_uint4(packed).astype(np.float64)
+    s = decode_fp16(scales)
+    z = np.asarray(zeros).astype(np.float64)
+    K = q.shape[-1]
+    assert s.shape[-1] * group_size == K and z.shape == s.shape, (s.shape, z.shape, K, group_size)
+    return (q - np.repeat(z, group_size, axis=-1)) * np.repeat(s, group_size, axis=-1)
+
+
 def decode_int4_grouped(packed: np.ndarray, scales: np.ndarray, group_size: int) -> np.ndarray:
     """Packed int4 [..., K/2] with fp16 scales [..., K/G] -> float64 [..., K]."""
     q = unpack_int4(packed).astype(np.float64)

@@ -48,7 +48,7 @@ import time
 
 import numpy as np
 
-from .codecs import decode_bf16, decode_e4m3, decode_int4_grouped, encode_e4m3
+from .codecs import decode_bf16, decode_e4m3, decode_int4_grouped, decode_int4_grouped_zp, encode_e4m3
 
 NEAR_TIE = 4e-6
 
@@ -221,10 +221,11 @@ def align_block_size(counts: np.ndarray, offsets: np.ndarray, perm: np.ndarray, 
 class ExpertWeights:
     """Decodes one expert's weights to exact float64 on demand."""
 
-    def __init__(self, p: Problem, w13, w2, w13_scale=None, w2_scale=None):
+    def __init__(self, p: Problem, w13, w2, w13_scale=None, w2_scale=None, w13_zero=None, w2_zero=None):
         self.p = p
         self.w13, self.w2 = w13, w2
         self.s13, self.s2 = w13_scale, w2_scale
+        self.z13, self.z2 = w13_zero, w2_zero  # int4 zero points (None: signed codes)
         self.prep_seconds = 0.0
 
     def __call__(self, e: int):
@@ -236,6 +237,9 @@ class ExpertWeights:
         elif p.wdtype == "fp8":
             W13 = decode_e4m3(self.w13[e]) * float(np.float32(self.s13[e]))
             W2 = decode_e4m3(self.w2[e]) * float(np.float32(self.s2[e]))
+        elif p.wdtype == "int4" and self.z13 is not None:
+            W13 = decode_int4_grouped_zp(self.w13[e], self.s13[e], self.z13[e], p.group_size)
+            W2 = decode_int4_grouped_zp(self.w2[e], self.s2[e], self.z2[e], p.group_size)
         elif p.wdtype == "int4":
             W13 = decode_int4_grouped(self.w13[e], self.s13[e], p.group_size)
             W2 = decode_int4_grouped(self.w2[e], self.s2[e], p.group_size)

@@ -49,6 +49,7 @@ class MoEShape:
     has_bias: bool = False
     routing: str = "iid"      # "iid" | "half_to_expert0"
     weight_sd: float = 0.02
+    zero_point: bool = False  # int4 only: unsigned codes with per-group zero points
 
 
 SHAPES = {
@@ -66,6 +67,10 @@ SHAPES = {
     "scout": MoEShape("scout", H=5120, I=8192, E=16, top_k=1, scoring="sigmoid", renormalize=False,
                       routing="half_to_expert0"),
 }
+
+# DeepSeek-V3 with asymmetric AWQ-style int4 (unsigned codes, per-group zero
+# points), the format of the DeepSeek-V3-AWQ checkpoints the pages benchmark.
+SHAPES["dsv3_awq"] = dataclasses.replace(SHAPES["dsv3"], name="dsv3_awq", zero_point=True)
 
 # Tensor-parallel slices of the same layers as the pages run them (the expert
 # intermediate size split over the TP ranks; one rank's share on one GPU):
@@ -107,6 +112,8 @@ class Weights:
     w2: torch.Tensor
     w13_scale: torch.Tensor | None = None
     w2_scale: torch.Tensor | None = None
+    w13_zero: torch.Tensor | None = None  # int4 with zero points: uint8 [E, 2I, H/G]
+    w2_zero: torch.Tensor | None = None   # uint8 [E, H, I/G]
 
 
 def _pack_int4(codes: torch.Tensor) -> torch.Tensor:
@@ -115,6 +122,21 @@ def _pack_int4(codes: torch.Tensor) -> torch.Tensor:
     lo = u[..., 0::2]
     hi = u[..., 1::2]
     return lo | (hi << 4)
+
+
+def _encode_expert_zp(w: torch.Tensor, group_size: int):
+    """Asymmetric int4 of one fp32 matrix [rows, K]: per group of `group_size`
+    along K, s = (max - min) / 15 (fp16), z = round(-min / s) in [0, 15],
+    q = round(w / s) + z clamped to [0, 15]; returns (packed uint8, s, z)."""
+    rows, K = w.shape
+    g = w.reshape(rows, K // group_size, group_size)
+    lo, hi = g.amin(dim=-1), g.amax(dim=-1)
+    s16 = ((hi - lo) / 15.0).clamp_min(2.0 ** -14).to(torch.float16)
+    sf = s16.float()
+    z = torch.round(-lo / sf).clamp(0, 15)
+    q = (torch.round(g / sf.unsqueeze(-1)) + z.unsqueeze(-1)).clamp(0, 15).to(torch.uint8)
+    q = q.reshape(rows, K)
+    return q[..., 0::2] | (q[..., 1::2] << 4), s16, z.to(torch.uint8)
 
 
 def _encode_expert(w: torch.Tensor, wdtype: str, group_size: int):
@@ -161,20 +183,31 @@ def make_weights(shape: MoEShape, device="cpu", seed: int = 0) -> Weights:
         s2 = torch.empty((E, H, I // G), dtype=torch.float16, device=device)
     else:
         raise ValueError(wd)
+    zp = wd == "int4" and shape.zero_point
+    z13 = torch.empty((E, 2 * I, H // shape.group_size), dtype=torch.uint8, device=device) if zp else None
+    z2 = torch.empty((E, H, I // shape.group_size), dtype=torch.uint8, device=device) if zp else None
     for e in range(E):
         a = torch.randn((2 * I, H), generator=gen, device=device, dtype=torch.float32) * shape.weight_sd
-        q, s = _encode_expert(a, wd, shape.group_size)
+        if zp:
+            q, s, z = _encode_expert_zp(a, shape.group_size)
+            z13[e].copy_(z)
+        else:
+            q, s = _encode_expert(a, wd, shape.group_size)
         w13[e].copy_(q)
         if s is not None:
             s13[e].copy_(s)
         del a
         b = torch.randn((H, I), generator=gen, device=device, dtype=torch.float32) * shape.weight_sd
-        q, s = _encode_expert(b, wd, shape.group_size)
+        if zp:
+            q, s, z = _encode_expert_zp(b, shape.group_size)
+            z2[e].copy_(z)
+        else:
+            q, s = _encode_expert(b, wd, shape.group_size)
         w2[e].copy_(q)
         if s is not None:
             s2[e].copy_(s)
         del b
-    return Weights(wd, w13, w2, s13, s2)
+    return Weights(wd, w13, w2, s13, s2, z13, z2)
 
 
 @dataclasses.dataclass

@@ -41,6 +41,9 @@ class LazyExperts(ExpertWeights):
         if w.w13_scale is not None:
             self.s13 = {e: np_of(w.w13_scale[e])}
             self.s2 = {e: np_of(w.w2_scale[e])}
+        if getattr(w, "w13_zero", None) is not None:
+            self.z13 = {e: np_of(w.w13_zero[e])}
+            self.z2 = {e: np_of(w.w2_zero[e])}
         return super().__call__(e)
 
 

@@ -1,5 +1,7 @@
 """Pins for the oracle's number-format codecs against library casts and closed forms."""
 import numpy as np
+
+import oracle
 import pytest
 import torch
 
@@ -92,3 +94,58 @@ def test_int4_grouped_decode_brute_force():
     # symmetric quantisation error is at most half a step per element
     step = np.repeat(s16.float().numpy(), 128, axis=1)
     assert np.all(np.abs(deq - w.numpy()) <= step * 0.5 + 1e-12)
+
+
+# ------------------------------------------------------ int4 with zero points
+
+def test_unpack_uint4_all_bytes():
+    b = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    q = oracle.unpack_uint4(b)
+    assert q.shape == (1, 512)
+    for v in range(256):
+        assert q[0, 2 * v] == v & 0xF and q[0, 2 * v + 1] == v >> 4
+
+
+def test_decode_zp_brute_force():
+    rng = np.random.default_rng(5)
+    rows, K, G = 3, 256, 128
+    packed = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    scales = rng.uniform(1e-3, 2e-2, (rows, K // G)).astype(np.float16)
+    zeros = rng.integers(0, 16, (rows, K // G), dtype=np.uint8)
+    got = oracle.decode_int4_grouped_zp(packed, scales.view(np.uint16), zeros, G)
+    for r in range(rows):
+        for k in range(K):
+            byte = int(packed[r, k // 2])
+            q = (byte >> 4) if k % 2 else (byte & 0xF)
+            want = (q - int(zeros[r, k // G])) * float(scales[r, k // G])
+            assert got[r, k] == want
+
+
+def test_zero_point_eight_on_flipped_nibbles_is_the_signed_format():
+    # a two's-complement nibble n read as unsigned after flipping bit 3 is n + 8,
+    # so (q - 8) * s with q = nibble ^ 8 reproduces the symmetric signed decode
+    rng = np.random.default_rng(6)
+    packed = rng.integers(0, 256, (4, 128), dtype=np.uint8)
+    scales = rng.uniform(1e-3, 2e-2, (4, 2)).astype(np.float16).view(np.uint16)
+    sym = oracle.decode_int4_grouped(packed, scales, 128)
+    zp = oracle.decode_int4_grouped_zp(packed ^ np.uint8(0x88), scales, np.full((4, 2), 8, np.uint8), 128)
+    assert np.array_equal(sym, zp)
+
+
+def test_zero_point_zero_gives_nonnegative_multiples():
+    packed = np.arange(64, dtype=np.uint8).reshape(1, 64)
+    scales = np.array([[np.float16(0.5)]]).view(np.uint16)
+    w = oracle.decode_int4_grouped_zp(packed, scales, np.zeros((1, 1), np.uint8), 128)
+    assert (w >= 0).all() and w.max() == 7.5  # q = 15 at most, times 0.5
+
+
+def test_zero_point_input_encoding_round_trips_within_half_a_step():
+    from synth.inputs import _encode_expert_zp
+    g = torch.Generator().manual_seed(2)
+    w = torch.randn(6, 256, generator=g) * 0.02
+    packed, s, z = _encode_expert_zp(w, 128)
+    assert int(z.max()) <= 15
+    dec = oracle.decode_int4_grouped_zp(packed.numpy(), s.numpy().view(np.uint16), z.numpy(), 128)
+    step = np.repeat(s.float().numpy().astype(np.float64), 128, axis=-1)
+    # rounding to the nearest level (edge groups may clamp by at most one step)
+    assert (np.abs(dec - w.double().numpy()) <= step * 1.0 + 1e-12).all()
