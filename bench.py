@@ -30,7 +30,7 @@ CONFIG_NAME = "mixtral"
 WORKLOADS = {"mixtral_tp2": "mixtral_8x7b_moe_layer_tp2_slice", "qwen2_tp4": "qwen2_57b_a14b_moe_layer_fp8_tp4_slice",
              "dsv3_tp8": "deepseek_v3_moe_layer_int4_tp8_slice", "scout_tp8": "llama4_scout_moe_layer_tp8_slice",
              "mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
-             "dsv3": "deepseek_v3_moe_layer_int4", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
+             "dsv3": "deepseek_v3_moe_layer_int4", "dsv3_awq": "deepseek_v3_moe_layer_int4_zero_points", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
 
 
 def _peaks():
@@ -145,7 +145,7 @@ def layer_bytes_flops(shape, T, touched):
     elif shape.wdtype == "fp8":
         wbytes = 3 * H * I + 8
     else:
-        wbytes = 3 * H * I // 2 + 3 * H * I // shape.group_size * 2
+        wbytes = 3 * H * I // 2 + 3 * H * I // shape.group_size * (3 if shape.zero_point else 2)
     B = touched * wbytes + T * H * 2 * 2 + T * E * 4
     F = 6.0 * k * H * I * T
     return B, F
@@ -176,7 +176,8 @@ def run_ours(args):
     p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                     renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
                     routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype)
-    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+                       w.w13_zero, w.w2_zero)
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -251,7 +252,8 @@ def run_ours(args):
     stream.synchronize()
     k_ms = g0.elapsed_time(g1) / reps
     up_flops = 2.0 * S * (2 * shape.I) * shape.H
-    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0, "int4": 0.5 + 2.0 / shape.group_size}[shape.wdtype]
+    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0,
+                       "int4": 0.5 + (3.0 if shape.zero_point else 2.0) / shape.group_size}[shape.wdtype]
     abytes = 1 if shape.wdtype == "fp8" else 2
     up_bytes = touched * (2 * shape.I * shape.H * wbytes_per_elem) + S * shape.H * abytes + S * shape.I * abytes
     tensor_peak = dtype_peak
@@ -334,7 +336,8 @@ def run_ours(args):
                    "top_k": shape.top_k, "gate": f"{shape.scoring} top-{shape.top_k}" +
                    (", renormalised" if shape.renormalize else "") +
                    (f", {shape.n_group} groups keep {shape.topk_group}" if shape.n_group else ""),
-                   "weights": {"bf16": "bf16", "fp8": "e4m3 per-expert scale", "int4": "int4 group-128"}[shape.wdtype],
+                   "weights": {"bf16": "bf16", "fp8": "e4m3 per-expert scale",
+                               "int4": "int4 group-128" + (" + zero points" if shape.zero_point else "")}[shape.wdtype],
                    "global_batch": world * T, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "no flush: expert weights exceed L2 (129 MB) every step",
                    "cuda_graph": True, "plan": {"bn_max": plan.bn_max_up, "splits_up": plan.splits_up,
@@ -370,7 +373,8 @@ def run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak):
         p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                         renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
                         routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype)
-        wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+        wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+                       w.w13_zero, w.w2_zero)
         ws = moe.alloc_workspace(p, dev)
         out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
         with torch.cuda.stream(stream):
@@ -460,7 +464,9 @@ class _OracleRunner:
                     t0 = time.perf_counter()
                     sub = oracle.ExpertWeights(outer.p, {e: np_of(w.w13[e])}, {e: np_of(w.w2[e])},
                                                None if w.w13_scale is None else {e: np_of(w.w13_scale[e])},
-                                               None if w.w2_scale is None else {e: np_of(w.w2_scale[e])})
+                                               None if w.w2_scale is None else {e: np_of(w.w2_scale[e])},
+                                               None if w.w13_zero is None else {e: np_of(w.w13_zero[e])},
+                                               None if w.w2_zero is None else {e: np_of(w.w2_zero[e])})
                     outer.cache[e] = sub(e)
                     self_inner.prep_seconds += time.perf_counter() - t0
                 return outer.cache[e]

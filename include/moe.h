@@ -86,10 +86,16 @@ typedef struct {
  *          w13_scale, w2_scale float [E] (value = e4m3(code) * scale[e]);
  *          a1_scale, a2_scale: float [1] static activation scales for the
  *          token rows entering gate_up and the activation entering down.
- *   int4 : w13 uint8 [E, 2I, H/2], w2 uint8 [E, H, I/2], two signed
- *          two's-complement codes per byte, the low nibble holding the even K
- *          index; w13_scale half [E, 2I, H/128], w2_scale half [E, H, I/128]
- *          (value = code * scale, symmetric, no zero point).
+ *   int4 : w13 uint8 [E, 2I, H/2], w2 uint8 [E, H, I/2], two codes per
+ *          byte, the low nibble holding the even K index; w13_scale half
+ *          [E, 2I, H/128], w2_scale half [E, H, I/128].  With w13_zero and
+ *          w2_zero NULL the codes are signed two's complement and
+ *          value = code * scale (symmetric).  With both set (uint8
+ *          [E, 2I, H/128] and [E, H, I/128], one zero point 0..15 per group,
+ *          the shape of the scales) the codes are unsigned 0..15 and
+ *          value = (code - zero) * scale (asymmetric, AWQ-style).  Setting
+ *          only one of the two is MOE_ERR_INVALID_ARG.
+ * Zero points must be NULL for bf16 and fp8.
  * In w13, rows [0, I) are the gate projection (SiLU applied) and rows
  * [I, 2I) the up projection. */
 typedef struct {
@@ -99,6 +105,8 @@ typedef struct {
   const void* w2_scale;
   const float* a1_scale;
   const float* a2_scale;
+  const void* w13_zero;
+  const void* w2_zero;
 } moe_weights_t;
 
 /* Bytes of workspace the stage calls need (error header, align scratch,

@@ -46,7 +46,7 @@ class Problem(ctypes.Structure):
 class WeightsStruct(ctypes.Structure):
     _fields_ = [("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("w13_scale", ctypes.c_void_p),
                 ("w2_scale", ctypes.c_void_p), ("a1_scale", ctypes.c_void_p),
-                ("a2_scale", ctypes.c_void_p)]
+                ("a2_scale", ctypes.c_void_p), ("w13_zero", ctypes.c_void_p), ("w2_zero", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -131,8 +131,9 @@ def problem(T, H, I, E, top_k, scoring="softmax", renormalize=True, n_group=0, t
 class Weights:
     """Expert weights as the library reads them; keeps the tensors alive."""
 
-    def __init__(self, w13, w2, w13_scale=None, w2_scale=None, a1_scale=None, a2_scale=None):
-        self.tensors = (w13, w2, w13_scale, w2_scale, a1_scale, a2_scale)
+    def __init__(self, w13, w2, w13_scale=None, w2_scale=None, a1_scale=None, a2_scale=None,
+                 w13_zero=None, w2_zero=None):
+        self.tensors = (w13, w2, w13_scale, w2_scale, a1_scale, a2_scale, w13_zero, w2_zero)
         self.struct = WeightsStruct(*[None if t is None else t.data_ptr() for t in self.tensors])
 
 

@@ -427,6 +427,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.w_scale = static_cast<const float*>(up ? wt.w13_scale : wt.w2_scale);
   gp.q_scale = wt.a2_scale;
   gp.w4_scale = up ? wt.w13_scale : wt.w2_scale;
+  gp.w4_zero = static_cast<const uint8_t*>(up ? wt.w13_zero : wt.w2_zero);
   gp.E = p.E;
   gp.S = S;
   gp.I = p.I;
@@ -496,6 +497,9 @@ moe_status_t check_weights(const moe_problem_t& p, const moe_weights_t* w) {
   if (p.wdtype == MOE_W_INT4_G128) {
     if (!w->w13_scale || !w->w2_scale || !aligned(w->w13_scale, 2) || !aligned(w->w2_scale, 2))
       return MOE_ERR_INVALID_ARG;
+    if ((w->w13_zero == nullptr) != (w->w2_zero == nullptr)) return MOE_ERR_INVALID_ARG;
+  } else if (w->w13_zero || w->w2_zero) {
+    return MOE_ERR_INVALID_ARG;
   }
   return MOE_OK;
 }

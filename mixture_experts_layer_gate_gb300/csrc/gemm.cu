@@ -146,23 +146,24 @@ __device__ void build_tile_table(const GemmParams& p, int lane, int* tile_base, 
   }
 }
 
-// 8 packed int4 codes (low nibble first, two's complement) times a bf16 scale
-// -> 8 bf16 in k order.  One byte permute of (x, x >> 4) puts the nibbles of
-// k = 2i and 2i + 1 at the bottom of the low and high halves; masking those
-// nibbles and flipping bit 3 gives v + 8 there, and OR-ing the bf16 pattern
-// 0x4300 (= 128) makes each half the exact bf16 value 136 + v (mask, flip and
-// OR fold into one three-input logic op).  Subtracting 136 recovers v
-// exactly; the scale multiply rounds once.  Integer-pipe work is the cost that
-// matters here (bf16x2 arithmetic is far cheaper), hence 9 integer ops per
-// 8 codes.
-__device__ __forceinline__ uint4 dequant8(uint32_t x, __nv_bfloat162 s2) {
+// 8 packed int4 codes (low nibble first) -> 8 bf16 (code - zero) * scale in k
+// order.  One byte permute of (x, x >> 4) puts the nibbles of k = 2i and
+// 2i + 1 at the bottom of the low and high halves; masking them and OR-ing the
+// bf16 pattern 0x4300 (= 128) makes each half the exact bf16 value 128 + q
+// (bf16 steps by 1 on [128, 256)).  Signed two's-complement codes v are the
+// unsigned codes q = v + 8 with zero point 8, which the same logic op reaches
+// by also flipping bit 3 (`flip` = 0x43084308 instead of 0x43004300).
+// Subtracting `off` = 128 + zero recovers q - zero exactly; the scale multiply
+// rounds once.  Integer-pipe work is the cost that matters here (bf16x2
+// arithmetic is far cheaper), hence 9 integer ops per 8 codes.
+__device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t flip, __nv_bfloat162 off,
+                                          __nv_bfloat162 s2) {
   const uint32_t xs = x >> 4;
   uint32_t o[4];
-  o[0] = (__byte_perm(x, xs, 0x4400) & 0x000F000Fu) ^ 0x43084308u;  // k0, k1
-  o[1] = (__byte_perm(x, xs, 0x5511) & 0x000F000Fu) ^ 0x43084308u;  // k2, k3
-  o[2] = (__byte_perm(x, xs, 0x6622) & 0x000F000Fu) ^ 0x43084308u;  // k4, k5
-  o[3] = (__byte_perm(x, xs, 0x7733) & 0x000F000Fu) ^ 0x43084308u;  // k6, k7
-  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+  o[0] = (__byte_perm(x, xs, 0x4400) & 0x000F000Fu) ^ flip;  // k0, k1
+  o[1] = (__byte_perm(x, xs, 0x5511) & 0x000F000Fu) ^ flip;  // k2, k3
+  o[2] = (__byte_perm(x, xs, 0x6622) & 0x000F000Fu) ^ flip;  // k4, k5
+  o[3] = (__byte_perm(x, xs, 0x7733) & 0x000F000Fu) ^ flip;  // k6, k7
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&o[i]);
@@ -951,6 +952,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
+    const uint8_t* zeros = p.w4_zero;  // null: signed codes (zero point 8 after the flip)
+    const uint32_t flip = zeros ? 0x43004300u : 0x43084308u;
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
     int ci = 0, cst = 0, cs = 0, ca = 0;  // stage / slot index and their ring positions
     uint32_t cph = 0, cap = 0;
@@ -967,7 +970,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       const int nst = (nkb + kSuper - 1) / kSuper;
       const int grow = p.is_up ? (((m >> 4) & 1) * p.I + t.fb * 64 + (m >> 5) * 16 + (m & 15))
                                : (t.fb * 128 + m);
-      const __half* srow = scales + (static_cast<size_t>(t.e) * p.R + grow) * p.G;
+      const size_t grow_off = (static_cast<size_t>(t.e) * p.R + grow) * p.G;
+      const __half* srow = scales + grow_off;
       int l = grp - ui % CG;
       if (l < 0) l += CG;
       for (; l < nst && ok; l += CG) {
@@ -976,8 +980,13 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         const int kbs = t.kb0 + kSuper * l;
         const int nk = min(kSuper, t.kb1 - kbs);
         __half sc[kSuper];
+        float zf[kSuper];
 #pragma unroll
-        for (int j = 0; j < kSuper; ++j) sc[j] = srow[min(kbs + j, t.kb1 - 1) >> 1];
+        for (int j = 0; j < kSuper; ++j) {
+          const int g = min(kbs + j, t.kb1 - 1) >> 1;  // 128-wide group of k-block j
+          sc[j] = srow[g];
+          zf[j] = zeros ? static_cast<float>(zeros[grow_off + g]) : 8.0f;
+        }
         if (!mbar_wait(RFULL(cst), cph, abort_flag, p.err, 0x400u)) {
           ok = false;
           break;
@@ -1007,6 +1016,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             tc_fence_after();
           }
           const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
+          const __nv_bfloat162 off = __float2bfloat162_rn(128.0f + zf[j]);
           // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
           const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
           const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
@@ -1014,7 +1024,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           uint32_t outv[32];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const uint4 o = dequant8(w[i], s2);
+            const uint4 o = dequant8(w[i], flip, off, s2);
             outv[4 * i + 0] = o.x;
             outv[4 * i + 1] = o.y;
             outv[4 * i + 2] = o.z;

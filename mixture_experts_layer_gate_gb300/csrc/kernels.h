@@ -83,6 +83,7 @@ struct GemmParams {
   const float* w_scale;    // fp8: per-expert weight scale [E]
   const float* q_scale;    // fp8 gate_up: a2, the scale `act` is quantised with
   const void* w4_scale;    // int4: half [E, R, G]
+  const uint8_t* w4_zero;  // int4: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
   int64_t out_ld;          // elements per output row
   int64_t part_stride;     // elements between split-K slices
   int E, S, I;

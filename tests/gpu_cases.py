@@ -23,7 +23,8 @@ def lib_problem(shape, T):
 
 
 def lib_weights(w, tok):
-    return moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale)
+    return moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+                       w.w13_zero, w.w2_zero)
 
 
 @dataclasses.dataclass
@@ -115,7 +116,7 @@ def check_align(shape, ids_g, g: StageOut):
 
 
 class _NoWeights:
-    w13 = w2 = w13_scale = w2_scale = None
+    w13 = w2 = w13_scale = w2_scale = w13_zero = w2_zero = None
 
 
 def full_check(shape, T, device, seed=0, check_stages=True):

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 48
-    assert ctypes.sizeof(binding.WeightsStruct) == 48
+    assert ctypes.sizeof(binding.WeightsStruct) == 64
     assert ctypes.sizeof(binding.Plan) == 52
 
 
@@ -87,6 +87,14 @@ def test_null_and_misaligned_arguments_rejected(lib):
     pf = moe.problem(4, 256, 512, 8, 2, wdtype="fp8")
     w = binding.WeightsStruct(4096, 8192, None, None, None, None)   # fp8 needs scales
     assert lib.moe_forward(ctypes.byref(pf), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    # zero points: only for int4, and both or neither
+    w = binding.WeightsStruct(4096, 8192, None, None, None, None, 4096, 4096)
+    assert lib.moe_forward(ctypes.byref(p), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    p4 = moe.problem(4, 256, 512, 8, 2, wdtype="int4")
+    w = binding.WeightsStruct(4096, 8192, 4096, 4096, None, None, 4096, None)
+    assert lib.moe_forward(ctypes.byref(p4), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    w = binding.WeightsStruct(4096, 8192, 4096, 4096, None, None, None, 4096)
+    assert lib.moe_grouped_gemm_down(ctypes.byref(p4), ctypes.byref(w), 16, 16, 16, 256, 1 << 30, None) == 1
 
 
 def test_workspace_sizes_are_monotone_and_cover_intermediates(lib):

@@ -33,7 +33,7 @@ def small(name):
         return shrink(base, H=512, I=1024)
     if name == "qwen2":
         return shrink(base, H=384, I=256, E=16)
-    if name == "dsv3":
+    if name in ("dsv3", "dsv3_awq"):
         return dataclasses.replace(shrink(base, H=1024, I=256, E=64), n_group=8, topk_group=4)
     if name == "scout":
         return shrink(base, H=512, I=512)
@@ -45,7 +45,7 @@ def test_tiny_all_stages(dev, T):
     gc.full_check(SHAPES["tiny"], T, dev)
 
 
-@pytest.mark.parametrize("name", ["mixtral", "qwen2", "dsv3", "scout"])
+@pytest.mark.parametrize("name", ["mixtral", "qwen2", "dsv3", "dsv3_awq", "scout"])
 @pytest.mark.parametrize("T", [1, 3, 37, 300])
 def test_small_shapes_all_stages(dev, name, T):
     gc.full_check(small(name), T, dev)
@@ -181,7 +181,7 @@ def test_align_block_size_matches_oracle(dev):
 # ----------------------------------------------------------------- full sizes
 
 FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), ("qwen2", 700),
-              ("dsv3", 2), ("dsv3", 129), ("scout", 3), ("scout", 1024),
+              ("dsv3", 2), ("dsv3", 129), ("dsv3_awq", 3), ("dsv3_awq", 256), ("scout", 3), ("scout", 1024),
               # tensor-parallel slices (I split over 2..8 ranks): short K in the down GEMM,
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
@@ -206,6 +206,8 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"MOE_CONV_GROUPS": "3"}),
     ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
+    ("dsv3_awq", {"MOE_PAIR": "0"}),
+    ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
 ])
 def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
     for k, v in knobs.items():
