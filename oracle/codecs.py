@@ -14,7 +14,15 @@ Formats:
     fused moe kernel for gptq/awq"): a signed two's-complement code in
     [-8, 7], two per byte with the low nibble holding the even index; value =
     code * scale, one fp16 scale per group of 128 consecutive K elements
-    (symmetric, no zero point).
+    (symmetric).  The asymmetric form of the same page (AWQ checkpoints,
+    `zero_point` in the quantisation config): unsigned codes q in [0, 15] and
+    one integer zero point z per group, value = (q - z) * scale.
+  * int8 with a per-group scale (the 8-bit, group-128 GPTQ Mixtral-8x7B
+    checkpoint a user runs on "Optimized fused MoE Kernel, take 2"; the
+    W{4,8}A16 `moe_wna16` path of "[Kernel] add triton fused moe kernel for
+    gptq/awq"): one signed two's-complement code in [-128, 127] per byte,
+    value = code * scale; asymmetric: unsigned q in [0, 255], zero point z in
+    [0, 255], value = (q - z) * scale.  Same fp16 group scales.
 
 All decoders return exact float64 values.
 """
@@ -132,3 +140,33 @@ def decode_int4_grouped(packed: np.ndarray, scales: np.ndarray, group_size: int)
     K = q.shape[-1]
     assert s.shape[-1] * group_size == K, (s.shape, K, group_size)
     return q * np.repeat(s, group_size, axis=-1)
+
+
+def _grouped(q: np.ndarray, scales: np.ndarray, zeros, group_size: int) -> np.ndarray:
+    """(q - z) * s with s (and z) repeated over each group of `group_size` along K."""
+    s = decode_fp16(scales)
+    K = q.shape[-1]
+    assert s.shape[-1] * group_size == K, (s.shape, K, group_size)
+    w = q.astype(np.float64)
+    if zeros is not None:
+        z = np.asarray(zeros).astype(np.float64)
+        assert z.shape == s.shape, (z.shape, s.shape)
+        w = w - np.repeat(z, group_size, axis=-1)
+    return w * np.repeat(s, group_size, axis=-1)
+
+
+def int8_codes(codes: np.ndarray) -> np.ndarray:
+    """Bytes read as signed two's-complement codes in [-128, 127] (int64)."""
+    return np.asarray(codes).astype(np.uint8).view(np.int8).astype(np.int64)
+
+
+def decode_int8_grouped(codes: np.ndarray, scales: np.ndarray, group_size: int) -> np.ndarray:
+    """Symmetric int8: one signed code per byte [..., K], fp16 scales [..., K/G]."""
+    return _grouped(int8_codes(codes), scales, None, group_size)
+
+
+def decode_int8_grouped_zp(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+                           group_size: int) -> np.ndarray:
+    """Asymmetric int8: unsigned codes q in [0, 255], zero points z in [0, 255]
+    per group; w = (q - z) * s."""
+    return _grouped(np.asarray(codes).astype(np.uint8).astype(np.int64), scales, zeros, group_size)

@@ -48,7 +48,8 @@ import time
 
 import numpy as np
 
-from .codecs import decode_bf16, decode_e4m3, decode_int4_grouped, decode_int4_grouped_zp, encode_e4m3
+from .codecs import (decode_bf16, decode_e4m3, decode_int4_grouped, decode_int4_grouped_zp, decode_int8_grouped,
+                     decode_int8_grouped_zp, encode_e4m3)
 
 NEAR_TIE = 4e-6
 
@@ -65,7 +66,7 @@ class Problem:
     n_group: int = 0
     topk_group: int = 0
     routed_scaling_factor: float = 1.0
-    wdtype: str = "bf16"              # "bf16" | "fp8" | "int4"
+    wdtype: str = "bf16"              # "bf16" | "fp8" | "int4" | "int8"
     group_size: int = 128
 
     @property
@@ -225,7 +226,7 @@ class ExpertWeights:
         self.p = p
         self.w13, self.w2 = w13, w2
         self.s13, self.s2 = w13_scale, w2_scale
-        self.z13, self.z2 = w13_zero, w2_zero  # int4 zero points (None: signed codes)
+        self.z13, self.z2 = w13_zero, w2_zero  # int4 / int8 zero points (None: signed codes)
         self.prep_seconds = 0.0
 
     def __call__(self, e: int):
@@ -243,6 +244,12 @@ class ExpertWeights:
         elif p.wdtype == "int4":
             W13 = decode_int4_grouped(self.w13[e], self.s13[e], p.group_size)
             W2 = decode_int4_grouped(self.w2[e], self.s2[e], p.group_size)
+        elif p.wdtype == "int8" and self.z13 is not None:
+            W13 = decode_int8_grouped_zp(self.w13[e], self.s13[e], self.z13[e], p.group_size)
+            W2 = decode_int8_grouped_zp(self.w2[e], self.s2[e], self.z2[e], p.group_size)
+        elif p.wdtype == "int8":
+            W13 = decode_int8_grouped(self.w13[e], self.s13[e], p.group_size)
+            W2 = decode_int8_grouped(self.w2[e], self.s2[e], p.group_size)
         else:
             raise ValueError(p.wdtype)
         self.prep_seconds += time.perf_counter() - t0

@@ -43,13 +43,13 @@ class MoEShape:
     n_group: int = 0          # 0 = ungrouped
     topk_group: int = 0
     routed_scaling_factor: float = 1.0
-    wdtype: str = "bf16"      # "bf16" | "fp8" | "int4"
-    group_size: int = 128     # int4 only
+    wdtype: str = "bf16"      # "bf16" | "fp8" | "int4" | "int8"
+    group_size: int = 128     # int4 / int8 only
     logit_sd: float = 1.0
     has_bias: bool = False
     routing: str = "iid"      # "iid" | "half_to_expert0"
     weight_sd: float = 0.02
-    zero_point: bool = False  # int4 only: unsigned codes with per-group zero points
+    zero_point: bool = False  # int4 / int8: unsigned codes with per-group zero points
 
 
 SHAPES = {
@@ -112,7 +112,7 @@ class Weights:
     w2: torch.Tensor
     w13_scale: torch.Tensor | None = None
     w2_scale: torch.Tensor | None = None
-    w13_zero: torch.Tensor | None = None  # int4 with zero points: uint8 [E, 2I, H/G]
+    w13_zero: torch.Tensor | None = None  # int4 / int8 with zero points: uint8 [E, 2I, H/G]
     w2_zero: torch.Tensor | None = None   # uint8 [E, H, I/G]
 
 
@@ -124,19 +124,23 @@ def _pack_int4(codes: torch.Tensor) -> torch.Tensor:
     return lo | (hi << 4)
 
 
-def _encode_expert_zp(w: torch.Tensor, group_size: int):
-    """Asymmetric int4 of one fp32 matrix [rows, K]: per group of `group_size`
-    along K, s = (max - min) / 15 (fp16), z = round(-min / s) in [0, 15],
-    q = round(w / s) + z clamped to [0, 15]; returns (packed uint8, s, z)."""
+def _encode_expert_zp(w: torch.Tensor, group_size: int, bits: int = 4):
+    """Asymmetric int4 / int8 of one fp32 matrix [rows, K]: per group of
+    `group_size` along K, with qmax = 2^bits - 1, s = (max - min) / qmax (fp16),
+    z = round(-min / s) in [0, qmax], q = round(w / s) + z clamped to
+    [0, qmax]; returns (codes uint8, packed two per byte for int4, s, z)."""
+    qmax = (1 << bits) - 1
     rows, K = w.shape
     g = w.reshape(rows, K // group_size, group_size)
     lo, hi = g.amin(dim=-1), g.amax(dim=-1)
-    s16 = ((hi - lo) / 15.0).clamp_min(2.0 ** -14).to(torch.float16)
+    s16 = ((hi - lo) / qmax).clamp_min(2.0 ** -14).to(torch.float16)
     sf = s16.float()
-    z = torch.round(-lo / sf).clamp(0, 15)
-    q = (torch.round(g / sf.unsqueeze(-1)) + z.unsqueeze(-1)).clamp(0, 15).to(torch.uint8)
+    z = torch.round(-lo / sf).clamp(0, qmax)
+    q = (torch.round(g / sf.unsqueeze(-1)) + z.unsqueeze(-1)).clamp(0, qmax).to(torch.uint8)
     q = q.reshape(rows, K)
-    return q[..., 0::2] | (q[..., 1::2] << 4), s16, z.to(torch.uint8)
+    if bits == 4:
+        q = q[..., 0::2] | (q[..., 1::2] << 4)
+    return q, s16, z.to(torch.uint8)
 
 
 def _encode_expert(w: torch.Tensor, wdtype: str, group_size: int):
@@ -153,6 +157,12 @@ def _encode_expert(w: torch.Tensor, wdtype: str, group_size: int):
         s16 = (g.abs().amax(dim=-1) / 7.0).clamp_min(2.0 ** -14).to(torch.float16)
         q = torch.round(g / s16.float().unsqueeze(-1)).clamp(-8, 7).to(torch.int8)
         return _pack_int4(q.reshape(rows, K)), s16
+    if wdtype == "int8":
+        rows, K = w.shape
+        g = w.reshape(rows, K // group_size, group_size)
+        s16 = (g.abs().amax(dim=-1) / 127.0).clamp_min(2.0 ** -14).to(torch.float16)
+        q = torch.round(g / s16.float().unsqueeze(-1)).clamp(-128, 127).to(torch.int8)
+        return q.reshape(rows, K).view(torch.uint8), s16
     raise ValueError(wdtype)
 
 
@@ -181,15 +191,23 @@ def make_weights(shape: MoEShape, device="cpu", seed: int = 0) -> Weights:
         w2 = torch.empty((E, H, I // 2), dtype=torch.uint8, device=device)
         s13 = torch.empty((E, 2 * I, H // G), dtype=torch.float16, device=device)
         s2 = torch.empty((E, H, I // G), dtype=torch.float16, device=device)
+    elif wd == "int8":
+        G = shape.group_size
+        assert H % G == 0 and I % G == 0
+        w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=device)
+        w2 = torch.empty((E, H, I), dtype=torch.uint8, device=device)
+        s13 = torch.empty((E, 2 * I, H // G), dtype=torch.float16, device=device)
+        s2 = torch.empty((E, H, I // G), dtype=torch.float16, device=device)
     else:
         raise ValueError(wd)
-    zp = wd == "int4" and shape.zero_point
+    zp = wd in ("int4", "int8") and shape.zero_point
+    bits = 8 if wd == "int8" else 4
     z13 = torch.empty((E, 2 * I, H // shape.group_size), dtype=torch.uint8, device=device) if zp else None
     z2 = torch.empty((E, H, I // shape.group_size), dtype=torch.uint8, device=device) if zp else None
     for e in range(E):
         a = torch.randn((2 * I, H), generator=gen, device=device, dtype=torch.float32) * shape.weight_sd
         if zp:
-            q, s, z = _encode_expert_zp(a, shape.group_size)
+            q, s, z = _encode_expert_zp(a, shape.group_size, bits)
             z13[e].copy_(z)
         else:
             q, s = _encode_expert(a, wd, shape.group_size)
@@ -199,7 +217,7 @@ def make_weights(shape: MoEShape, device="cpu", seed: int = 0) -> Weights:
         del a
         b = torch.randn((H, I), generator=gen, device=device, dtype=torch.float32) * shape.weight_sd
         if zp:
-            q, s, z = _encode_expert_zp(b, shape.group_size)
+            q, s, z = _encode_expert_zp(b, shape.group_size, bits)
             z2[e].copy_(z)
         else:
             q, s = _encode_expert(b, wd, shape.group_size)

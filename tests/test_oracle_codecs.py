@@ -149,3 +149,66 @@ def test_zero_point_input_encoding_round_trips_within_half_a_step():
     step = np.repeat(s.float().numpy().astype(np.float64), 128, axis=-1)
     # rounding to the nearest level (edge groups may clamp by at most one step)
     assert (np.abs(dec - w.double().numpy()) <= step * 1.0 + 1e-12).all()
+
+
+# ---------------------------------------------------------------- int8 group-128
+
+
+def test_int8_codes_are_twos_complement_bytes():
+    b = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(b.copy()).view(torch.int8).numpy().astype(np.int64)
+    assert np.array_equal(oracle.int8_codes(b), want)
+
+
+def test_int8_grouped_decode_brute_force():
+    rng = np.random.default_rng(5)
+    rows, K, G = 3, 384, 128
+    codes = rng.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    s = rng.uniform(0.01, 2.0, size=(rows, K // G)).astype(np.float16)
+    z = rng.integers(0, 256, size=(rows, K // G), dtype=np.uint8)
+    sym = oracle.decode_int8_grouped(codes, s, G)
+    asym = oracle.decode_int8_grouped_zp(codes, s, z, G)
+    for r in range(rows):
+        for k in range(K):
+            b = int(codes[r, k])
+            sc = float(s[r, k // G])
+            assert sym[r, k] == (b - 256 if b >= 128 else b) * sc
+            assert asym[r, k] == (b - int(z[r, k // G])) * sc
+
+
+def test_int8_zero_point_128_on_flipped_sign_bits_is_the_signed_format():
+    rng = np.random.default_rng(6)
+    codes = rng.integers(0, 256, size=(4, 256), dtype=np.uint8)
+    s = rng.uniform(0.01, 1.0, size=(4, 2)).astype(np.float16)
+    z = np.full((4, 2), 128, dtype=np.uint8)
+    assert np.array_equal(oracle.decode_int8_grouped_zp(codes ^ 0x80, s, z, 128),
+                          oracle.decode_int8_grouped(codes, s, 128))
+
+
+def test_int8_agrees_with_int4_on_the_int4_range():
+    # a code in [-8, 7] means the same in both formats; same scales, same groups
+    rng = np.random.default_rng(7)
+    c = rng.integers(-8, 8, size=(5, 512))
+    s = rng.uniform(0.01, 1.0, size=(5, 4)).astype(np.float16)
+    from synth.inputs import _pack_int4
+    packed = _pack_int4(torch.from_numpy(c).to(torch.int8)).numpy()
+    assert np.array_equal(oracle.decode_int8_grouped(c.astype(np.int8).view(np.uint8), s, 128),
+                          oracle.decode_int4_grouped(packed, s, 128))
+
+
+@pytest.mark.parametrize("zp", [False, True])
+def test_int8_input_encoding_round_trips(zp):
+    from synth.inputs import _encode_expert, _encode_expert_zp
+    g = torch.Generator().manual_seed(3)
+    w = torch.randn(6, 256, generator=g) * 0.02
+    if zp:
+        q, s, z = _encode_expert_zp(w, 128, bits=8)
+        assert q.shape == w.shape
+        dec = oracle.decode_int8_grouped_zp(q.numpy(), s.numpy(), z.numpy(), 128)
+    else:
+        q, s = _encode_expert(w, "int8", 128)
+        dec = oracle.decode_int8_grouped(q.numpy(), s.numpy(), 128)
+    step = np.repeat(s.float().numpy().astype(np.float64), 128, axis=-1)
+    assert (np.abs(dec - w.double().numpy()) <= step + 1e-12).all()
+    # nearest level: most errors within half a step
+    assert np.mean(np.abs(dec - w.double().numpy()) <= 0.5 * step + 1e-9) > 0.99
