@@ -30,7 +30,8 @@ CONFIG_NAME = "mixtral"
 WORKLOADS = {"mixtral_tp2": "mixtral_8x7b_moe_layer_tp2_slice", "qwen2_tp4": "qwen2_57b_a14b_moe_layer_fp8_tp4_slice",
              "dsv3_tp8": "deepseek_v3_moe_layer_int4_tp8_slice", "scout_tp8": "llama4_scout_moe_layer_tp8_slice",
              "mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
-             "dsv3": "deepseek_v3_moe_layer_int4", "dsv3_awq": "deepseek_v3_moe_layer_int4_zero_points", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
+             "dsv3": "deepseek_v3_moe_layer_int4", "dsv3_awq": "deepseek_v3_moe_layer_int4_zero_points",
+             "mixtral_w8": "mixtral_8x7b_moe_layer_int8", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
 
 
 def _peaks():
@@ -145,7 +146,8 @@ def layer_bytes_flops(shape, T, touched):
     elif shape.wdtype == "fp8":
         wbytes = 3 * H * I + 8
     else:
-        wbytes = 3 * H * I // 2 + 3 * H * I // shape.group_size * (3 if shape.zero_point else 2)
+        wbytes = 3 * H * I // (2 if shape.wdtype == "int4" else 1) + \
+            3 * H * I // shape.group_size * (3 if shape.zero_point else 2)
     B = touched * wbytes + T * H * 2 * 2 + T * E * 4
     F = 6.0 * k * H * I * T
     return B, F
@@ -252,8 +254,8 @@ def run_ours(args):
     stream.synchronize()
     k_ms = g0.elapsed_time(g1) / reps
     up_flops = 2.0 * S * (2 * shape.I) * shape.H
-    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0,
-                       "int4": 0.5 + (3.0 if shape.zero_point else 2.0) / shape.group_size}[shape.wdtype]
+    gbytes = (3.0 if shape.zero_point else 2.0) / shape.group_size  # scale (+ zero point) per group
+    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0, "int4": 0.5 + gbytes, "int8": 1.0 + gbytes}[shape.wdtype]
     abytes = 1 if shape.wdtype == "fp8" else 2
     up_bytes = touched * (2 * shape.I * shape.H * wbytes_per_elem) + S * shape.H * abytes + S * shape.I * abytes
     tensor_peak = dtype_peak
@@ -268,7 +270,8 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": up_bytes / (k_ms / 1e3) / 1e9, "peak": hbm,
                 "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = ("grouped_gemm_w4_kernel" if shape.wdtype == "int4" else f"grouped_gemm_kernel<{shape.wdtype}>") + " (gate_up + SwiGLU)"
+    roof["kernel"] = (f"grouped_gemm_wna16_kernel<{shape.wdtype}>" if shape.wdtype in ("int4", "int8")
+                      else f"grouped_gemm_kernel<{shape.wdtype}>") + " (gate_up + SwiGLU)"
     roof["kernel_ms"] = k_ms
     roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
 
@@ -330,14 +333,15 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "int4": "bf16"}[shape.wdtype],
+        "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "int4": "bf16", "int8": "bf16"}[shape.wdtype],
         "data": "synthetic",
         "config": {"workload": WORKLOADS.get(args.config, args.config) + (f"_E{shape.E}" if args.E else ""), "T": T, "H": shape.H, "I": shape.I, "E": shape.E,
                    "top_k": shape.top_k, "gate": f"{shape.scoring} top-{shape.top_k}" +
                    (", renormalised" if shape.renormalize else "") +
                    (f", {shape.n_group} groups keep {shape.topk_group}" if shape.n_group else ""),
                    "weights": {"bf16": "bf16", "fp8": "e4m3 per-expert scale",
-                               "int4": "int4 group-128" + (" + zero points" if shape.zero_point else "")}[shape.wdtype],
+                               "int4": "int4 group-128" + (" + zero points" if shape.zero_point else ""),
+                               "int8": "int8 group-128" + (" + zero points" if shape.zero_point else "")}[shape.wdtype],
                    "global_batch": world * T, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "no flush: expert weights exceed L2 (129 MB) every step",
                    "cuda_graph": True, "plan": {"bn_max": plan.bn_max_up, "splits_up": plan.splits_up,

@@ -65,7 +65,7 @@ typedef enum {
   MOE_ERR_TIMEOUT = 6           /* a kernel pipeline wait ran out (about 1 s) */
 } moe_status_t;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_INT4_G128 = 2 } moe_wdtype_t;
+typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_INT4_G128 = 2, MOE_W_INT8_G128 = 3 } moe_wdtype_t;
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
 
 /* Problem description.  Enum-valued fields are stored as int32_t so the
@@ -77,7 +77,7 @@ typedef struct {
   int32_t n_group, topk_group;   /* 0, 0 = ungrouped selection */
   float routed_scaling_factor;   /* multiplies the final weights (1.0f = none) */
   int32_t wdtype;                /* moe_wdtype_t */
-  int32_t group_size;            /* int4 only: must be 128 */
+  int32_t group_size;            /* int4 / int8 only: must be 128 */
 } moe_problem_t;
 
 /* Expert weights (device pointers).
@@ -95,6 +95,13 @@ typedef struct {
  *          the shape of the scales) the codes are unsigned 0..15 and
  *          value = (code - zero) * scale (asymmetric, AWQ-style).  Setting
  *          only one of the two is MOE_ERR_INVALID_ARG.
+ *   int8 : w13 uint8 [E, 2I, H], w2 uint8 [E, H, I], one code per byte;
+ *          scales and zero points exactly as for int4 (zero points 0..255).
+ *          Without zero points a byte is a signed two's-complement code
+ *          (value = code * scale); with them an unsigned code
+ *          (value = (code - zero) * scale).  Int4 and int8 weights are
+ *          turned into bf16 (code - zero) * scale, rounded once, before the
+ *          bf16 tensor-core product; activations stay bf16 (W4A16 / W8A16).
  * Zero points must be NULL for bf16 and fp8.
  * In w13, rows [0, I) are the gate projection (SiLU applied) and rows
  * [I, 2I) the up projection. */

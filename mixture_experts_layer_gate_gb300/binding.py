@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BAD_INDEX", 6: "MOE_ERR_TIMEOUT"}
-WDTYPES = {"bf16": 0, "fp8": 1, "int4": 2}
+WDTYPES = {"bf16": 0, "fp8": 1, "int4": 2, "int8": 3}
 SCORING = {"softmax": 0, "sigmoid": 1}
 
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "moe_gate_topk",

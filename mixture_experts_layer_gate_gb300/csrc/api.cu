@@ -52,9 +52,11 @@ moe_status_t validate_problem(const moe_problem_t* p) {
   } else if (p->topk_group != 0) {
     return MOE_ERR_INVALID_ARG;
   }
-  if (p->wdtype != MOE_W_BF16 && p->wdtype != MOE_W_FP8_E4M3 && p->wdtype != MOE_W_INT4_G128)
+  if (p->wdtype != MOE_W_BF16 && p->wdtype != MOE_W_FP8_E4M3 && p->wdtype != MOE_W_INT4_G128 &&
+      p->wdtype != MOE_W_INT8_G128)
     return MOE_ERR_INVALID_ARG;
-  if (p->wdtype == MOE_W_INT4_G128 && p->group_size != 128) return MOE_ERR_UNSUPPORTED;
+  if ((p->wdtype == MOE_W_INT4_G128 || p->wdtype == MOE_W_INT8_G128) && p->group_size != 128)
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -127,20 +129,25 @@ int env_int(const char* name, int dflt) {
 }
 
 int wkind_of(const moe_problem_t& p) {
-  return p.wdtype == MOE_W_FP8_E4M3 ? kW_FP8 : (p.wdtype == MOE_W_INT4_G128 ? kW_INT4 : kW_BF16);
+  switch (p.wdtype) {
+    case MOE_W_FP8_E4M3: return kW_FP8;
+    case MOE_W_INT4_G128: return kW_INT4;
+    case MOE_W_INT8_G128: return kW_INT8;
+    default: return kW_BF16;
+  }
 }
 
 // Token tile limit: generous enough that one tile usually holds all of an
 // expert's tokens (each extra token block re-reads the expert's weights).
-// int4 keeps two accumulators and its converted weight tiles in TMEM, which
-// caps its token tile at 128 columns.
+// int4 / int8 keep two accumulators and the converted weight tiles in TMEM,
+// which caps their token tile at 128 columns.
 int plan_bn_max(const moe_problem_t& p) {
   const long long S = static_cast<long long>(p.T) * p.top_k;
   if (S <= 0) return 16;
   const long long touched = std::max(1ll, std::min<long long>(p.E, S));
   const long long m_avg = (S + touched - 1) / touched;
   long long bn = std::max(3 * m_avg, m_avg + 24);
-  const long long cap = (p.wdtype == MOE_W_INT4_G128) ? 128 : 256;
+  const long long cap = (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) ? 128 : 256;
   bn = std::min<long long>(cap, std::max<long long>(16, bn));
   return roundup16(static_cast<int>(bn));
 }
@@ -177,7 +184,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   const int wk = wkind_of(p);
   g.bn_max = plan_bn_max(p);
   const int bn_env = env_int("MOE_BN_MAX", 0);
-  if (bn_env >= 16 && bn_env <= (wk == kW_INT4 ? 128 : 256) && bn_env % 16 == 0) g.bn_max = bn_env;
+  if (bn_env >= 16 && bn_env <= (converts(wk) ? 128 : 256) && bn_env % 16 == 0) g.bn_max = bn_env;
   g.FB = up ? p.I / 64 : p.H / 128;
   const int K = up ? p.H : p.I;
   g.KB = K / (wk == kW_FP8 ? 128 : 64);
@@ -193,7 +200,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
-  if (wk == kW_INT4) {
+  if (converts(wk)) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of
     // slot_kb k-blocks (32 columns each).  A converter group that fills the
     // 4 / slot_kb slots of its stage jumps (groups - 1) * 4 / slot_kb slots
@@ -208,14 +215,14 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // the pace once slots hold whole stages (three groups measured no faster);
     // three are available with CTA pairs for tuning.
     g.conv_groups = 2;
-    if (cg_env == 3 && g.pair) g.conv_groups = 3;
+    if (cg_env == 3 && g.pair && wk == kW_INT4) g.conv_groups = 3;
     auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
     auto slots_fit = [&](int sk) { return std::min(kMaxSlotsInt4, free_cols / (32 * sk)); };
     g.slot_kb = (slots_fit(4) >= slots_needed(4)) ? 4 : 2;
     if ((sk_env == 2 || sk_env == 4) && slots_fit(sk_env) >= slots_needed(sk_env)) g.slot_kb = sk_env;
     if (slots_fit(g.slot_kb) < slots_needed(g.slot_kb)) g.conv_groups = 2;  // 3 groups do not fit
     g.astages = slots_fit(g.slot_kb);
-    per_stage = 16384 + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
+    per_stage = static_cast<size_t>(raw_stage_bytes(wk)) + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStagesInt4;
   } else {
     g.acc_cols = 256;
@@ -232,12 +239,12 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
   while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E) > kMaxDynSmem)
     --g.stages;
-  // int4: converter group g takes every conv_groups-th ring stage, so the ring
-  // depth must be a multiple of the group count (parity-wait rule).
-  if (wk == kW_INT4) g.stages -= g.stages % g.conv_groups;
-  // int4 whole-stage slots: converters wait on the stage ring for slot reuse,
-  // which needs at least as many ring stages as slots (parity-wait rule)
-  if (wk == kW_INT4 && g.slot_kb == kSuper && g.astages > g.stages) g.astages = g.stages;
+  // int4 / int8: converter group g takes every conv_groups-th ring stage, so
+  // the ring depth must be a multiple of the group count (parity-wait rule).
+  if (converts(wk)) g.stages -= g.stages % g.conv_groups;
+  // whole-stage slots: converters wait on the stage ring for slot reuse, which
+  // needs at least as many ring stages as slots (parity-wait rule)
+  if (converts(wk) && g.slot_kb == kSuper && g.astages > g.stages) g.astages = g.stages;
   g.smem = gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E);
   return g;
 }
@@ -379,16 +386,16 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   if (up) {
     // [E][2][I/16][16][K] viewed as dims (K, 16, 2, I/16, E): one box = 4 blocks
     // of 16 rows of gate followed by the 16 matching rows of up.
-    const uint64_t Kb = (wk == kW_INT4) ? H / 2 : (wk == kW_FP8 ? H : H * 2);  // bytes per row
+    const uint64_t Kb = (wk == kW_INT4) ? H / 2 : (wk == kW_BF16 ? H * 2 : H);  // bytes per row
     const uint64_t dimK = (wk == kW_BF16) ? H : Kb;
     uint64_t dims[5] = {dimK, 16, 2, I / 16, E};
     uint64_t str[4] = {Kb, I * Kb, 16 * Kb, 2 * I * Kb};
-    // 128 bytes of each row per box: 64 bf16, 128 e4m3, or 256 int4 codes
+    // 128 bytes of each row per box: 64 bf16, 128 e4m3 / int8, or 256 int4 codes
     uint32_t box[5] = {wk == kW_BF16 ? 64u : 128u, 16, 2, 4, 1};
     ok = encode_map(&maps.a, wk == kW_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                     5, wt.w13, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
-    const uint64_t Kb = (wk == kW_INT4) ? I / 2 : (wk == kW_FP8 ? I : I * 2);
+    const uint64_t Kb = (wk == kW_INT4) ? I / 2 : (wk == kW_BF16 ? I * 2 : I);
     const uint64_t dimK = (wk == kW_BF16) ? I : Kb;
     uint64_t dims[3] = {dimK, H, E};
     uint64_t str[2] = {Kb, H * Kb};
@@ -410,7 +417,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
       uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
       if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
     }
-    if (wk == kW_INT4) {
+    if (converts(wk)) {
       // full tiles: the token rows of 4 consecutive k-blocks in one box, viewed
       // as [K/64][S][64] so each k-block lands as its own 128-byte-swizzled tile
       uint64_t d3[3] = {64, static_cast<uint64_t>(S), K / 64};
@@ -494,7 +501,7 @@ moe_status_t check_weights(const moe_problem_t& p, const moe_weights_t* w) {
   if (p.wdtype == MOE_W_FP8_E4M3) {
     if (!w->w13_scale || !w->w2_scale || !w->a1_scale || !w->a2_scale) return MOE_ERR_INVALID_ARG;
   }
-  if (p.wdtype == MOE_W_INT4_G128) {
+  if (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) {
     if (!w->w13_scale || !w->w2_scale || !aligned(w->w13_scale, 2) || !aligned(w->w2_scale, 2))
       return MOE_ERR_INVALID_ARG;
     if ((w->w13_zero == nullptr) != (w->w2_zero == nullptr)) return MOE_ERR_INVALID_ARG;

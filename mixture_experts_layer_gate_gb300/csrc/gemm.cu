@@ -20,12 +20,12 @@
 //     warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5 drain
 //     the double-buffered accumulator (tcgen05.ld) and run the epilogue while
 //     the next unit accumulates.
-//   * int4 weights (grouped_gemm_w4_kernel): each ring stage holds 4 k-blocks
-//     of packed codes (128 bytes per weight row, one TMA row request per 256
-//     K values) plus the 4 matching token tiles; converter warp groups turn the
-//     codes and fp16 group scales into bf16 and write them straight into TMEM
-//     (tcgen05.st), and the MMA reads its A operand from TMEM.  No converted
-//     tile passes through shared memory.
+//   * int4 / int8 weights (grouped_gemm_wna16_kernel, W4A16 / W8A16): each
+//     ring stage holds 4 k-blocks of codes (128 / 256 bytes per weight row)
+//     plus the 4 matching token tiles; converter warp groups turn the codes,
+//     fp16 group scales and optional zero points into bf16 and write them
+//     straight into TMEM (tcgen05.st), and the MMA reads its A operand from
+//     TMEM.  No converted tile passes through shared memory.
 //   * gate_up: the A tile holds 64 gate rows and the 64 matching up rows,
 //     interleaved in blocks of 16 (one 5-D TMA box), so SiLU(gate) * up pairs
 //     lanes l and l + 16 of the same warp in the epilogue.
@@ -39,15 +39,15 @@ namespace moe {
 namespace {
 
 constexpr int kABytes = 16384;    // 128 rows x 128 B (bf16 / e4m3 weight tile)
-constexpr int kRawBytes = 16384;  // int4: 128 rows x 128 B of packed codes = 4 k-blocks
-constexpr int kSuper = kInt4StageKb;  // int4: k-blocks per ring stage
+constexpr int kSuper = kInt4StageKb;  // int4 / int8: k-blocks per ring stage
+constexpr int kCodeBox = 16384;       // int4 / int8: one TMA box of codes, 128 rows x 128 B
 constexpr int kStgBytesPerWarp = 2048;
 constexpr int kStgBytes = 4 * kStgBytesPerWarp;
 constexpr uint32_t kTmemCols = 512;
 
 // Shared-memory plan (offsets from a 1024-aligned base).
 //   bf16 / fp8 : ring of `stages` x {A tile 16 KB} then `stages` x {B tile bn_max x 128 B}
-//   int4       : ring of `stages` x {packed A 16 KB, 4 B tiles of bn_max x 128 B}
+//   int4 / int8: ring of `stages` x {codes 16 / 32 KB, 4 B tiles of bn_max x 128 B}
 struct SmemLayout {
   uint32_t a, r, r_stride, stg, bars, misc, tiles, total;
 };
@@ -57,10 +57,10 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
   SmemLayout L;
   uint32_t o = 0;
   const uint32_t bbytes = static_cast<uint32_t>(bn_max) * 128u;  // multiple of 2 KB
-  if (wk == kW_INT4) {
+  if (converts(wk)) {
     L.a = 0;
     L.r = o;
-    L.r_stride = kRawBytes + kSuper * bbytes;
+    L.r_stride = static_cast<uint32_t>(raw_stage_bytes(wk)) + kSuper * bbytes;
     o += stages * L.r_stride;
   } else {
     L.a = o;
@@ -173,6 +173,19 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t flip, __nv_bfloat
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 4 unsigned 8-bit codes (byte i = k i) -> 4 bf16 (code - zero) * scale in k
+// order.  A byte permute writes code q into the low byte of the float
+// 2^23 (bit pattern 0x4B000000), giving exactly 2^23 + q; subtracting
+// `zoff` = 2^23 + zero leaves q - zero exactly, the product with the fp16
+// scale (at most 9 + 11 significant bits) is exact in fp32, and the bf16
+// conversion rounds once.
+__device__ __forceinline__ uint2 dequant4_i8(uint32_t x, float zoff, float s) {
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + i)) - zoff) * s;
+  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
 // Moves a ring cursor to entry `target` (>= idx) of a ring of n entries:
 // pos = target mod n, phase flips once per wrap.
 __device__ __forceinline__ void ring_advance(int& pos, uint32_t& phase, int& idx, int target, int n) {
@@ -206,12 +219,14 @@ __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const Gemm
   }
 }
 
-// Weight tile of k-block kb (bf16 / e4m3: 64 / 128 K) or super-block at kb (int4: 256 K).
+// Weight tile of k-block kb (bf16 / e4m3: 64 / 128 K), or the codes of the
+// ring stage starting at k-block kb (int4: 256 K; int8: 128 K, the first of
+// the stage's two boxes).  `kc` = byte column of the box within the row.
 template <int WK>
 __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const GemmParams& p,
                                                  const Unit& t, uint32_t dst, uint32_t bar, int kb,
                                                  uint64_t pol) {
-  const int kc = (WK == kW_INT4) ? kb * 32 : (WK == kW_FP8 ? kb * 128 : kb * 64);
+  const int kc = kb * (WK == kW_INT4 ? 32 : (WK == kW_FP8 ? 128 : 64));  // bf16: elements, else bytes
   if (p.is_up)
     tma_load_5d_hint(dst, &maps.a, bar, kc, 0, 0, t.fb * 4, t.e, pol);
   else
@@ -695,9 +710,11 @@ __global__ void __launch_bounds__(192, 1)
 // converting its own 128 weight rows into its own TMEM and staging half of the
 // token rows; converter groups of both CTAs report to the leader's AFULL, the
 // leader's commits are multicast to both CTAs.
-template <int CG, bool PAIR, int SK>
+template <int BITS, int CG, bool PAIR, int SK>
 __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
-    grouped_gemm_w4_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+    grouped_gemm_wna16_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  constexpr int WKQ = BITS == 8 ? kW_INT8 : kW_INT4;
+  constexpr uint32_t kRaw = static_cast<uint32_t>(raw_stage_bytes(WKQ));  // codes per ring stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
@@ -705,7 +722,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const int ns = p.stages;
   const int na = p.astages;
   const int brows = PAIR ? p.bn_max / 2 : p.bn_max;  // token rows this CTA stages per k-block
-  const SmemLayout L = smem_layout(kW_INT4, brows, ns, na, p.E);
+  const SmemLayout L = smem_layout(WKQ, brows, ns, na, p.E);
   const uint32_t sR = base_u32 + L.r;
   const uint32_t btile = static_cast<uint32_t>(brows) * 128u;
   const uint32_t bars = base_u32 + L.bars;
@@ -802,14 +819,18 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           const uint32_t stage = sR + st * L.r_stride;
           const bool full = (t.n == brows);
           const uint32_t bbytes = full ? kSuper * btile : static_cast<uint32_t>(nk * t.n) * 128u;
-          mbar_expect_tx(RFULL(st), kRawBytes + bbytes);
-          load_weight_tile<kW_INT4>(maps, p, t, stage, RFULL(st), kbs, pol_w);
+          // int8: the stage's codes are two boxes of two k-blocks; a stage of at
+          // most two k-blocks (the end of a K range) needs only the first
+          const bool two_boxes = BITS == 8 && nk > 2;
+          mbar_expect_tx(RFULL(st), (BITS == 8 && !two_boxes ? kCodeBox : kRaw) + bbytes);
+          load_weight_tile<WKQ>(maps, p, t, stage, RFULL(st), kbs, pol_w);
+          if (two_boxes) load_weight_tile<WKQ>(maps, p, t, stage + kCodeBox, RFULL(st), kbs + 2, pol_w);
           if (full) {
-            tma_load_3d_hint(stage + kRawBytes, &maps.b, RFULL(st), 0, t.row0, kbs, pol_t);
+            tma_load_3d_hint(stage + kRaw, &maps.b, RFULL(st), 0, t.row0, kbs, pol_t);
           } else {
             // ragged last tile of an expert: 64- and 16-row boxes per k-block
             for (int j = 0; j < nk; ++j) {
-              const uint32_t dst = stage + kRawBytes + j * btile;
+              const uint32_t dst = stage + kRaw + j * btile;
               int r = 0;
               for (; r + 64 <= t.n; r += 64)
                 tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, RFULL(st),
@@ -860,7 +881,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           // thread goes from the commit straight to the next wait (the tensor
           // pipe idles while this single thread does bookkeeping).
           uint32_t afull = AFULL(as), rempty = REMPTY(st);
-          uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRawBytes) >> 4);
+          uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRaw) >> 4);
           uint32_t a_tm = a_tmem0 + slot_cols * static_cast<uint32_t>(as);
           for (int kbs = t.kb0; kbs < t.kb1; kbs += kSuper) {
             const int nk = min(kSuper, t.kb1 - kbs);
@@ -875,7 +896,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             const int as_n = (as + 1 == na) ? 0 : as + 1;
             const uint32_t aph_n = (as + 1 == na) ? (aph ^ 1u) : aph;
             const uint32_t afull_n = AFULL(as_n), rempty_n = REMPTY(st_n);
-            const uint32_t b_lo_n = bd_lo0 + ((sR + st_n * L.r_stride + kRawBytes) >> 4);
+            const uint32_t b_lo_n = bd_lo0 + ((sR + st_n * L.r_stride + kRaw) >> 4);
             const uint32_t a_tm_n = a_tmem0 + slot_cols * static_cast<uint32_t>(as_n);
             for (int jj = 1; jj < nk; ++jj)
               mma_kblock_tmem_a<PAIR>(d, a_tm + 32u * jj, b_lo + btile16 * jj, bd_hi, idesc, 1u);
@@ -894,7 +915,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         for (int kbs = t.kb0; kbs < t.kb1 && ok; kbs += kSuper) {
           const int nk = min(kSuper, t.kb1 - kbs);
           // low descriptor word of the stage's first token tile
-          const uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRawBytes) >> 4);
+          const uint32_t b_lo = bd_lo0 + ((sR + st * L.r_stride + kRaw) >> 4);
           for (int jp = 0; jp < nk; jp += SK) {
             // the converted slot's barrier also covers the stage's token rows:
             // its converter group waited for the whole stage before converting
@@ -937,12 +958,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       }
     }
   } else if (warp < 6) {
-    run_epilogue<kW_INT4>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
+    run_epilogue<WKQ>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
                           tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
   } else {
-    // --------------------------------------------- int4 -> bf16 converters
+    // ---------------------------------------- int4 / int8 -> bf16 converters
     // The CTA's stages are numbered i = 0, 1, ... in (unit, k) order; a stage of
-    // nk k-blocks fills ceil(nk / 2) TMEM slots, numbered the same way.  Group
+    // nk k-blocks fills ceil(nk / slot_kb) TMEM slots, numbered the same way.  Group
     // g (4 warps) converts the stages with i % CG == g and jumps straight from
     // one to the next: stepping through the other groups' stages one by one
     // costs hundreds of cycles each while the other groups saturate the
@@ -952,8 +973,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
-    const uint8_t* zeros = p.w4_zero;  // null: signed codes (zero point 8 after the flip)
-    const uint32_t flip = zeros ? 0x43004300u : 0x43084308u;
+    // null zero points: signed codes, read as unsigned codes (sign bit flipped)
+    // with zero point 8 (int4) or 128 (int8)
+    const uint8_t* zeros = p.w4_zero;
+    const uint32_t flip = zeros ? 0x43004300u : 0x43084308u;  // int4 (see dequant8)
+    const uint32_t flip8 = zeros ? 0u : 0x80808080u;           // int8
+    const float zdef = BITS == 8 ? 128.0f : 8.0f;
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
     int ci = 0, cst = 0, cs = 0, ca = 0;  // stage / slot index and their ring positions
     uint32_t cph = 0, cap = 0;
@@ -985,7 +1010,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         for (int j = 0; j < kSuper; ++j) {
           const int g = min(kbs + j, t.kb1 - 1) >> 1;  // 128-wide group of k-block j
           sc[j] = srow[g];
-          zf[j] = zeros ? static_cast<float>(zeros[grow_off + g]) : 8.0f;
+          zf[j] = zeros ? static_cast<float>(zeros[grow_off + g]) : zdef;
         }
         if (!mbar_wait(RFULL(cst), cph, abort_flag, p.err, 0x400u)) {
           ok = false;
@@ -1015,20 +1040,38 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             }
             tc_fence_after();
           }
-          const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
-          const __nv_bfloat162 off = __float2bfloat162_rn(128.0f + zf[j]);
-          // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
-          const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
-          const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
-          const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
           uint32_t outv[32];
+          if (BITS == 4) {
+            const __nv_bfloat162 s2 = __float2bfloat162_rn(__half2float(sc[j]));
+            const __nv_bfloat162 off = __float2bfloat162_rn(128.0f + zf[j]);
+            // 32 bytes of codes = 128-byte-swizzled chunks 2j and 2j+1 of the row
+            const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
+            const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
+            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 o = dequant8(w[i], flip, off, s2);
-            outv[4 * i + 0] = o.x;
-            outv[4 * i + 1] = o.y;
-            outv[4 * i + 2] = o.z;
-            outv[4 * i + 3] = o.w;
+            for (int i = 0; i < 8; ++i) {
+              const uint4 o = dequant8(w[i], flip, off, s2);
+              outv[4 * i + 0] = o.x;
+              outv[4 * i + 1] = o.y;
+              outv[4 * i + 2] = o.z;
+              outv[4 * i + 3] = o.w;
+            }
+          } else {
+            // 64 bytes of codes = chunks 4 (j & 1) .. + 3 of box j / 2
+            const uint8_t* rb = rrow + (j >> 1) * kCodeBox;
+            const float sf = __half2float(sc[j]);
+            const float zoff = 8388608.0f + zf[j];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint4 r = *reinterpret_cast<const uint4*>(rb + ((((j & 1) * 4 + c) ^ (m & 7)) << 4));
+              const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint2 o = dequant4_i8(w[i] ^ flip8, zoff, sf);
+                outv[8 * c + 2 * i] = o.x;
+                outv[8 * c + 2 * i + 1] = o.y;
+              }
+            }
           }
           tmem_st32(tmem_base + tlane + a_col0 + 32u * static_cast<uint32_t>(SK * a + js), outv);
           if (js == SK - 1 || j == nk - 1) {
@@ -1097,13 +1140,13 @@ cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, siz
   return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
 }
 
-template <int CG, bool PAIR, int SK>
-cudaError_t launch_w4(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
-                      cudaStream_t s) {
+template <int BITS, int CG, bool PAIR, int SK>
+cudaError_t launch_wna16(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                         cudaStream_t s) {
   static int configured = -1;
-  cudaError_t err = set_smem_attr(grouped_gemm_w4_kernel<CG, PAIR, SK>, &configured);
+  cudaError_t err = set_smem_attr(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl_cluster(grouped_gemm_w4_kernel<CG, PAIR, SK>, dim3(PAIR ? (grid & ~1) : grid),
+  return launch_pdl_cluster(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK>, dim3(PAIR ? (grid & ~1) : grid),
                             dim3(gemm_threads(kW_INT4, CG)), smem, s, PAIR ? 2u : 1u, maps, p);
 }
 
@@ -1114,7 +1157,7 @@ size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E) {
 }
 
 int gemm_threads(int wkind, int conv_groups) {
-  return wkind == kW_INT4 ? 64 + 128 + 128 * conv_groups : 192;
+  return converts(wkind) ? 64 + 128 + 128 * conv_groups : 192;
 }
 
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
@@ -1126,13 +1169,23 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
       return p.pair ? launch_pair<kW_FP8>(maps, p, grid, smem, s) : launch_dense<kW_FP8>(maps, p, grid, smem, s);
     case kW_INT4:
       if (p.slot_kb == 4) {
-        if (p.pair && p.conv_groups == 3) return launch_w4<3, true, 4>(maps, p, grid, smem, s);
-        if (p.pair && p.conv_groups == 2) return launch_w4<2, true, 4>(maps, p, grid, smem, s);
-        if (!p.pair && p.conv_groups == 2) return launch_w4<2, false, 4>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 4>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 2) return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
+        if (!p.pair && p.conv_groups == 2) return launch_wna16<4, 2, false, 4>(maps, p, grid, smem, s);
       } else if (p.slot_kb == 2) {
-        if (p.pair && p.conv_groups == 3) return launch_w4<3, true, 2>(maps, p, grid, smem, s);
-        if (p.pair && p.conv_groups == 2) return launch_w4<2, true, 2>(maps, p, grid, smem, s);
-        if (!p.pair && p.conv_groups == 2) return launch_w4<2, false, 2>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 2>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 2) return launch_wna16<4, 2, true, 2>(maps, p, grid, smem, s);
+        if (!p.pair && p.conv_groups == 2) return launch_wna16<4, 2, false, 2>(maps, p, grid, smem, s);
+      }
+      return cudaErrorInvalidValue;
+    case kW_INT8:  // two converter groups only
+      if (p.conv_groups != 2) return cudaErrorInvalidValue;
+      if (p.slot_kb == 4) {
+        if (p.pair) return launch_wna16<8, 2, true, 4>(maps, p, grid, smem, s);
+        return launch_wna16<8, 2, false, 4>(maps, p, grid, smem, s);
+      } else if (p.slot_kb == 2) {
+        if (p.pair) return launch_wna16<8, 2, true, 2>(maps, p, grid, smem, s);
+        return launch_wna16<8, 2, false, 2>(maps, p, grid, smem, s);
       }
       return cudaErrorInvalidValue;
     default:

@@ -69,10 +69,17 @@ cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pst
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
-// int4: k-blocks (64 reduction elements each) per operand ring stage.
+// int4 / int8: k-blocks (64 reduction elements each) per operand ring stage.
 constexpr int kInt4StageKb = 4;
 
-enum WKind : int { kW_BF16 = 0, kW_FP8 = 1, kW_INT4 = 2 };
+enum WKind : int { kW_BF16 = 0, kW_FP8 = 1, kW_INT4 = 2, kW_INT8 = 3 };
+
+// int4 / int8 weights are turned into bf16 by converter warps before the MMA.
+__host__ __device__ constexpr bool converts(int wk) { return wk == kW_INT4 || wk == kW_INT8; }
+// Packed weight codes per ring stage: 128 rows x kInt4StageKb k-blocks.
+__host__ __device__ constexpr int raw_stage_bytes(int wk) {
+  return wk == kW_INT8 ? 128 * kInt4StageKb * 64 : 128 * kInt4StageKb * 32;
+}
 enum EpiKind : int { kEpiSwiglu = 0, kEpiStore = 1, kEpiPartial = 2 };
 
 struct GemmParams {
@@ -82,8 +89,8 @@ struct GemmParams {
   const float* a_scale;    // fp8: activation scale of the B operand (a1 or a2)
   const float* w_scale;    // fp8: per-expert weight scale [E]
   const float* q_scale;    // fp8 gate_up: a2, the scale `act` is quantised with
-  const void* w4_scale;    // int4: half [E, R, G]
-  const uint8_t* w4_zero;  // int4: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
+  const void* w4_scale;    // int4 / int8: half [E, R, G]
+  const uint8_t* w4_zero;  // int4 / int8: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
   int64_t out_ld;          // elements per output row
   int64_t part_stride;     // elements between split-K slices
   int E, S, I;
@@ -91,25 +98,26 @@ struct GemmParams {
   int KB;                  // k blocks of the reduction
   int P;                   // split-K factor
   int bn_max;              // token tile limit: multiple of 16, <= 256
-  int stages;              // operand ring depth (int4: ring of packed A + token tiles)
-  int astages;             // int4 only: ring of converted bf16 A tiles
-  int slot_kb;             // int4 only: k-blocks per converted tile (2 or 4)
+  int stages;              // operand ring depth (int4 / int8: ring of packed A + token tiles)
+  int astages;             // int4 / int8 only: ring of converted bf16 A tiles
+  int slot_kb;             // int4 / int8 only: k-blocks per converted tile (2 or 4)
   int full_box;            // 1: always load bn_max token rows (tuning)
-  int conv_groups;         // int4 only: converter warp groups (2, or 3 with CTA pairs)
+  int conv_groups;         // int4 / int8 only: converter warp groups (2, or 3 with CTA pairs)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
-  int G;                   // int4 groups per weight row
+  int G;                   // int4 / int8 groups per weight row
 };
 
 struct GemmMaps {
   CUtensorMap a;    // weights: bf16/e4m3 tile of 128 rows x 128 B, or for int4 128 rows x
-                    // 128 B of packed codes (4 k-blocks); 128-byte swizzle
+                    // 128 B of packed codes (4 k-blocks), for int8 128 rows x 128 B of codes
+                    // (2 k-blocks, two boxes per ring stage); 128-byte swizzle
   CUtensorMap b;    // token rows (x_perm or act), box of bn_max rows: one load per full tile
-                    // (int4: 3-D view [k-block][row][64], box of 4 k-blocks)
+                    // (int4 / int8: 3-D view [k-block][row][64], box of 4 k-blocks)
   CUtensorMap b64;  // the same rows, 64-row box (ragged last tile of an expert)
   CUtensorMap b16;  // the same rows, 16-row box (ragged last tile of an expert)
 };

@@ -71,6 +71,8 @@ SHAPES = {
 # DeepSeek-V3 with asymmetric AWQ-style int4 (unsigned codes, per-group zero
 # points), the format of the DeepSeek-V3-AWQ checkpoints the pages benchmark.
 SHAPES["dsv3_awq"] = dataclasses.replace(SHAPES["dsv3"], name="dsv3_awq", zero_point=True)
+# Mixtral-8x7B with 8-bit group-128 GPTQ-style weights (W8A16, symmetric).
+SHAPES["mixtral_w8"] = dataclasses.replace(SHAPES["mixtral"], name="mixtral_w8", wdtype="int8")
 
 # Tensor-parallel slices of the same layers as the pages run them (the expert
 # intermediate size split over the TP ranks; one rank's share on one GPU):

@@ -138,7 +138,7 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             st, ast = getattr(pl, f"stages_{side}"), getattr(pl, f"astages_{side}")
             assert st >= 2
             assert getattr(pl, f"smem_{side}") <= 232448
-            if shape.wdtype == "int4":
+            if shape.wdtype in ("int4", "int8"):
                 # TMEM holds two accumulators and the converted-weight slot ring
                 sk = getattr(pl, f"slot_kb_{side}")
                 assert bn <= 128 and sk in (2, 4)

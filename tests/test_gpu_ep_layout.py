@@ -24,13 +24,14 @@ COUNTS = [0, 37, 1, 0, 300, 5]  # rows per local expert: empty, ragged, single, 
 def _local_shape(name):
     base = {"bf16": shrink(SHAPES["mixtral"], H=512, I=1024),
             "fp8": shrink(SHAPES["qwen2"], H=384, I=256),
-            "int4": shrink(SHAPES["dsv3"], H=1024, I=256)}[name]
+            "int4": shrink(SHAPES["dsv3"], H=1024, I=256),
+            "int8": shrink(SHAPES["mixtral_w8"], H=512, I=256)}[name]
     # no gate runs here: an ungrouped softmax problem with one row per "token"
     return dataclasses.replace(base, E=len(COUNTS), top_k=1, n_group=0, topk_group=0,
                                scoring="softmax", routed_scaling_factor=1.0, has_bias=False)
 
 
-@pytest.mark.parametrize("wdtype", ["bf16", "fp8", "int4"])
+@pytest.mark.parametrize("wdtype", ["bf16", "fp8", "int4", "int8"])
 def test_grouped_gemms_over_dispatched_rows(wdtype):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -51,7 +52,7 @@ def test_grouped_gemms_over_dispatched_rows(wdtype):
     else:
         x_perm = x.to(dev)
     w = make_weights(shape, dev, seed=3)
-    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, a1, a2)
+    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, a1, a2, w.w13_zero, w.w2_zero)
     offsets = torch.tensor(np.concatenate([[0], np.cumsum(COUNTS)]), dtype=torch.int32, device=dev)
     p = moe.problem(R, shape.H, shape.I, shape.E, 1, scoring="softmax", renormalize=False,
                     wdtype=shape.wdtype)

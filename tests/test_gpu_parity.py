@@ -26,10 +26,14 @@ def dev():
 
 
 def small(name):
+    if name == "mixtral_w8_zp":
+        return dataclasses.replace(small("mixtral_w8"), name="mixtral_w8_zp_small", zero_point=True)
     base = SHAPES[name]
     if name == "tiny":
         return base
     if name == "mixtral":
+        return shrink(base, H=512, I=1024)
+    if name == "mixtral_w8":
         return shrink(base, H=512, I=1024)
     if name == "qwen2":
         return shrink(base, H=384, I=256, E=16)
@@ -45,7 +49,7 @@ def test_tiny_all_stages(dev, T):
     gc.full_check(SHAPES["tiny"], T, dev)
 
 
-@pytest.mark.parametrize("name", ["mixtral", "qwen2", "dsv3", "dsv3_awq", "scout"])
+@pytest.mark.parametrize("name", ["mixtral", "qwen2", "dsv3", "dsv3_awq", "scout", "mixtral_w8", "mixtral_w8_zp"])
 @pytest.mark.parametrize("T", [1, 3, 37, 300])
 def test_small_shapes_all_stages(dev, name, T):
     gc.full_check(small(name), T, dev)
@@ -182,6 +186,7 @@ def test_align_block_size_matches_oracle(dev):
 
 FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), ("qwen2", 700),
               ("dsv3", 2), ("dsv3", 129), ("dsv3_awq", 3), ("dsv3_awq", 256), ("scout", 3), ("scout", 1024),
+              ("mixtral_w8", 1), ("mixtral_w8", 600),
               # tensor-parallel slices (I split over 2..8 ranks): short K in the down GEMM,
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
@@ -207,6 +212,9 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_PAIR": "0"}),
+    ("mixtral_w8", {"MOE_PAIR": "0"}),
+    ("mixtral_w8", {"MOE_SLOT_KB": "2"}),
+    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
 ])
 def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
