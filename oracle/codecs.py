@@ -39,6 +39,44 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
+def encode_bf16(x: np.ndarray) -> np.ndarray:
+    """Values taken exactly (float64 or float32) -> nearest bf16 bit patterns
+    (uint16), ties to even.  bf16: 1 sign bit, 8 exponent bits with bias 127,
+    7 stored mantissa bits; the quantum is 2^(e-7) for |x| in [2^e, 2^(e+1)),
+    e >= -126 (below that the subnormal quantum 2^-133); results past the
+    largest finite value (2 - 2^-7) * 2^127 round to infinity; NaN -> 0x7FC0.
+    One rounding from the exact value (no detour through float32)."""
+    with np.errstate(invalid="ignore"):
+        v = np.asarray(x).astype(np.float64)
+    nan = np.isnan(v)
+    neg = np.signbit(v)
+    inf = np.isinf(v)
+    a = np.abs(np.where(nan | inf, 0.0, v))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(np.exp2(e) > a, e - 1, e)
+    e = np.where(np.exp2(e + 1) <= a, e + 1, e)
+    e = np.maximum(e, -126.0)
+    q = np.exp2(e - 7.0)
+    r = np.rint(a / q) * q               # RNE on the exact quotient (q is a power of two)
+    over = (r >= 2.0 ** 128) | inf
+    r32 = np.where(over, np.inf, r).astype(np.float32)   # exact: r has at most 8 significant bits
+    bits = (r32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    bits = bits | np.where(neg, np.uint16(0x8000), np.uint16(0))
+    return np.where(nan, np.uint16(0x7FC0), bits).astype(np.uint16)
+
+
+def dynamic_scale(values: np.ndarray) -> float:
+    """Per-tensor dynamic fp8 scale: float32(max |v|) / 448 in float32
+    arithmetic (the largest magnitude maps to the e4m3 maximum); 1.0 when the
+    tensor is empty or all zero (any scale then quantises it to zeros)."""
+    v = np.asarray(values, dtype=np.float64)
+    amax = float(np.max(np.abs(v))) if v.size else 0.0
+    if amax == 0.0:
+        return 1.0
+    return float(np.float32(amax) / np.float32(E4M3_MAX))
+
+
 def decode_fp16(bits_or_values: np.ndarray) -> np.ndarray:
     a = np.asarray(bits_or_values)
     if a.dtype == np.uint16:

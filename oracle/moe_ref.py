@@ -49,7 +49,7 @@ import time
 import numpy as np
 
 from .codecs import (decode_bf16, decode_e4m3, decode_int4_grouped, decode_int4_grouped_zp, decode_int8_grouped,
-                     decode_int8_grouped_zp, encode_e4m3)
+                     decode_int8_grouped_zp, dynamic_scale, encode_bf16, encode_e4m3)
 
 NEAR_TIE = 4e-6
 
@@ -68,6 +68,11 @@ class Problem:
     routed_scaling_factor: float = 1.0
     wdtype: str = "bf16"              # "bf16" | "fp8" | "int4" | "int8"
     group_size: int = 128
+    act_scale: str = "static"         # fp8: "static" (given a1, a2) | "dynamic" (per-tensor amax)
+
+    @property
+    def dynamic(self) -> bool:
+        return self.wdtype == "fp8" and self.act_scale == "dynamic"
 
     @property
     def S(self) -> int:
@@ -267,19 +272,31 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def gate_up_swiglu(p: Problem, X: np.ndarray, W13: np.ndarray, a2=None) -> np.ndarray:
-    """act = silu(X W1^T) * (X W3^T), with W1 = W13[:I], W3 = W13[I:].
-
-    For fp8 W8A8 the activation is then quantised with the static scale a2 and
-    read back (the second quantisation point of the W8A8 path).
-    """
+def swiglu_act(p: Problem, X: np.ndarray, W13: np.ndarray) -> np.ndarray:
+    """act = silu(X W1^T) * (X W3^T), with W1 = W13[:I], W3 = W13[I:] (fp64)."""
     h = X @ W13.T
     I = p.I
-    act = silu(h[:, :I]) * h[:, I:]
-    if p.wdtype == "fp8":
-        a2f = float(np.float32(a2))
-        act = decode_e4m3(quantize_fp8(act, a2f)) * a2f
-    return act
+    return silu(h[:, :I]) * h[:, I:]
+
+
+def quantize_act(p: Problem, act: np.ndarray, a2) -> np.ndarray:
+    """The second quantisation point of the fp8 W8A8 path: act as the down
+    GEMM reads it.  Static: e4m3(act / a2) * a2.  Dynamic: act is first stored
+    in bf16 (the pages' fused-MoE code keeps the SwiGLU output in the model
+    dtype and quantises it in a separate pass), then e4m3(bf16(act) / a2) * a2
+    with a2 the dynamic scale of the whole bf16 tensor."""
+    if p.wdtype != "fp8":
+        return act
+    a2f = float(np.float32(a2))
+    if p.dynamic:
+        act = decode_bf16(encode_bf16(act))
+    return decode_e4m3(quantize_fp8(act, a2f)) * a2f
+
+
+def gate_up_swiglu(p: Problem, X: np.ndarray, W13: np.ndarray, a2=None) -> np.ndarray:
+    """SwiGLU activation of one expert's rows as the down GEMM reads it (fp8:
+    quantised with a2, see quantize_act)."""
+    return quantize_act(p, swiglu_act(p, X, W13), a2)
 
 
 def down(act: np.ndarray, W2: np.ndarray) -> np.ndarray:
@@ -311,7 +328,9 @@ def forward(p: Problem, x_bits, logits, bias, experts: ExpertWeights, a1=None, a
 
     `ids` overrides the gate's selection (weights are recomputed for them), for
     tokens flagged as near-ties.  `stats` receives compute and weight-decode
-    seconds separately.
+    seconds separately.  Dynamic fp8 scales (p.dynamic) ignore a1 / a2 and use
+    a1 = dynamic_scale(x) over all T tokens and a2 = dynamic_scale(bf16(act))
+    over all S rows; both are returned.
     """
     t0 = time.perf_counter()
     prep0 = experts.prep_seconds
@@ -320,16 +339,24 @@ def forward(p: Problem, x_bits, logits, bias, experts: ExpertWeights, a1=None, a
         ids = sel
     w = gate_weights(p, logits, ids)
     counts, offsets, perm, inv = align(ids, p.E)
+    if p.dynamic:
+        a1 = dynamic_scale(decode_bf16(x_bits))
     X = input_rows(p, x_bits, a1)
     x_perm = X[np.asarray(perm, dtype=np.int64) // p.top_k]
     act = np.zeros((p.S, p.I), dtype=np.float64)
     y_perm = np.zeros((p.S, p.H), dtype=np.float64)
+    W2s = {}
     for e in range(p.E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue
-        W13, W2 = experts(e)
-        act[lo:hi] = gate_up_swiglu(p, x_perm[lo:hi], W13, a2)
+        W13, W2s[e] = experts(e)
+        act[lo:hi] = swiglu_act(p, x_perm[lo:hi], W13)
+    if p.dynamic:
+        a2 = dynamic_scale(decode_bf16(encode_bf16(act)))
+    act = quantize_act(p, act, a2)
+    for e, W2 in W2s.items():
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
         y_perm[lo:hi] = down(act[lo:hi], W2)
     out = reduce(p, y_perm, inv, w)
     if stats is not None:
@@ -338,7 +365,7 @@ def forward(p: Problem, x_bits, logits, bias, experts: ExpertWeights, a1=None, a
         stats["seconds"] = total - prep
         stats["prep_seconds"] = prep
     return dict(ids=ids, w=w, ambiguous=amb, selected=sel, counts=counts, offsets=offsets,
-                perm=perm, inv=inv, x_perm=x_perm, act=act, y_perm=y_perm, out=out)
+                perm=perm, inv=inv, x_perm=x_perm, act=act, y_perm=y_perm, out=out, a1=a1, a2=a2)
 
 
 def token_outputs(p: Problem, tokens, x_bits, logits, bias, experts: ExpertWeights,
@@ -346,7 +373,9 @@ def token_outputs(p: Problem, tokens, x_bits, logits, bias, experts: ExpertWeigh
     """Output rows for a subset of tokens only (per-token definition, no permute).
 
     out[t] = sum_j w[t,j] * MLP_{ids[t,j]}(x_t); used to check sampled rows of
-    full-size runs.  `ids`, if given, is the full [T,k] id array to use.
+    full-size runs.  `ids`, if given, is the full [T,k] id array to use.  With
+    dynamic fp8 scales the caller passes a1 and a2 (they depend on the whole
+    batch); a2 = None then skips the second quantisation (act kept exact).
     """
     tokens = np.asarray(tokens, dtype=np.int64)
     lg = np.asarray(logits)[tokens]
@@ -360,7 +389,9 @@ def token_outputs(p: Problem, tokens, x_bits, logits, bias, experts: ExpertWeigh
     for e in np.unique(sel):
         W13, W2 = experts(int(e))
         rows, cols = np.nonzero(sel == e)
-        act = gate_up_swiglu(p, X[rows], W13, a2)
+        act = swiglu_act(p, X[rows], W13)
+        if not (p.dynamic and a2 is None):
+            act = quantize_act(p, act, a2)
         y = down(act, W2)
         for r, c, yy in zip(rows, cols, y):
             out[r] += w[r, c] * yy

@@ -50,6 +50,7 @@ class MoEShape:
     routing: str = "iid"      # "iid" | "half_to_expert0"
     weight_sd: float = 0.02
     zero_point: bool = False  # int4 / int8: unsigned codes with per-group zero points
+    act_scale: str = "static"  # fp8: "static" scales from the generator, or "dynamic" (computed per batch)
 
 
 SHAPES = {
@@ -73,6 +74,8 @@ SHAPES = {
 SHAPES["dsv3_awq"] = dataclasses.replace(SHAPES["dsv3"], name="dsv3_awq", zero_point=True)
 # Mixtral-8x7B with 8-bit group-128 GPTQ-style weights (W8A16, symmetric).
 SHAPES["mixtral_w8"] = dataclasses.replace(SHAPES["mixtral"], name="mixtral_w8", wdtype="int8")
+# Qwen2-57B-A14B fp8 W8A8 with dynamic per-tensor activation scales.
+SHAPES["qwen2_dyn"] = dataclasses.replace(SHAPES["qwen2"], name="qwen2_dyn", act_scale="dynamic")
 
 # Tensor-parallel slices of the same layers as the pages run them (the expert
 # intermediate size split over the TP ranks; one rank's share on one GPU):
@@ -270,7 +273,7 @@ def make_tokens(shape: MoEShape, T: int, device="cpu", seed: int = 0) -> Tokens:
     if shape.has_bias:
         bias = (torch.rand((shape.E,), generator=gen, device=device, dtype=torch.float32) * 0.2 - 0.1)
     a1 = a2 = None
-    if shape.wdtype == "fp8":
+    if shape.wdtype == "fp8" and shape.act_scale == "static":
         amax = x.float().abs().amax() if T > 0 else torch.tensor(1.0, device=device)
         a1 = (amax.clamp_min(1e-12) / 448.0).reshape(1).to(torch.float32)
         a2 = torch.full((1,), static_act_scale(shape), dtype=torch.float32, device=device)

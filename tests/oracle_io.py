@@ -9,7 +9,7 @@ def problem_for(shape, T) -> Problem:
     return Problem(T=T, H=shape.H, I=shape.I, E=shape.E, top_k=shape.top_k, scoring=shape.scoring,
                    renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
-                   group_size=shape.group_size)
+                   group_size=shape.group_size, act_scale=shape.act_scale)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
