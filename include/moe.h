@@ -67,9 +67,17 @@ typedef enum {
 
 typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_INT4_G128 = 2, MOE_W_INT8_G128 = 3 } moe_wdtype_t;
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+/* fp8 activation scales ("[kernel] introduce fused_moe_triton_splitk to
+ * sglang" and the FBGEMM grouped-GEMM blog run fp8 W8A8 with per-tensor
+ * activation scales).  STATIC: the caller passes a1 (token rows) and a2
+ * (SwiGLU output).  DYNAMIC: the library computes them per call as
+ * max |v| / 448 over the whole tensor (a1 over the T x H input rows, a2 over
+ * the S x I SwiGLU output as stored in bf16), then quantises v / scale; the
+ * SwiGLU output goes through a bf16 scratch buffer and a separate pass. */
+typedef enum { MOE_ACT_SCALE_STATIC = 0, MOE_ACT_SCALE_DYNAMIC = 1 } moe_act_scale_t;
 
 /* Problem description.  Enum-valued fields are stored as int32_t so the
- * struct layout is fixed: 12 four-byte fields, no padding. */
+ * struct layout is fixed: 13 four-byte fields, no padding. */
 typedef struct {
   int32_t T, H, I, E, top_k;
   int32_t scoring;               /* moe_score_t */
@@ -78,6 +86,7 @@ typedef struct {
   float routed_scaling_factor;   /* multiplies the final weights (1.0f = none) */
   int32_t wdtype;                /* moe_wdtype_t */
   int32_t group_size;            /* int4 / int8 only: must be 128 */
+  int32_t act_scale;             /* moe_act_scale_t; DYNAMIC only with fp8 */
 } moe_problem_t;
 
 /* Expert weights (device pointers).
@@ -85,7 +94,8 @@ typedef struct {
  *   fp8  : w13 uint8 e4m3 [E, 2I, H], w2 uint8 e4m3 [E, H, I];
  *          w13_scale, w2_scale float [E] (value = e4m3(code) * scale[e]);
  *          a1_scale, a2_scale: float [1] static activation scales for the
- *          token rows entering gate_up and the activation entering down.
+ *          token rows entering gate_up and the activation entering down;
+ *          both NULL with MOE_ACT_SCALE_DYNAMIC (see moe_dynamic_scales).
  *   int4 : w13 uint8 [E, 2I, H/2], w2 uint8 [E, H, I/2], two codes per
  *          byte, the low nibble holding the even K index; w13_scale half
  *          [E, 2I, H/128], w2_scale half [E, H, I/128].  With w13_zero and
@@ -148,7 +158,8 @@ moe_status_t moe_gate_topk(const moe_problem_t* p, const float* logits, const fl
  * expand_and_permute).  A stable counting sort of the flat slots f = t*k + j.
  *   topk_ids int32 [T, k]
  *   x        bf16 [T, H] token rows
- *   a1_scale float [1] (fp8 only, else ignored/NULL)
+ *   a1_scale float [1] (fp8 with static scales; NULL otherwise: with dynamic
+ *            scales this call computes a1 from x into the workspace)
  *   counts   int32 [E]      out: slots per expert
  *   offsets  int32 [E + 1]  out: exclusive prefix sum, offsets[E] = S
  *   perm     int32 [S]      out: row -> slot; the r-th slot (ascending f)
@@ -168,7 +179,9 @@ moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, 
  * scratch buffer to a custom operator, or a serving loop that forbids
  * cudaMalloc after start-up because it synchronises the device.  The pages
  * have no counterpart: it is a packaging variant of stage 2 only.
- *   Arguments and results are those of moe_align_permute minus ws/ws_bytes.
+ *   Arguments and results are those of moe_align_permute minus ws/ws_bytes,
+ *   except that fp8 always needs a1_scale (with dynamic scales too: there is
+ *   no workspace to compute a1 in).
  *   Its scratch (per-CTA expert histograms) is a fixed 256 KiB array in the
  *   library's device image, one per device that loads the library, held until
  *   the process exits.  Limit: ceil(T*k / 1024) * E <= 65536 (e.g. E = 256 up
@@ -240,6 +253,19 @@ moe_status_t moe_unpermute_reduce(const moe_problem_t* p, const void* y_perm, co
 moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const void* x,
                          const float* logits, const float* bias, void* out, void* ws,
                          size_t ws_bytes, moe_stream_t stream);
+
+/* Kernel launches the library has issued in this process so far, counting
+ * launches recorded into a CUDA graph once (at capture); for measurement, e.g.
+ * the launches of one moe_forward = the count's change across one call. */
+uint64_t moe_launch_count(void);
+
+/* Dynamic fp8 scales (MOE_ACT_SCALE_DYNAMIC): device pointer to float [2]
+ * inside the workspace ws, {a1, a2}.  moe_align_permute / moe_forward write
+ * a1, moe_grouped_gemm_swiglu reads a1 and writes a2, moe_grouped_gemm_down
+ * reads a2.  A caller that feeds the GEMMs with rows it quantised itself (an
+ * expert-parallel dispatch) stores its a1 there before the gate_up call.
+ * No work is launched; NULL for a NULL or misaligned ws. */
+float* moe_dynamic_scales(void* ws);
 
 /* Synchronises `stream`, returns the sticky device error recorded in ws (MOE_OK
  * if none) and clears it.  Debug/test use: it is the only blocking call. */

@@ -7,4 +7,5 @@ from .binding import (MoEError, Problem, Plan, Weights, MoELayer, load, problem,
                       workspace_size, padded_capacity, alloc_workspace, gate_topk, align_permute,
                       align_permute_noalloc,
                       align_block_size, grouped_gemm_swiglu, grouped_gemm_down, unpermute_reduce,
-                      forward, get_device_error, get_plan, status_string, EXPORTED, LIB_PATH)
+                      forward, get_device_error, get_plan, dynamic_scales, launch_count, status_string, EXPORTED,
+                      LIB_PATH)

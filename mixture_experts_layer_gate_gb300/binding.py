@@ -17,12 +17,14 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BAD_INDEX", 6: "MOE_ERR_TIMEOUT"}
 WDTYPES = {"bf16": 0, "fp8": 1, "int4": 2, "int8": 3}
+ACT_SCALES = {"static": 0, "dynamic": 1}
 SCORING = {"softmax": 0, "sigmoid": 1}
 
 EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "moe_gate_topk",
             "moe_align_permute", "moe_align_block_size", "moe_grouped_gemm_swiglu",
             "moe_grouped_gemm_down", "moe_unpermute_reduce", "moe_forward", "moe_get_device_error",
-            "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms", "moe_align_permute_noalloc")
+            "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms", "moe_align_permute_noalloc",
+            "moe_dynamic_scales", "moe_launch_count")
 
 
 class MoEError(RuntimeError):
@@ -36,7 +38,7 @@ class Problem(ctypes.Structure):
                 ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("scoring", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("n_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
-                ("wdtype", ctypes.c_int32), ("group_size", ctypes.c_int32)]
+                ("wdtype", ctypes.c_int32), ("group_size", ctypes.c_int32), ("act_scale", ctypes.c_int32)]
 
     @property
     def S(self) -> int:
@@ -87,6 +89,8 @@ def load(path: str = LIB_PATH):
         "moe_status_string": (ctypes.c_char_p, [st]),
         "moe_get_plan": (st, [P, ctypes.POINTER(Plan)]),
         "moe_get_plan_for_sms": (st, [P, i32, ctypes.POINTER(Plan)]),
+        "moe_dynamic_scales": (vp, [vp]),
+        "moe_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -122,10 +126,10 @@ def _check(status: int, where: str):
 
 
 def problem(T, H, I, E, top_k, scoring="softmax", renormalize=True, n_group=0, topk_group=0,
-            routed_scaling_factor=1.0, wdtype="bf16", group_size=128) -> Problem:
+            routed_scaling_factor=1.0, wdtype="bf16", group_size=128, act_scale="static") -> Problem:
     return Problem(int(T), int(H), int(I), int(E), int(top_k), SCORING[scoring], int(bool(renormalize)),
                    int(n_group), int(topk_group), float(routed_scaling_factor), WDTYPES[wdtype],
-                   int(group_size))
+                   int(group_size), ACT_SCALES[act_scale])
 
 
 class Weights:
@@ -208,6 +212,21 @@ def forward(p: Problem, w: Weights, x, logits, bias, out, ws, stream=None):
 def get_device_error(ws, stream=None) -> int:
     """Synchronises the stream; returns (and clears) the sticky device error code."""
     return int(load().moe_get_device_error(_ptr(ws), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernel launches the library has issued in this process (graph captures once)."""
+    return int(load().moe_launch_count())
+
+
+def dynamic_scales(ws):
+    """The workspace's dynamic fp8 scales {a1, a2} as a float32 view [2] of ws."""
+    import torch
+    ptr = load().moe_dynamic_scales(_ptr(ws))
+    if not ptr:
+        raise MoEError(1, "moe_dynamic_scales")
+    off = ptr - ws.data_ptr()
+    return ws[off: off + 8].view(torch.float32)
 
 
 def get_plan(p: Problem, num_sms: int | None = None) -> Plan:

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cmath>
 #include <mutex>
@@ -14,6 +15,12 @@
 #include "kernels.h"
 
 using namespace moe;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void moe::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -57,6 +64,8 @@ moe_status_t validate_problem(const moe_problem_t* p) {
     return MOE_ERR_INVALID_ARG;
   if ((p->wdtype == MOE_W_INT4_G128 || p->wdtype == MOE_W_INT8_G128) && p->group_size != 128)
     return MOE_ERR_UNSUPPORTED;
+  if (p->act_scale != MOE_ACT_SCALE_STATIC && p->act_scale != MOE_ACT_SCALE_DYNAMIC) return MOE_ERR_INVALID_ARG;
+  if (p->act_scale == MOE_ACT_SCALE_DYNAMIC && p->wdtype != MOE_W_FP8_E4M3) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -252,7 +261,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
 // ---------------------------------------------------------- workspace layout
 
 struct Layout {
-  size_t hdr, align_counts, partial, scratch_end;
+  size_t hdr, align_counts, partial, act_bf16, scratch_end;
   size_t ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, total;
 };
 
@@ -276,6 +285,9 @@ Layout layout_of(const moe_problem_t& p) {
   o = align256(o + static_cast<size_t>(std::max(1, align_blocks(static_cast<int>(S)))) * p.E * 4);
   L.partial = o;
   o = align256(o + std::max(partial_bytes(p, true), partial_bytes(p, false)));
+  // dynamic fp8 scales: the SwiGLU output in bf16 before its scale is known
+  L.act_bf16 = o;
+  if (p.act_scale == MOE_ACT_SCALE_DYNAMIC) o = align256(o + S * p.I * 2);
   L.scratch_end = o;
   L.ids = o;
   o = align256(o + S * 4);
@@ -303,6 +315,9 @@ template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
+
+bool dynamic_scales(const moe_problem_t& p) { return p.act_scale == MOE_ACT_SCALE_DYNAMIC; }
+DynScales* dyn_of(void* ws) { return at<DynScales>(ws, kDynScalesOffset); }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -430,9 +445,18 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   GemmParams gp;
   gp.offsets = offsets;
   gp.err = at<uint32_t>(ws, L.hdr);
-  gp.a_scale = up ? wt.a1_scale : wt.a2_scale;
+  const bool dyn = dynamic_scales(p);
+  DynScales* ds = dyn_of(ws);
+  // dynamic scales: a1 comes from the align stage, a2 from this gate_up call,
+  // whose GEMM then writes bf16 to scratch for a separate quantisation pass
+  const float* a1 = dyn ? &ds->scale[0] : wt.a1_scale;
+  const float* a2 = dyn ? &ds->scale[1] : wt.a2_scale;
+  void* const final_out = out;
+  if (dyn && up) out = at<void>(ws, L.act_bf16);
+  gp.a_scale = up ? a1 : a2;
   gp.w_scale = static_cast<const float*>(up ? wt.w13_scale : wt.w2_scale);
-  gp.q_scale = wt.a2_scale;
+  gp.q_scale = dyn ? nullptr : wt.a2_scale;
+  gp.amax = (dyn && up) ? &ds->amax[1] : nullptr;
   gp.w4_scale = up ? wt.w13_scale : wt.w2_scale;
   gp.w4_zero = static_cast<const uint8_t*>(up ? wt.w13_zero : wt.w2_zero);
   gp.E = p.E;
@@ -483,7 +507,8 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   if (g.P > 1) {
     if (up) {
-      err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8, out, s);
+      err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8 && !dyn, out,
+                                 gp.amax, s);
     } else if (defer != nullptr) {
       defer->part = part;  // the caller folds the slice sum into its reduce
       defer->P = g.P;
@@ -492,6 +517,8 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
       err = launch_down_finish(part, g.P, gp.part_stride, S, p.H, out, s);
     }
   }
+  if (err == cudaSuccess && dyn && up)
+    err = launch_quantize_e4m3_dynamic(out, static_cast<int64_t>(S) * p.I, ds, 1, final_out, s);
   return cuda_status(err);
 }
 
@@ -499,7 +526,10 @@ moe_status_t check_weights(const moe_problem_t& p, const moe_weights_t* w) {
   if (w == nullptr || w->w13 == nullptr || w->w2 == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned(w->w13, 16) || !aligned(w->w2, 16)) return MOE_ERR_INVALID_ARG;
   if (p.wdtype == MOE_W_FP8_E4M3) {
-    if (!w->w13_scale || !w->w2_scale || !w->a1_scale || !w->a2_scale) return MOE_ERR_INVALID_ARG;
+    if (!w->w13_scale || !w->w2_scale) return MOE_ERR_INVALID_ARG;
+    // static: both activation scales given; dynamic: both computed, none given
+    const bool given = w->a1_scale && w->a2_scale, none = !w->a1_scale && !w->a2_scale;
+    if (dynamic_scales(p) ? !none : !given) return MOE_ERR_INVALID_ARG;
   }
   if (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) {
     if (!w->w13_scale || !w->w2_scale || !aligned(w->w13_scale, 2) || !aligned(w->w2_scale, 2))
@@ -566,10 +596,15 @@ moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, 
     if (!topk_ids || !x || !perm || !inv || !x_perm || !aligned(x, 16) || !aligned(x_perm, 16) ||
         !aligned(perm, 4) || !aligned(inv, 4) || !aligned(topk_ids, 4))
       return MOE_ERR_INVALID_ARG;
-    if (p->wdtype == MOE_W_FP8_E4M3 && !a1_scale) return MOE_ERR_INVALID_ARG;
+    if (p->wdtype == MOE_W_FP8_E4M3 && !dynamic_scales(*p) && !a1_scale) return MOE_ERR_INVALID_ARG;
   }
-  return run_align(*p, topk_ids, x, a1_scale, counts, offsets, perm, inv, x_perm, ws,
-                   reinterpret_cast<cudaStream_t>(stream));
+  if (dynamic_scales(*p) && a1_scale) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dynamic_scales(*p) && p->T > 0) {
+    MOE_TRY(cuda_status(launch_absmax_scale(x, static_cast<int64_t>(p->T) * p->H, dyn_of(ws), 0, s)));
+    a1_scale = &dyn_of(ws)->scale[0];
+  }
+  return run_align(*p, topk_ids, x, a1_scale, counts, offsets, perm, inv, x_perm, ws, s);
 }
 
 moe_status_t moe_align_block_size(const moe_problem_t* p, const int32_t* offsets,
@@ -644,15 +679,20 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
   void* x_perm = at<void>(ws, L.x_perm);
   void* act = at<void>(ws, L.act);
   void* y_perm = at<void>(ws, L.y_perm);
+  const float* a1 = w->a1_scale;
+  if (dynamic_scales(*p)) {
+    MOE_TRY(cuda_status(launch_absmax_scale(x, static_cast<int64_t>(p->T) * p->H, dyn_of(ws), 0, s)));
+    a1 = &dyn_of(ws)->scale[0];
+  }
   if (p->T * p->top_k <= kRouteMaxSlots) {
     // small batch: gate, histogram, offsets and permutation in one CTA (results
     // identical to the two-step path below), then the row gather
-    const AlignArgs aa = align_args(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws);
+    const AlignArgs aa = align_args(*p, ids, x, a1, counts, offsets, perm, inv, x_perm, ws);
     MOE_TRY(cuda_status(launch_route_small(gate_args(*p, logits, bias, ids, tw), aa, s)));
     MOE_TRY(cuda_status(launch_gather(aa, s)));
   } else {
     MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
-    MOE_TRY(run_align(*p, ids, x, w->a1_scale, counts, offsets, perm, inv, x_perm, ws, s));
+    MOE_TRY(run_align(*p, ids, x, a1, counts, offsets, perm, inv, x_perm, ws, s));
   }
   MOE_TRY(run_gemm(*p, *w, true, x_perm, offsets, act, ws, s));
   DeferredFinish df;
@@ -661,6 +701,13 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
     return cuda_status(launch_unpermute_reduce_splitk(df.part, df.P, df.pstride, inv, tw, p->T, p->H,
                                                       p->top_k, out, s));
   return cuda_status(launch_unpermute_reduce(y_perm, inv, tw, p->T, p->H, p->top_k, out, s));
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+float* moe_dynamic_scales(void* ws) {
+  if (ws == nullptr || !aligned(ws, 256)) return nullptr;
+  return dyn_of(ws)->scale;
 }
 
 moe_status_t moe_get_device_error(void* ws, moe_stream_t stream) {

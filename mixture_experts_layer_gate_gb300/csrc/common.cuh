@@ -440,6 +440,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Counts a kernel launch the library issued (moe_launch_count).
+void note_launch();
+
 // Launches `kernel` on `stream` with programmatic stream serialisation; a
 // cluster size > 1 groups consecutive CTAs into clusters along x.
 template <typename... KArgs, typename... Args>
@@ -463,7 +466,9 @@ inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (err == cudaSuccess) note_launch();
+  return err;
 }
 
 template <typename... KArgs, typename... Args>

@@ -253,12 +253,15 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
     if (!mbar_wait(tfull0 + 8u * acc, accph, abort_flag, p.err, 0x300u)) break;
     tc_fence_after();
     float sc = 1.0f, inv_q = 1.0f;
+    // e4m3 output (static a2); with dynamic scales the fp8 gate_up stores bf16
+    const bool q8 = WK == kW_FP8 && p.q_scale != nullptr;
     if (WK == kW_FP8) {
       sc = p.a_scale[0] * p.w_scale[t.e];
-      inv_q = 1.0f / p.q_scale[0];
+      if (q8) inv_q = 1.0f / p.q_scale[0];
     }
     const uint32_t tbase =
         tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_cols);
+    uint32_t mx = 0;  // dynamic scales: largest stored |act| (bf16 magnitude bits), valid tokens only
     for (int cb = 0; cb < t.nvalid; cb += 32) {
       // two 16-column loads in flight, one wait
       uint32_t vv[2][16];
@@ -290,14 +293,18 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
           const float uu = upl ? x1 : recv;
           const float a = silu_f32(g) * uu;
           const int col = c + (upl ? 1 : 0);
-          if (WK == kW_FP8)
+          if (q8) {
             stg[col * 16 + f16] = static_cast<uint8_t>(f32x2_to_e4m3x2(a * inv_q, 0.f) & 0xFF);
-          else
-            reinterpret_cast<__nv_bfloat16*>(stg)[col * 16 + f16] = __float2bfloat16_rn(a);
+          } else {
+            const __nv_bfloat16 ab = __float2bfloat16_rn(a);
+            reinterpret_cast<__nv_bfloat16*>(stg)[col * 16 + f16] = ab;
+            if (WK == kW_FP8 && col < ntok)  // only the fp8 gate_up stores bf16 for a later scale
+              mx = max(mx, static_cast<uint32_t>(__bfloat16_as_ushort(ab)) & 0x7FFFu);
+          }
         }
         __syncwarp();
         const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16;
-        if (WK == kW_FP8) {
+        if (q8) {
           if (lane < ntok)
             *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row + lane) * p.out_ld + col) =
                 *reinterpret_cast<const uint4*>(stg + lane * 16);
@@ -346,6 +353,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       }
       __syncwarp();
     }
+    }
+    if (WK == kW_FP8 && p.amax != nullptr) {
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0 && mx != 0u) atomicMax(p.amax, mx);
     }
     tc_fence_before();
     __syncwarp();

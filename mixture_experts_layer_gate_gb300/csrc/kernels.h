@@ -60,13 +60,32 @@ cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, cons
                                     int T, int H, int k, void* out, cudaStream_t s);
 
 // Split-K finishing passes (fixed summation order over the P slices).
+// amax: dynamic fp8 scales only (bf16 act): running max of the stored |act| bits, else null.
 cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
-                                 const float* a2, int fp8, void* act, cudaStream_t s);
+                                 const float* a2, int fp8, void* act, uint32_t* amax, cudaStream_t s);
 cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H,
                                void* y, cudaStream_t s);
 // down_finish + unpermute_reduce in one pass, bit-identical to the pair.
 cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pstride, const int32_t* inv,
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s);
+
+// ------------------------------------------------- dynamic fp8 scales
+// Words in the workspace header (byte kDynScalesOffset) for dynamic per-tensor
+// activation scales; index 0 = a1 (token rows), 1 = a2 (SwiGLU output).  amax
+// and ticket are zero between calls (the last CTA of each pass clears them).
+struct DynScales {
+  uint32_t amax[2];    // largest bf16 magnitude bits seen so far
+  uint32_t ticket[2];  // CTAs finished
+  float scale[2];      // amax / 448 (1 for an all-zero tensor)
+};
+constexpr size_t kDynScalesOffset = 64;
+// scale[which] = max |x[0..n)| / 448 over bf16 x (n a multiple of 8).
+cudaError_t launch_absmax_scale(const void* x, int64_t n, DynScales* d, int which, cudaStream_t s);
+// out[i] = e4m3(x[i] / s) (round to nearest even, saturating), n a multiple of 8, with
+// s = amax[which] / 448 from the bits a producer folded in; the last CTA stores s in
+// scale[which] and clears amax and ticket.
+cudaError_t launch_quantize_e4m3_dynamic(const void* x, int64_t n, DynScales* d, int which, void* out,
+                                         cudaStream_t s);
 
 // ------------------------------------------------------------ grouped GEMM
 // int4 / int8: k-blocks (64 reduction elements each) per operand ring stage.
@@ -88,7 +107,8 @@ struct GemmParams {
   void* out;
   const float* a_scale;    // fp8: activation scale of the B operand (a1 or a2)
   const float* w_scale;    // fp8: per-expert weight scale [E]
-  const float* q_scale;    // fp8 gate_up: a2, the scale `act` is quantised with
+  const float* q_scale;    // fp8 gate_up: a2, the scale `act` is quantised with (null: store bf16)
+  uint32_t* amax;          // dynamic fp8 gate_up: running max of the stored |bf16 act| bits, or null
   const void* w4_scale;    // int4 / int8: half [E, R, G]
   const uint8_t* w4_zero;  // int4 / int8: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
   int64_t out_ld;          // elements per output row

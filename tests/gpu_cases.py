@@ -19,7 +19,7 @@ def lib_problem(shape, T):
     return moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                        renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
                        routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
-                       group_size=shape.group_size)
+                       group_size=shape.group_size, act_scale=shape.act_scale)
 
 
 def lib_weights(w, tok):
@@ -40,6 +40,7 @@ class StageOut:
     y_perm: torch.Tensor
     out: torch.Tensor
     out_forward: torch.Tensor
+    scales: np.ndarray | None = None  # dynamic fp8: {a1, a2} of the staged run (float32)
 
 
 def run_stages(shape, T, weights, tok, device) -> StageOut:
@@ -69,7 +70,11 @@ def run_stages(shape, T, weights, tok, device) -> StageOut:
     moe.forward(p, wts, tok.x, tok.logits, tok.bias, out_f, wsf)
     assert moe.get_device_error(wsf) == 0
     torch.cuda.synchronize()
-    return StageOut(ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, out, out_f)
+    scales = None
+    if shape.act_scale == "dynamic":
+        scales = moe.dynamic_scales(ws).cpu().numpy()
+        assert np.array_equal(scales, moe.dynamic_scales(wsf).cpu().numpy())
+    return StageOut(ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, out, out_f, scales)
 
 
 def rel_err(gpu, ref) -> float:
@@ -131,36 +136,39 @@ def full_check(shape, T, device, seed=0, check_stages=True):
     res = oracle.forward(p, inp["x_bits"], inp["logits"], inp["bias"], inp["experts"], inp["a1"],
                          inp["a2"], ids=ids_g)
     tol = TOL[shape.wdtype]
+    a1, a2 = inp["a1"], inp["a2"]
+    a2_g = a2
+    if shape.act_scale == "dynamic":
+        # a1 = amax(x) / 448: exact on both sides; a2 from the bf16 SwiGLU output,
+        # whose largest element may round to a neighbouring bf16 on the GPU
+        a1, a2 = res["a1"], res["a2"]
+        assert np.float32(g.scales[0]) == np.float32(a1), (g.scales[0], a1)
+        a2_g = float(g.scales[1])
+        assert abs(a2_g - a2) <= 2.0 ** -7 * a2, (a2_g, a2)
     if check_stages:
         # x_perm: exact copy (bf16) or exact e4m3 codes of x / a1
         xg = g.x_perm.cpu()
         if shape.wdtype == "fp8":
-            codes = oracle.quantize_fp8(oracle.decode_bf16(inp["x_bits"]), inp["a1"])
+            codes = oracle.quantize_fp8(oracle.decode_bf16(inp["x_bits"]), a1)
             assert np.array_equal(xg.numpy(), codes[perm // shape.top_k])
         else:
             assert np.array_equal(to_f64(xg, "bf16"), oracle.decode_bf16(inp["x_bits"])[perm // shape.top_k])
         # act from the same x_perm
-        act_g = to_f64(g.act, shape.wdtype, inp["a2"])
+        act_g = to_f64(g.act, shape.wdtype, a2_g)
         if shape.wdtype == "fp8":
-            # compare in e4m3 steps: neighbours allowed on a small fraction
+            # compare in e4m3 steps (each side's codes): neighbours allowed on a small fraction
             vals = np.sort(oracle.decode_e4m3(np.arange(256, dtype=np.uint8)))
             vals = vals[np.isfinite(vals)]
-            a2 = float(np.float32(inp["a2"]))
-            idx_g = np.searchsorted(vals, act_g / a2)
-            idx_o = np.searchsorted(vals, res["act"] / a2)
+            idx_g = np.searchsorted(vals, act_g / float(np.float32(a2_g)))
+            idx_o = np.searchsorted(vals, res["act"] / float(np.float32(a2)))
             diff = np.abs(idx_g - idx_o)
             assert diff.max() <= 1, diff.max()
             assert np.mean(diff > 0) < 0.02, np.mean(diff > 0)
         else:
             assert rel_err(act_g, res["act"]) <= tol, rel_err(act_g, res["act"])
-        # y_perm from the GPU's act (isolates the down GEMM)
-        y_ref = np.zeros_like(res["y_perm"])
-        for e in range(shape.E):
-            lo, hi = int(offsets[e]), int(offsets[e + 1])
-            if hi > lo:
-                _, W2 = inp["experts"](e)
-                y_ref[lo:hi] = oracle.down(act_g[lo:hi], W2)
-        assert rel_err(to_f64(g.y_perm, "bf16"), y_ref) <= 1e-2, rel_err(to_f64(g.y_perm, "bf16"), y_ref)
+        # y_perm against the oracle's own
+        assert rel_err(to_f64(g.y_perm, "bf16"), res["y_perm"]) <= tol, \
+            rel_err(to_f64(g.y_perm, "bf16"), res["y_perm"])
     err = rel_err(to_f64(g.out, "bf16"), res["out"])
     assert err <= tol, f"{shape.name} T={T}: out rel err {err}"
     return dict(err=err, mism=n_mism, amb=n_amb, counts=counts)
@@ -177,8 +185,25 @@ def sampled_check(shape, T, device, n_sample=4, seed=0):
     p, inp = oracle_inputs(shape, w, tok)
     rng = np.random.default_rng(T)
     rows = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, size=n_sample)]))
+    a1, a2 = inp["a1"], inp["a2"]
+    if shape.act_scale == "dynamic":
+        # a1 depends on x alone: exact.  a2 needs every row's activation, so only
+        # a bound holds here: it covers the sampled tokens' bf16 activations;
+        # the sampled outputs are compared with the activation unquantised.
+        a1 = oracle.dynamic_scale(oracle.decode_bf16(inp["x_bits"]))
+        assert np.float32(g.scales[0]) == np.float32(a1)
+        X = oracle.input_rows(p, inp["x_bits"][rows], a1)
+        sel = ids_g[rows]
+        amax = 0.0
+        for e in np.unique(sel):
+            W13, _ = inp["experts"](int(e))
+            r, _ = np.nonzero(sel == e)
+            act = oracle.decode_bf16(oracle.encode_bf16(oracle.swiglu_act(p, X[r], W13)))
+            amax = max(amax, float(np.abs(act).max()))
+        assert float(g.scales[1]) * 448.0 >= amax * (1 - 2.0 ** -7), (g.scales[1], amax)
+        a2 = None
     ref = oracle.token_outputs(p, rows, inp["x_bits"], inp["logits"], inp["bias"], inp["experts"],
-                               inp["a1"], inp["a2"], ids=ids_g)
+                               a1, a2, ids=ids_g)
     got = to_f64(g.out[torch.as_tensor(rows, device=device)], "bf16")
     err = rel_err(got, ref)
     assert err <= TOL[shape.wdtype], f"{shape.name} T={T}: sampled out rel err {err}"

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layout_matches_header():
-    assert ctypes.sizeof(binding.Problem) == 48
+    assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
     assert ctypes.sizeof(binding.Plan) == 52
 
@@ -95,6 +95,30 @@ def test_null_and_misaligned_arguments_rejected(lib):
     assert lib.moe_forward(ctypes.byref(p4), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
     w = binding.WeightsStruct(4096, 8192, 4096, 4096, None, None, None, 4096)
     assert lib.moe_grouped_gemm_down(ctypes.byref(p4), ctypes.byref(w), 16, 16, 16, 256, 1 << 30, None) == 1
+    # dynamic fp8 scales: computed, so neither activation scale may be given
+    pd = moe.problem(4, 256, 512, 8, 2, wdtype="fp8", act_scale="dynamic")
+    w = binding.WeightsStruct(4096, 8192, 4096, 4096, 4096, None)
+    assert lib.moe_forward(ctypes.byref(pd), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+    assert lib.moe_align_permute(ctypes.byref(pd), 16, 16, 16, 16, 16, 16, 16, 16, 256, 1 << 30, None) == 1
+    w = binding.WeightsStruct(4096, 8192, 4096, 4096, None, None)     # static fp8 needs both
+    assert lib.moe_forward(ctypes.byref(pf), ctypes.byref(w), 16, 16, None, 16, 256, 1 << 30, None) == 1
+
+
+def test_dynamic_scale_problems(lib):
+    # only fp8 takes dynamic scales; they add a bf16 [S, I] scratch buffer
+    assert moe.scratch_size(moe.problem(4, 256, 512, 8, 2, act_scale="dynamic")) == 0
+    assert moe.scratch_size(moe.problem(4, 256, 512, 8, 2, wdtype="int4", act_scale="dynamic")) == 0
+    bad = moe.problem(4, 256, 512, 8, 2, wdtype="fp8")
+    bad.act_scale = 2
+    assert moe.scratch_size(bad) == 0
+    for T in (1, 100, 4096):
+        st = moe.scratch_size(moe.problem(T, 256, 512, 8, 2, wdtype="fp8"))
+        dy = moe.scratch_size(moe.problem(T, 256, 512, 8, 2, wdtype="fp8", act_scale="dynamic"))
+        assert dy - st >= T * 2 * 512 * 2
+    # the scales' address is plain arithmetic on ws (no device access)
+    assert lib.moe_dynamic_scales(None) is None
+    assert lib.moe_dynamic_scales(ctypes.c_void_p(1 << 20)) == (1 << 20) + 80
+    assert lib.moe_dynamic_scales(ctypes.c_void_p((1 << 20) + 8)) is None
 
 
 def test_workspace_sizes_are_monotone_and_cover_intermediates(lib):

@@ -35,7 +35,7 @@ def small(name):
         return shrink(base, H=512, I=1024)
     if name == "mixtral_w8":
         return shrink(base, H=512, I=1024)
-    if name == "qwen2":
+    if name in ("qwen2", "qwen2_dyn"):
         return shrink(base, H=384, I=256, E=16)
     if name in ("dsv3", "dsv3_awq"):
         return dataclasses.replace(shrink(base, H=1024, I=256, E=64), n_group=8, topk_group=4)
@@ -49,7 +49,8 @@ def test_tiny_all_stages(dev, T):
     gc.full_check(SHAPES["tiny"], T, dev)
 
 
-@pytest.mark.parametrize("name", ["mixtral", "qwen2", "dsv3", "dsv3_awq", "scout", "mixtral_w8", "mixtral_w8_zp"])
+@pytest.mark.parametrize("name", ["mixtral", "qwen2", "qwen2_dyn", "dsv3", "dsv3_awq", "scout", "mixtral_w8",
+                                  "mixtral_w8_zp"])
 @pytest.mark.parametrize("T", [1, 3, 37, 300])
 def test_small_shapes_all_stages(dev, name, T):
     gc.full_check(small(name), T, dev)
@@ -81,8 +82,10 @@ def test_determinism_bitwise(dev):
         assert torch.equal(getattr(a, f), getattr(b, f)), f
 
 
-def test_cuda_graph_capture_matches_eager(dev):
-    shape = small("qwen2")
+@pytest.mark.parametrize("name", ["qwen2", "qwen2_dyn"])
+def test_cuda_graph_capture_matches_eager(dev, name):
+    # qwen2_dyn: the replays recompute the dynamic scales of the new inputs
+    shape = small(name)
     T = 50
     w = make_weights(shape, dev, 0)
     tok = make_tokens(shape, T, dev, 0)
@@ -186,11 +189,18 @@ def test_align_block_size_matches_oracle(dev):
 
 FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), ("qwen2", 700),
               ("dsv3", 2), ("dsv3", 129), ("dsv3_awq", 3), ("dsv3_awq", 256), ("scout", 3), ("scout", 1024),
-              ("mixtral_w8", 1), ("mixtral_w8", 600),
+              ("mixtral_w8", 1), ("mixtral_w8", 600), ("qwen2_dyn", 700),
               # tensor-parallel slices (I split over 2..8 ranks): short K in the down GEMM,
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
               ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("scout_tp8", 32), ("scout_tp8", 4096)]
+
+
+def test_dynamic_scales_full_size_exact(dev):
+    # Qwen2-57B-A14B at full size, one token: the oracle computes every row's
+    # activation, so a2 is compared too (not only bounded)
+    r = gc.full_check(SHAPES["qwen2_dyn"], 1, dev)
+    print(f"qwen2_dyn T=1: err={r['err']:.3e}")
 
 
 @pytest.mark.parametrize("name,T", FULL_CASES)
@@ -213,6 +223,7 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_PAIR": "0"}),
     ("mixtral_w8", {"MOE_PAIR": "0"}),
+    ("qwen2_dyn", {"MOE_PAIR": "0"}),
     ("mixtral_w8", {"MOE_SLOT_KB": "2"}),
     ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
@@ -226,3 +237,24 @@ def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
         assert plan.slot_kb_up == int(knobs["MOE_SLOT_KB"])
     for T in (37, 300):
         gc.full_check(shape, T, dev)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("tiny", 2000), ("qwen2_dyn", 37)])
+def test_launch_count_of_forward(dev, name, T):
+    # the library's own count of the kernels one moe_forward launches
+    shape = small(name)
+    w = make_weights(shape, dev, 0)
+    tok = make_tokens(shape, T, dev, 0)
+    p = gc.lib_problem(shape, T)
+    plan = moe.get_plan(p)
+    ws = moe.alloc_workspace(p, dev)
+    out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
+    n0 = moe.launch_count()
+    moe.forward(p, gc.lib_weights(w, tok), tok.x, tok.logits, tok.bias, out, ws)
+    torch.cuda.synchronize()
+    small_path = T * shape.top_k <= 1024
+    expect = (2 if small_path else 4)             # route + gather | gate + count + scatter + gather
+    expect += 1 + (plan.splits_up > 1)            # gate_up GEMM (+ split-K finish)
+    expect += 1 + 1                               # down GEMM, reduce (split-K finish folded in)
+    expect += 2 if shape.act_scale == "dynamic" else 0  # amax(x), e4m3 pass of act
+    assert moe.launch_count() - n0 == expect
