@@ -126,7 +126,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, slot_kb, conv_groups, acc_cols, pair, FB, KB;
+  int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, pair, FB, KB;
   size_t smem;
 };
 
@@ -203,6 +203,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   size_t per_stage;
   int cap;
   g.conv_groups = 0;
+  g.ksplit = 0;
   // bf16 / fp8: CTA pairs (M = 256 per MMA) whenever the weight blocks pair up.
   g.pair = 0;
   if (g.FB % 2 == 0 && env_int("MOE_PAIR", 1) != 0) {
@@ -250,7 +251,18 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     --g.stages;
   // int4 / int8: converter group g takes every conv_groups-th ring stage, so
   // the ring depth must be a multiple of the group count (parity-wait rule).
-  if (converts(wk)) g.stages -= g.stages % g.conv_groups;
+  if (converts(wk)) {
+    // Groups alternating stages need a ring depth that is a multiple of the group
+    // count.  k-split (both groups convert every stage, each half its k-blocks)
+    // has no such rule but more bookkeeping per stage (measured slower at equal
+    // depth), so it is taken only where rounding down would leave a shallow ring
+    // (int8 codes with 128-token tiles: three stages instead of two).
+    const int alt = g.stages - g.stages % g.conv_groups;
+    const int ks_env = env_int("MOE_KSPLIT", -1);
+    const bool can_ks = g.conv_groups == 2 && g.slot_kb == kSuper;
+    g.ksplit = (can_ks && (ks_env == 1 || (ks_env != 0 && alt < 4 && g.stages > alt))) ? 1 : 0;
+    if (!g.ksplit) g.stages = alt;
+  }
   // whole-stage slots: converters wait on the stage ring for slot reuse, which
   // needs at least as many ring stages as slots (parity-wait rule)
   if (converts(wk) && g.slot_kb == kSuper && g.astages > g.stages) g.astages = g.stages;
@@ -481,6 +493,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.astages = g.astages;
   gp.slot_kb = g.slot_kb;
   gp.conv_groups = g.conv_groups;
+  gp.ksplit = g.ksplit;
   gp.acc_cols = g.acc_cols;
   gp.full_box = env_int("MOE_FULL_BOX", 0) != 0 ? 1 : 0;
   gp.is_up = up ? 1 : 0;

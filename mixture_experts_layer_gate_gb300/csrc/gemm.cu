@@ -707,7 +707,11 @@ __global__ void __launch_bounds__(192, 1)
 // if the waiter is never two phases ahead of the barrier):
 //   RFULL/REMPTY over `stages` ring stages of 4 k-blocks (packed codes + token
 //   tiles).  Converter group g takes every CG-th stage; `stages` is a multiple
-//   of CG, so the previous use of a slot was by the same group.
+//   of CG, so the previous use of a slot was by the same group.  With k-split
+//   (two groups, whole-stage slots) both groups take every stage instead,
+//   group g converting its k-blocks 2g and 2g + 1, and AFULL counts all eight
+//   warps: a stage is converted in half the time, which keeps the MMA fed when
+//   TMEM holds only two whole-stage slots.
 //   AFULL/AEMPTY over `astages` TMEM slots of slot_kb (2 or 4) converted
 //   k-blocks, 128 rows x 32 * slot_kb columns each: one wait and one commit
 //   per 4 * slot_kb MMAs.  A group fills the 4 / slot_kb slots of its stage
@@ -756,7 +760,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
-  if (p.slot_kb != SK || (SK == kSuper && ns < na) || na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0 ||
+  // k-split: both groups convert every stage (group g its k-blocks 2g, 2g + 1)
+  const bool ks = p.ksplit != 0;
+  if (p.slot_kb != SK || (SK == kSuper && ns < na) || (ks && (SK != kSuper || CG != 2)) ||
+      (!ks && (na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0)) ||
       a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
     if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
     return;
@@ -768,7 +775,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
       mbar_init(REMPTY(s), 1u);
     }
     for (int s = 0; s < na; ++s) {
-      mbar_init(AFULL(s), 4u * kCtas);  // the 4 warps of one converter group (in each CTA)
+      // the 4 warps of the stage's converter group, or of both groups with k-split (in each CTA)
+      mbar_init(AFULL(s), (ks ? 4u * CG : 4u) * kCtas);
       mbar_init(AEMPTY(s), 1u);
     }
     mbar_init(tfull0, 1u);
@@ -975,7 +983,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
     // ---------------------------------------- int4 / int8 -> bf16 converters
     // The CTA's stages are numbered i = 0, 1, ... in (unit, k) order; a stage of
     // nk k-blocks fills ceil(nk / slot_kb) TMEM slots, numbered the same way.  Group
-    // g (4 warps) converts the stages with i % CG == g and jumps straight from
+    // g (4 warps) converts the stages with i % CG == g (with k-split: k-blocks
+    // 2g, 2g + 1 of every stage) and jumps straight from
     // one to the next: stepping through the other groups' stages one by one
     // costs hundreds of cycles each while the other groups saturate the
     // integer pipe.  The thread owns weight row m of the tile, which is TMEM
@@ -1008,9 +1017,9 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
                                : (t.fb * 128 + m);
       const size_t grow_off = (static_cast<size_t>(t.e) * p.R + grow) * p.G;
       const __half* srow = scales + grow_off;
-      int l = grp - ui % CG;
+      int l = ks ? 0 : grp - ui % CG;
       if (l < 0) l += CG;
-      for (; l < nst && ok; l += CG) {
+      for (; l < nst && ok; l += (ks ? 1 : CG)) {
         ring_advance(cst, cph, ci, ui + l, ns);
         ring_advance(ca, cap, cs, us + spp * l, na);  // every earlier stage of the unit is full
         const int kbs = t.kb0 + kSuper * l;
@@ -1040,9 +1049,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
         const uint8_t* rrow = base + L.r + cst * L.r_stride + m * 128;
         int a = ca;
         uint32_t ap = cap;
+        const int j0 = ks ? 2 * grp : 0;            // this warp's k-blocks of the stage: [j0, j1)
+        const int j1 = ks ? min(nk, 2 * grp + 2) : nk;
 #pragma unroll
         for (int j = 0; j < kSuper; ++j) {
-          if (j >= nk) break;
+          if (j < j0) continue;
+          if (j >= j1) break;
           const int js = j & (SK - 1);  // k-block within the slot
           if (SK != kSuper && js == 0) {
             if (!mbar_wait(AEMPTY(a), ap ^ 1u, abort_flag, p.err, 0x410u)) {
@@ -1085,7 +1097,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             }
           }
           tmem_st32(tmem_base + tlane + a_col0 + 32u * static_cast<uint32_t>(SK * a + js), outv);
-          if (js == SK - 1 || j == nk - 1) {
+          if (!ks && (js == SK - 1 || j == nk - 1)) {
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1095,6 +1107,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
               ap ^= 1u;
             }
           }
+        }
+        if (ks && ok) {  // one arrival per warp and stage, k-blocks or not
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(afull_cl0 + 8u * static_cast<uint32_t>(a));
         }
       }
       if (nst > 0) {

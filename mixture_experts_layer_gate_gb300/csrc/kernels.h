@@ -123,6 +123,8 @@ struct GemmParams {
   int slot_kb;             // int4 / int8 only: k-blocks per converted tile (2 or 4)
   int full_box;            // 1: always load bn_max token rows (tuning)
   int conv_groups;         // int4 / int8 only: converter warp groups (2, or 3 with CTA pairs)
+  int ksplit;              // int4 / int8, 2 groups, whole-stage slots: both groups convert every
+                           // stage, group g its k-blocks 2g and 2g + 1 (else groups alternate stages)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)

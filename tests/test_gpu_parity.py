@@ -211,8 +211,8 @@ def test_full_size_sampled(dev, name, T):
 
 # Kernel variants the planner does not pick for these shapes, forced through the
 # library's tuning knobs (read from the environment at every plan): the single-CTA
-# bf16/fp8 kernel (no CTA pairs), and the int4 kernel's non-pair, two-k-block-slot and
-# three-converter-group instantiations.
+# bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's non-pair,
+# two-k-block-slot, three-converter-group and alternating-stage (no k-split) modes.
 @pytest.mark.parametrize("name,knobs", [
     ("mixtral", {"MOE_PAIR": "0"}),
     ("qwen2", {"MOE_PAIR": "0"}),
@@ -224,6 +224,8 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3_awq", {"MOE_PAIR": "0"}),
     ("mixtral_w8", {"MOE_PAIR": "0"}),
     ("qwen2_dyn", {"MOE_PAIR": "0"}),
+    ("dsv3", {"MOE_KSPLIT": "1"}),
+    ("mixtral_w8", {"MOE_KSPLIT": "0", "MOE_PAIR": "0"}),
     ("mixtral_w8", {"MOE_SLOT_KB": "2"}),
     ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
