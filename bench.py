@@ -275,7 +275,8 @@ def run_ours(args):
                 "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = (f"grouped_gemm_wna16_kernel<{shape.wdtype}>" if shape.wdtype in ("int4", "int8")
-                      else f"grouped_gemm_kernel<{shape.wdtype}>") + " (gate_up + SwiGLU)" + \
+                      else f"grouped_gemm_{'pair_' if plan.pair_up else ''}kernel<{shape.wdtype}>") + \
+        (" (clusters of 2 CTAs)" if plan.pair_up else "") + " (gate_up + SwiGLU)" + \
         (" + absmax + e4m3 pass (dynamic scales)" if shape.act_scale == "dynamic" else "")
     roof["kernel_ms"] = k_ms
     roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
@@ -572,7 +573,7 @@ def main():
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling small cases)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", type=int, default=2048)
+    ap.add_argument("--cpu-sample", type=int, default=4096)
     ap.add_argument("--ref-sample", type=int, default=16)
     ap.add_argument("--measure-tensor-peaks", action="store_true",
                     help="print the library's dense bf16 / e4m3 GEMM throughput and exit")

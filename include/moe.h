@@ -276,14 +276,17 @@ const char* moe_status_string(moe_status_t s);
 
 /* Launch plan the library makes for a problem (for tests and benchmarks): per
  * GEMM the token tile limit, split-K factor, operand ring depth, converted
- * weight ring depth (int4 only, else 0) and dynamic shared memory bytes; then
- * the SM count planned for and, for int4, the k-blocks (64 reduction elements
- * each) per converted weight slot in tensor memory (else 0). */
+ * weight ring depth (int4 / int8 only, else 0) and dynamic shared memory
+ * bytes; then the SM count planned for; for int4 / int8 the k-blocks (64
+ * reduction elements each) per converted weight slot in tensor memory (else
+ * 0); and per GEMM whether it runs as clusters of two CTAs sharing M = 256
+ * MMAs (1) or one CTA per 128 weight rows (0). */
 typedef struct {
   int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
   int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
   int32_t num_sms;
   int32_t slot_kb_up, slot_kb_down;
+  int32_t pair_up, pair_down;
 } moe_plan_t;
 
 /* Plan on the current device. */

@@ -767,6 +767,8 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->num_sms = num_sms;
   plan->slot_kb_up = u.slot_kb;
   plan->slot_kb_down = d.slot_kb;
+  plan->pair_up = u.pair;
+  plan->pair_down = d.pair;
   return MOE_OK;
 }
 

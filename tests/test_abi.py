@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
-    assert ctypes.sizeof(binding.Plan) == 52
+    assert ctypes.sizeof(binding.Plan) == 60
 
 
 def test_status_strings(lib):
@@ -148,7 +148,8 @@ def _all_problems():
         for T in (0,) + tuple(T_SWEEP) + (3, 37, 1000, 8192):
             yield s, moe.problem(T, s.H, s.I, s.E, s.top_k, scoring=s.scoring, renormalize=s.renormalize,
                                  n_group=s.n_group, topk_group=s.topk_group,
-                                 routed_scaling_factor=s.routed_scaling_factor, wdtype=s.wdtype)
+                                 routed_scaling_factor=s.routed_scaling_factor, wdtype=s.wdtype,
+                                 act_scale=s.act_scale)
 
 
 @pytest.mark.parametrize("sms", [148, 152, 160])
@@ -170,9 +171,14 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
                 # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
                 # stage count that is a multiple of g; g = 2 always satisfies both here
                 assert ast >= 4 // sk + 1
-                if sk == 4:  # whole-stage slots reuse the stage ring's barriers; both groups
-                    assert st >= ast  # convert every stage (k-split), any ring depth
+                if sk == 4:
+                    # whole-stage slots reuse the stage ring's barriers; an odd depth only
+                    # with both groups converting every stage (k-split, for a shallow ring)
+                    assert st >= ast and (st % 2 == 0 or st == 3)
                 else:
                     assert st % 2 == 0 or st % 3 == 0
             else:
                 assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0
+            # CTA pairs exactly when the 128-row weight blocks pair up
+            fb = shape.I // 64 if side == "up" else shape.H // 128
+            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 else 0)
