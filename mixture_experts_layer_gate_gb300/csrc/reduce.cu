@@ -13,21 +13,39 @@ namespace moe {
 
 namespace {
 
+constexpr int kReduceMaxK = 32;  // top_k limit of the problem checks
+
+// Loads token t's k (row, weight) pairs into shared memory once, so the row
+// loads of different j depend on no global load and can be in flight together
+// (a small batch is otherwise a chain of k dependent round trips).
+__device__ __forceinline__ void load_slots(const int32_t* __restrict__ inv, const float* __restrict__ w,
+                                           int t, int k, int* s_inv, float* s_w) {
+  if (threadIdx.x < k) {
+    s_inv[threadIdx.x] = inv[static_cast<size_t>(t) * k + threadIdx.x];
+    s_w[threadIdx.x] = w[static_cast<size_t>(t) * k + threadIdx.x];
+  }
+  __syncthreads();
+}
+
 // grid (ceil(H / 2048), T); each thread owns 8 consecutive elements of a row.
 __global__ void __launch_bounds__(256)
     unpermute_reduce_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ inv,
                             const float* __restrict__ w, int H, int k, __nv_bfloat16* out) {
+  __shared__ int s_inv[kReduceMaxK];
+  __shared__ float s_w[kReduceMaxK];
   const int t = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_trigger();
+  load_slots(inv, w, t, k, s_inv, s_w);
   if (c * 8 >= H) return;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 4
   for (int j = 0; j < k; ++j) {
-    const int r = inv[static_cast<size_t>(t) * k + j];
-    const float wj = w[static_cast<size_t>(t) * k + j];
+    const int r = s_inv[j];
+    const float wj = s_w[j];
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(r) * H) + c);
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -53,17 +71,21 @@ __global__ void __launch_bounds__(256)
     unpermute_reduce_splitk_kernel(const float* __restrict__ part, int P, int64_t pstride,
                                    const int32_t* __restrict__ inv, const float* __restrict__ w, int H,
                                    int k, __nv_bfloat16* out) {
+  __shared__ int s_inv[kReduceMaxK];
+  __shared__ float s_w[kReduceMaxK];
   const int t = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_trigger();
+  load_slots(inv, w, t, k, s_inv, s_w);
   if (c * 8 >= H) return;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 2
   for (int j = 0; j < k; ++j) {
-    const int r = inv[static_cast<size_t>(t) * k + j];
-    const float wj = w[static_cast<size_t>(t) * k + j];
+    const int r = s_inv[j];
+    const float wj = s_w[j];
     const float* row = part + static_cast<size_t>(r) * H;
     float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
     for (int q = 0; q < P; ++q) {
