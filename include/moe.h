@@ -219,9 +219,11 @@ size_t moe_padded_capacity(const moe_problem_t* p, int32_t block);
 /* Stage 3a: grouped gate_up GEMM with SiLU-and-mul fused into its epilogue.
  * For every expert e and row r in [offsets[e], offsets[e+1]):
  *   h = W13[e] x_perm[r]  (fp32 accumulation; fp8: times a1 * w13_scale[e];
- *                          int4: codes times group scales, rounded to bf16)
+ *                          int4 / int8: weights (code - zero) * scale, each
+ *                          rounded to bf16)
  *   act[r, i] = silu(h[i]) * h[I + i],  silu(z) = z / (1 + exp(-z))
- * act is bf16 [S, I], or for fp8 the e4m3 code of act / a2.
+ * act is bf16 [S, I], or for fp8 the e4m3 code of act / a2 (a2 static, or with
+ * dynamic scales computed here from the bf16 act over all S rows).
  * Uses ws for split-K partial sums when the expert row counts are small.
  * offsets need not come from moe_align_permute: any nondecreasing int32
  * [E + 1] with offsets[0] = 0 and offsets[E] = S works, e.g. rows an

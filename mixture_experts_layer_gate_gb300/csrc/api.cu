@@ -29,8 +29,8 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
 constexpr int kMaxStages = 8;  // bf16 / fp8 operand ring
 constexpr int kMaxStagesInt4 = 8;
-constexpr int kMaxSlotsInt4 = 7;  // int4: converted weight tiles in TMEM
-constexpr int kSuper = kInt4StageKb;  // int4: k-blocks per ring stage
+constexpr int kMaxSlotsInt4 = 7;  // int4 / int8: converted weight tiles in TMEM
+constexpr int kSuper = kInt4StageKb;  // int4 / int8: k-blocks per ring stage
 constexpr int kSmsForSizing = 160;  // upper bound on SMs used when sizing split-K scratch
 constexpr size_t kMaxDynSmem = 232448;
 
