@@ -260,3 +260,17 @@ def test_launch_count_of_forward(dev, name, T):
     expect += 1 + 1                               # down GEMM, reduce (split-K finish folded in)
     expect += 2 if shape.act_scale == "dynamic" else 0  # amax(x), e4m3 pass of act
     assert moe.launch_count() - n0 == expect
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_limits_experts_topk_groups(dev, T):
+    # the largest E, top_k and n_group the library accepts (E = 1024, k = 32, 32 groups)
+    shape = dataclasses.replace(SHAPES["dsv3"], name="limits", H=128, I=128, E=1024, top_k=32,
+                                n_group=32, topk_group=8, wdtype="bf16")
+    gc.full_check(shape, T, dev)
+
+
+def test_limit_token_count(dev):
+    # the largest T (65535): 131070 slots through the multi-CTA counting sort
+    shape = dataclasses.replace(SHAPES["tiny"], name="max_tokens", H=128, I=128)
+    gc.full_check(shape, 65535, dev)
