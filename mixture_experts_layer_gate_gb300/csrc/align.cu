@@ -11,7 +11,8 @@
 //                   CTAs) from the histograms, an exclusive scan for offsets,
 //                   then a rank for each slot that keeps ascending slot order
 //                   inside an expert (warp match + per-warp prefix counts).
-//   gather_rows   : x_perm[r] = x[perm[r] / k] (fp8: e4m3 of x / a1).
+//   gather_rows   : x_perm[inv[t*k + j]] = x[t] for each of token t's k slots
+//                   (fp8: e4m3 of x / a1, quantised once per token).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -20,7 +21,8 @@ namespace moe {
 namespace {
 
 constexpr int kScatterThreads = 512;
-constexpr int kGatherThreads = 128;
+constexpr int kGatherThreads = 256;
+constexpr int kGatherMaxK = 32;  // top_k limit of the problem checks
 constexpr int kScatterWarps = kScatterThreads / 32;
 
 __global__ void __launch_bounds__(512) align_count_kernel(AlignArgs a) {
@@ -157,25 +159,31 @@ __global__ void __launch_bounds__(kScatterThreads) align_scatter_kernel(AlignArg
   }
 }
 
-// One CTA of 128 threads per permuted row; 16-byte vectors along H.  (A warp
-// per row left small batches latency-bound on the per-element divisions.)
+// One CTA per token: its row is read once, quantised once (fp8), and written to
+// the k permuted rows its slots landed on (inv).  A CTA per permuted row read
+// and quantised each token row k times; the divisions of the fp8 path made
+// that instruction-bound.
 template <bool FP8>
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(AlignArgs a) {
-  const int r = blockIdx.x;
+  __shared__ int rows[kGatherMaxK];
+  const int t = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const int t = a.perm[r] / a.k;
+  if (threadIdx.x < a.k) rows[threadIdx.x] = a.inv[static_cast<size_t>(t) * a.k + threadIdx.x];
+  __syncthreads();
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
                                                     static_cast<size_t>(t) * a.H);
   const int nvec = a.H / 8;
   if (!FP8) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.x_perm) +
-                                          static_cast<size_t>(r) * a.H);
-    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) dst[c] = __ldg(src + c);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.x_perm);
+    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) {
+      const uint4 v = __ldg(src + c);
+      for (int j = 0; j < a.k; ++j)
+        reinterpret_cast<uint4*>(dst + static_cast<size_t>(rows[j]) * a.H)[c] = v;
+    }
   } else {
     const float s = a.a1[0];
-    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.x_perm) +
-                                          static_cast<size_t>(r) * a.H);
+    uint8_t* dst = static_cast<uint8_t*>(a.x_perm);
     for (int c = threadIdx.x; c < nvec; c += kGatherThreads) {
       const uint4 v = __ldg(src + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -188,7 +196,9 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(AlignArgs a
                                             __fdiv_rn(bf16_hi(w[2 * h + 1]), s));
         q[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
       }
-      dst[c] = make_uint2(q[0], q[1]);
+      const uint2 qv = make_uint2(q[0], q[1]);
+      for (int j = 0; j < a.k; ++j)
+        reinterpret_cast<uint2*>(dst + static_cast<size_t>(rows[j]) * a.H)[c] = qv;
     }
   }
 }
@@ -245,8 +255,9 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gather(const AlignArgs& a, cudaStream_t s) {
   if (a.S == 0) return cudaSuccess;
-  if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
-  return launch_pdl(gather_rows_kernel<false>, dim3(a.S), dim3(kGatherThreads), 0, s, a);
+  const int T = a.S / a.k;
+  if (a.fp8) return launch_pdl(gather_rows_kernel<true>, dim3(T), dim3(kGatherThreads), 0, s, a);
+  return launch_pdl(gather_rows_kernel<false>, dim3(T), dim3(kGatherThreads), 0, s, a);
 }
 
 cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm, int E, int S,
