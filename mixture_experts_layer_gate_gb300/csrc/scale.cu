@@ -66,6 +66,9 @@ __global__ void __launch_bounds__(kScaleThreads)
   pdl_trigger();
   const float a = __uint_as_float(*reinterpret_cast<volatile uint32_t*>(&d->amax[which]) << 16);
   const float s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
+  // times the reciprocal, as the static requantisation in the GEMM epilogue does
+  // (an IEEE division per element made this pass instruction-bound)
+  const float rs = __fdiv_rn(1.0f, s);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kScaleThreads + threadIdx.x; i < nvec;
        i += static_cast<int64_t>(gridDim.x) * kScaleThreads) {
     const uint4 v = __ldg(x + i);
@@ -73,9 +76,8 @@ __global__ void __launch_bounds__(kScaleThreads)
     uint32_t q[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h]), s), __fdiv_rn(bf16_hi(w[2 * h]), s));
-      const uint16_t hi =
-          f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h + 1]), s), __fdiv_rn(bf16_hi(w[2 * h + 1]), s));
+      const uint16_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * h]) * rs, bf16_hi(w[2 * h]) * rs);
+      const uint16_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * h + 1]) * rs, bf16_hi(w[2 * h + 1]) * rs);
       q[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
     }
     out[i] = make_uint2(q[0], q[1]);
