@@ -130,7 +130,9 @@ struct GemmPlan {
   size_t smem;
 };
 
-// Tuning overrides (benchmarking only): MOE_BN_MAX, MOE_STAGES, MOE_SPLITS.
+// Tuning overrides (benchmarking and tests only; the defaults are the planner's):
+// MOE_BN_MAX, MOE_STAGES, MOE_SPLITS, MOE_PAIR, MOE_CONV_GROUPS, MOE_SLOT_KB,
+// MOE_KSPLIT, MOE_FULL_BOX, MOE_W_STREAM.
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (v == nullptr || *v == 0) return dflt;
@@ -249,11 +251,10 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
   while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E) > kMaxDynSmem)
     --g.stages;
-  // int4 / int8: converter group g takes every conv_groups-th ring stage, so
-  // the ring depth must be a multiple of the group count (parity-wait rule).
   if (converts(wk)) {
-    // Groups alternating stages need a ring depth that is a multiple of the group
-    // count.  k-split (both groups convert every stage, each half its k-blocks)
+    // Converter groups alternating stages need a ring depth that is a multiple of
+    // the group count (parity-wait rule: a stage's previous user was the same
+    // group).  k-split (both groups convert every stage, each half its k-blocks)
     // has no such rule but more bookkeeping per stage (measured slower at equal
     // depth), so it is taken only where rounding down would leave a shallow ring
     // (int8 codes with 128-token tiles: three stages instead of two).
