@@ -81,14 +81,24 @@ def _env_int(name, default):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples every 50 ms; `mark()` brackets the
+    timed region, whose samples the summary keeps (all samples if none fell
+    inside, e.g. a region shorter than the interval, flagged in the summary)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.t0 = self.t1 = None
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
 
     def __enter__(self):
         try:
@@ -96,7 +106,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
             self.proc = None
@@ -114,25 +124,32 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         try:
             for line in open(self.path):
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    sm, smax = float(parts[1]), float(parts[2])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+                try:  # e.g. 2026/12/02 14:09:14.123 (host local time)
+                    ts = time.mktime(time.strptime(parts[9].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[9].split(".")[1]) if "." in parts[9] else 0.0
+                except (ValueError, IndexError):
+                    ts = None
+                rows.append((ts, sm, smax, [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]))
         except OSError:
             pass
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        reasons = sorted({n for r in use for n in r[3]})
+        return {"sm_mhz": statistics.median([r[1] for r in use]) if use else None,
+                "sm_max_mhz": use[-1][2] if use else None, "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
 
 
 # --------------------------------------------------------------- our arm
@@ -224,6 +241,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark(True)
         with torch.cuda.stream(stream):
             for e0, e1 in ev:
                 if flush is not None:
@@ -232,6 +250,7 @@ def run_ours(args):
                 graph.replay()
                 e1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(False)
         time.sleep(0.05)
     if dist is not None:
         dist.barrier()
