@@ -217,6 +217,7 @@ def test_full_size_sampled(dev, name, T):
     ("mixtral", {"MOE_PAIR": "0"}),
     ("qwen2", {"MOE_PAIR": "0"}),
     ("dsv3", {"MOE_PAIR": "0"}),
+    ("dsv3", {"MOE_PAIR": "1"}),
     ("dsv3", {"MOE_SLOT_KB": "2"}),
     ("dsv3", {"MOE_CONV_GROUPS": "3"}),
     ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
