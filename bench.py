@@ -313,7 +313,8 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = (f"grouped_gemm_wna16_kernel<{shape.wdtype}>" if shape.wdtype in ("int4", "int8")
                       else f"grouped_gemm_{'pair_' if plan.pair_up else ''}kernel<{shape.wdtype}>") + \
-        (" (clusters of 2 CTAs)" if plan.pair_up else "") + " (gate_up + SwiGLU)" + \
+        (" (clusters of 2 CTAs)" if plan.pair_up else "") + \
+        (" (2 MMA-issuing threads)" if plan.issuers_up == 2 else "") + " (gate_up + SwiGLU)" + \
         (" + absmax + e4m3 pass (dynamic scales)" if shape.act_scale == "dynamic" else "")
     roof["kernel_ms"] = k_ms
     roof["l2_flushed"] = kflush is not None

@@ -281,14 +281,17 @@ const char* moe_status_string(moe_status_t s);
  * weight ring depth (int4 / int8 only, else 0) and dynamic shared memory
  * bytes; then the SM count planned for; for int4 / int8 the k-blocks (64
  * reduction elements each) per converted weight slot in tensor memory (else
- * 0); and per GEMM whether it runs as clusters of two CTAs sharing M = 256
- * MMAs (1) or one CTA per 128 weight rows (0). */
+ * 0); per GEMM whether it runs as clusters of two CTAs sharing M = 256
+ * MMAs (1) or one CTA per 128 weight rows (0); and per GEMM the threads that
+ * issue its MMAs in a CTA (1, or for int4 / int8 tiles of at most 64 tokens
+ * on one CTA 2, each its half of the reduction into its own accumulator). */
 typedef struct {
   int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
   int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
   int32_t num_sms;
   int32_t slot_kb_up, slot_kb_down;
   int32_t pair_up, pair_down;
+  int32_t issuers_up, issuers_down;
 } moe_plan_t;
 
 /* Plan on the current device. */

@@ -58,7 +58,8 @@ class Plan(ctypes.Structure):
                 ("stages_down", ctypes.c_int32), ("astages_down", ctypes.c_int32),
                 ("smem_down", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("slot_kb_up", ctypes.c_int32), ("slot_kb_down", ctypes.c_int32),
-                ("pair_up", ctypes.c_int32), ("pair_down", ctypes.c_int32)]
+                ("pair_up", ctypes.c_int32), ("pair_down", ctypes.c_int32),
+                ("issuers_up", ctypes.c_int32), ("issuers_down", ctypes.c_int32)]
 
 
 _lib = None

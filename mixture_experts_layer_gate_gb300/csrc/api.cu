@@ -126,13 +126,13 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, pair, FB, KB;
+  int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, pair, dual, full_box, FB, KB;
   size_t smem;
 };
 
 // Tuning overrides (benchmarking and tests only; the defaults are the planner's):
 // MOE_BN_MAX, MOE_STAGES, MOE_SPLITS, MOE_PAIR, MOE_CONV_GROUPS, MOE_SLOT_KB,
-// MOE_KSPLIT, MOE_FULL_BOX, MOE_W_STREAM.
+// MOE_KSPLIT, MOE_DUAL, MOE_FULL_BOX, MOE_W_STREAM.
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (v == nullptr || *v == 0) return dflt;
@@ -206,16 +206,24 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   int cap;
   g.conv_groups = 0;
   g.ksplit = 0;
-  // CTA pairs (M = 256 per MMA) whenever the weight blocks pair up, except int4
-  // decode tiles (<= 32 tokens): there one CTA per 128 weight rows measured 1-3%
-  // faster (DeepSeek-V3 T = 1 and 32; pairs win from T = 512 and for int8).
+  g.dual = 0;
+  // int4 / int8: one CTA per 128 weight rows with two MMA-issuing threads for
+  // small token tiles (<= 32 tokens; int4 <= 64), CTA pairs (M = 256 per MMA)
+  // above that, as for bf16 / fp8 whenever the weight blocks pair up.  Measured
+  // on DeepSeek-V3 int4 (T = 1 to 512) and Mixtral int8 (T = 1, 32; pairs win
+  // at 64 tokens, where int8's larger stages leave one CTA a shallow ring).
+  // Converting kernels always load whole token tiles: one TMA per stage keeps
+  // the producer thread, which shares its SM sub-partition with integer-bound
+  // converter warps, short of instructions (ragged tiles otherwise take one box
+  // per 64 / 16 rows and k-block).
+  const bool dual_fit = converts(wk) && (g.bn_max <= 32 || (wk == kW_INT4 && g.bn_max <= 64));
   g.pair = 0;
   const int pair_env = env_int("MOE_PAIR", -1);
-  const bool pair_default = !(wk == kW_INT4 && g.bn_max <= 32);
-  if (g.FB % 2 == 0 && (pair_env == 1 || (pair_env != 0 && pair_default))) {
+  if (g.FB % 2 == 0 && (pair_env == 1 || (pair_env != 0 && !dual_fit))) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
+  g.full_box = env_int("MOE_FULL_BOX", converts(wk) ? 1 : 0) != 0 ? 1 : 0;
   if (converts(wk)) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of
     // slot_kb k-blocks (32 columns each).  A converter group that fills the
@@ -224,7 +232,12 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // Whole-stage slots (one wait and one commit per 16 MMAs) when TMEM holds
     // one per group; else two-k-block slots.
     g.acc_cols = (g.bn_max + 31) / 32 * 32;
-    const int free_cols = 512 - 2 * g.acc_cols;
+    // Two MMA-issuing threads (one CTA, whole-stage slots, tiles of <= 64
+    // tokens): each keeps its own pair of partial accumulators, so four
+    // accumulators and at least two whole-stage slots must fit.
+    const int dual_env = env_int("MOE_DUAL", -1);
+    if (!g.pair && g.acc_cols <= 64 && (dual_env == 1 || (dual_env != 0 && dual_fit))) g.dual = 1;
+    const int free_cols = 512 - (g.dual ? 4 : 2) * g.acc_cols;
     const int cg_env = env_int("MOE_CONV_GROUPS", 0);
     const int sk_env = env_int("MOE_SLOT_KB", 0);
     // Two converter groups: the single MMA-issuing thread, not conversion, sets
@@ -235,7 +248,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
     auto slots_fit = [&](int sk) { return std::min(kMaxSlotsInt4, free_cols / (32 * sk)); };
     g.slot_kb = (slots_fit(4) >= slots_needed(4)) ? 4 : 2;
-    if ((sk_env == 2 || sk_env == 4) && slots_fit(sk_env) >= slots_needed(sk_env)) g.slot_kb = sk_env;
+    if ((sk_env == 2 || sk_env == 4) && !g.dual && slots_fit(sk_env) >= slots_needed(sk_env)) g.slot_kb = sk_env;
     if (slots_fit(g.slot_kb) < slots_needed(g.slot_kb)) g.conv_groups = 2;  // 3 groups do not fit
     g.astages = slots_fit(g.slot_kb);
     per_stage = static_cast<size_t>(raw_stage_bytes(wk)) + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
@@ -498,9 +511,10 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.astages = g.astages;
   gp.slot_kb = g.slot_kb;
   gp.conv_groups = g.conv_groups;
+  gp.dual = g.dual;
   gp.ksplit = g.ksplit;
   gp.acc_cols = g.acc_cols;
-  gp.full_box = env_int("MOE_FULL_BOX", 0) != 0 ? 1 : 0;
+  gp.full_box = g.full_box;
   gp.is_up = up ? 1 : 0;
   gp.R = up ? 2 * p.I : p.H;
   gp.G = up ? p.H / 128 : p.I / 128;
@@ -774,6 +788,8 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->slot_kb_down = d.slot_kb;
   plan->pair_up = u.pair;
   plan->pair_down = d.pair;
+  plan->issuers_up = u.dual ? 2 : 1;
+  plan->issuers_down = d.dual ? 2 : 1;
   return MOE_OK;
 }
 

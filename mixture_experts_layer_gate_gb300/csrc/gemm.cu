@@ -72,7 +72,7 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
   L.stg = o;
   o += kStgBytes;
   L.bars = o;
-  o += (2 * stages + 2 * astages + 5) * 8;
+  o += (2 * stages + 2 * astages + 6) * 8;
   o = (o + 15u) & ~15u;
   L.misc = o;
   o += 16;
@@ -238,8 +238,10 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
 // Units are taken from `first` in steps of `stride`; `pair_rank` >= 0 marks a
 // CTA-pair kernel (this CTA's rows are weight block 2*fb + rank); the arrival
 // that frees an accumulator goes, one per warp, to the shared::cluster address
-// `tempty_cl0` (+8 for buffer 1).
-template <int WK>
+// `tempty_cl0` (+8 for buffer 1).  DUAL: buffer b is two partial accumulators
+// (columns 2b and 2b + 1 times acc_cols) from two MMA-issuing threads, the
+// second written only for units of more than two k-blocks; the epilogue adds them.
+template <int WK, bool DUAL = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
                                              int units, int first, int stride, int pair_rank,
                                              uint32_t tmem_base, uint32_t tfull0, uint32_t tempty_cl0,
@@ -259,8 +261,9 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       sc = p.a_scale[0] * p.w_scale[t.e];
       if (q8) inv_q = 1.0f / p.q_scale[0];
     }
-    const uint32_t tbase =
-        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.acc_cols);
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           (DUAL ? 2u * acc : acc) * static_cast<uint32_t>(p.acc_cols);
+    const bool part1 = DUAL && t.kb1 - t.kb0 > 2;  // warp-uniform
     uint32_t mx = 0;  // dynamic scales: largest stored |act| (bf16 magnitude bits), valid tokens only
     for (int cb = 0; cb < t.nvalid; cb += 32) {
       // two 16-column loads in flight, one wait
@@ -268,7 +271,23 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
       const bool two = cb + 16 < t.nvalid;  // warp-uniform
       tmem_ld16(tbase + static_cast<uint32_t>(cb), vv[0]);
       if (two) tmem_ld16(tbase + static_cast<uint32_t>(cb + 16), vv[1]);
-      tmem_ld_wait();
+      if (DUAL && part1) {
+        uint32_t ww[2][16];
+        const uint32_t t1 = tbase + static_cast<uint32_t>(p.acc_cols);
+        tmem_ld16(t1 + static_cast<uint32_t>(cb), ww[0]);
+        if (two) tmem_ld16(t1 + static_cast<uint32_t>(cb + 16), ww[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          vv[0][c] = __float_as_uint(__uint_as_float(vv[0][c]) + __uint_as_float(ww[0][c]));
+        if (two) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            vv[1][c] = __float_as_uint(__uint_as_float(vv[1][c]) + __uint_as_float(ww[1][c]));
+        }
+      } else {
+        tmem_ld_wait();
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
       if (h == 1 && !two) break;
@@ -725,9 +744,17 @@ __global__ void __launch_bounds__(192, 1)
 // converting its own 128 weight rows into its own TMEM and staging half of the
 // token rows; converter groups of both CTAs report to the leader's AFULL, the
 // leader's commits are multicast to both CTAs.
-template <int BITS, int CG, bool PAIR, int SK>
-__global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
+// DUAL (one CTA, whole-stage slots): one thread issues MMAs at a fixed rate
+// however idle the tensor pipe is, and the converters' integer work slows it
+// further, so a second issuing thread (an extra warp) takes k-blocks 2 and 3
+// of every stage into its own partial accumulator while warp 1 takes k-blocks
+// 0 and 1.  Both wait for every stage and both report on its REMPTY (count 2)
+// and on the accumulator's TFULL (count 2); a thread with no k-block in a stage
+// or unit (a short end of a K range) arrives without a commit.
+template <int BITS, int CG, bool PAIR, int SK, bool DUAL>
+__global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     grouped_gemm_wna16_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  static_assert(!DUAL || (!PAIR && SK == kSuper), "two issuers: one CTA, whole-stage slots");
   constexpr int WKQ = BITS == 8 ? kW_INT8 : kW_INT4;
   constexpr uint32_t kRaw = static_cast<uint32_t>(raw_stage_bytes(WKQ));  // codes per ring stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -747,7 +774,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
 #define AEMPTY(s) (bars + 8u * static_cast<uint32_t>(2 * ns + na + (s)))
   const uint32_t tfull0 = bars + 8u * static_cast<uint32_t>(2 * ns + 2 * na);
   const uint32_t tempty0 = tfull0 + 16u;
-  const uint32_t drain_bar = tfull0 + 32u;
+  const uint32_t drain_bar = tfull0 + 32u;  // (+8: the second issuer's)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.misc + 4);
   int* tile_base = reinterpret_cast<int*>(base + L.tiles);
@@ -755,14 +782,15 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t acc_cols = static_cast<uint32_t>(p.acc_cols);
-  const uint32_t a_col0 = 2u * acc_cols;  // TMEM column of converted slot 0
+  const uint32_t a_col0 = (DUAL ? 4u : 2u) * acc_cols;  // TMEM column of converted slot 0
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
   // k-split: both groups convert every stage (group g its k-blocks 2g, 2g + 1)
   const bool ks = p.ksplit != 0;
-  if (p.slot_kb != SK || (SK == kSuper && ns < na) || (ks && (SK != kSuper || CG != 2)) ||
+  if (p.slot_kb != SK || p.dual != (DUAL ? 1 : 0) || (SK == kSuper && ns < na) ||
+      (ks && (SK != kSuper || CG != 2)) ||
       (!ks && (na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0)) ||
       a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
     if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x500u);  // host plans never do this
@@ -772,18 +800,19 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(RFULL(s), 1u);
-      mbar_init(REMPTY(s), 1u);
+      mbar_init(REMPTY(s), DUAL ? 2u : 1u);
     }
     for (int s = 0; s < na; ++s) {
       // the 4 warps of the stage's converter group, or of both groups with k-split (in each CTA)
       mbar_init(AFULL(s), (ks ? 4u * CG : 4u) * kCtas);
       mbar_init(AEMPTY(s), 1u);
     }
-    mbar_init(tfull0, 1u);
-    mbar_init(tfull0 + 8u, 1u);
+    mbar_init(tfull0, DUAL ? 2u : 1u);
+    mbar_init(tfull0 + 8u, DUAL ? 2u : 1u);
     mbar_init(tempty0, 4u * kCtas);  // one arrival per epilogue warp (of each CTA)
     mbar_init(tempty0 + 8u, 4u * kCtas);
     mbar_init(drain_bar, 1u);
+    if (DUAL) mbar_init(drain_bar + 8u, 1u);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
@@ -836,7 +865,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             break;
           }
           const uint32_t stage = sR + st * L.r_stride;
-          const bool full = (t.n == brows);
+          const bool full = (t.n == brows) || p.full_box;
           const uint32_t bbytes = full ? kSuper * btile : static_cast<uint32_t>(nk * t.n) * 128u;
           // int8: the stage's codes are two boxes of two k-blocks; a stage of at
           // most two k-blocks (the end of a K range) needs only the first
@@ -872,9 +901,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           if ((issued >> s) & 1u) mbar_wait(RFULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (DUAL && warp == 6 + 4 * CG)) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
+      // issuer j (DUAL): k-blocks [2j, 2j + 2) of every stage, partial accumulator j
+      const int j = warp == 1 ? 0 : 1;
+      const int jb0 = DUAL ? 2 * j : 0;
       int st = 0, as = 0;
       uint32_t ph = 0, aph = 0, acc = 0, accph = 0;
       bool ok = true, any = false;
@@ -890,7 +922,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * acc_cols;
+        const uint32_t d = tmem_base + (DUAL ? 2u * acc + static_cast<uint32_t>(j) : acc) * acc_cols;
+        bool unit_any = !DUAL;  // DUAL: whether this thread issued any MMA of the unit
         const uint32_t n_mma = PAIR ? static_cast<uint32_t>((t.nvalid + 31) & ~31) : static_cast<uint32_t>(t.n);
         const uint32_t idesc = make_idesc(PAIR ? 256u : 128u, n_mma, 1u);
         if (SK == kSuper) {
@@ -904,12 +937,16 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           uint32_t a_tm = a_tmem0 + slot_cols * static_cast<uint32_t>(as);
           for (int kbs = t.kb0; kbs < t.kb1; kbs += kSuper) {
             const int nk = min(kSuper, t.kb1 - kbs);
+            const int jend = DUAL ? min(nk, jb0 + 2) : nk;
+            const bool mine = !DUAL || jb0 < jend;
             if (!mbar_wait(afull, aph, abort_flag, p.err, 0x210u)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_kblock_tmem_a<PAIR>(d, a_tm, b_lo, bd_hi, idesc, kbs > t.kb0 ? 1u : 0u);
+            if (mine)
+              mma_kblock_tmem_a<PAIR>(d, a_tm + 32u * jb0, b_lo + btile16 * jb0, bd_hi, idesc,
+                                      kbs > t.kb0 ? 1u : 0u);
             const int st_n = (st + 1 == ns) ? 0 : st + 1;
             const uint32_t ph_n = (st + 1 == ns) ? (ph ^ 1u) : ph;
             const int as_n = (as + 1 == na) ? 0 : as + 1;
@@ -917,10 +954,16 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
             const uint32_t afull_n = AFULL(as_n), rempty_n = REMPTY(st_n);
             const uint32_t b_lo_n = bd_lo0 + ((sR + st_n * L.r_stride + kRaw) >> 4);
             const uint32_t a_tm_n = a_tmem0 + slot_cols * static_cast<uint32_t>(as_n);
-            for (int jj = 1; jj < nk; ++jj)
+            for (int jj = jb0 + 1; jj < jend; ++jj)
               mma_kblock_tmem_a<PAIR>(d, a_tm + 32u * jj, b_lo + btile16 * jj, bd_hi, idesc, 1u);
-            if (PAIR) mma_commit_pair(rempty, 0x3); else mma_commit(rempty);
-            any = true;
+            if (PAIR)
+              mma_commit_pair(rempty, 0x3);
+            else if (mine)
+              mma_commit(rempty);
+            else
+              mbar_arrive_cluster(map_to_rank(rempty, 0));  // read nothing of this stage
+            any = any || mine;
+            unit_any = unit_any || mine;
             st = st_n;
             ph = ph_n;
             as = as_n;
@@ -967,17 +1010,23 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG, 1)
           }
         }
         if (!ok) break;
-        if (PAIR) mma_commit_pair(tfull0 + 8u * acc, 0x3); else mma_commit(tfull0 + 8u * acc);
+        if (PAIR)
+          mma_commit_pair(tfull0 + 8u * acc, 0x3);
+        else if (unit_any)
+          mma_commit(tfull0 + 8u * acc);
+        else
+          mbar_arrive_cluster(map_to_rank(tfull0 + 8u * acc, 0));
         acc ^= 1u;
         if (acc == 0u) accph ^= 1u;
       }
       if (!ok && any) {
-        if (PAIR) mma_commit_pair(drain_bar, 0x1); else mma_commit(drain_bar);
-        mbar_wait(drain_bar, 0u, nullptr, p.err, 0x280u);
+        const uint32_t db = drain_bar + 8u * static_cast<uint32_t>(j);
+        if (PAIR) mma_commit_pair(db, 0x1); else mma_commit(db);
+        mbar_wait(db, 0u, nullptr, p.err, 0x280u);
       }
     }
   } else if (warp < 6) {
-    run_epilogue<WKQ>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
+    run_epilogue<WKQ, DUAL>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
                           tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
   } else {
     // ---------------------------------------- int4 / int8 -> bf16 converters
@@ -1169,14 +1218,15 @@ cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, siz
   return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
 }
 
-template <int BITS, int CG, bool PAIR, int SK>
+template <int BITS, int CG, bool PAIR, int SK, bool DUAL = false>
 cudaError_t launch_wna16(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
                          cudaStream_t s) {
   static int configured = -1;
-  cudaError_t err = set_smem_attr(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK>, &configured);
+  cudaError_t err = set_smem_attr(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl_cluster(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK>, dim3(PAIR ? (grid & ~1) : grid),
-                            dim3(gemm_threads(kW_INT4, CG)), smem, s, PAIR ? 2u : 1u, maps, p);
+  return launch_pdl_cluster(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL>,
+                            dim3(PAIR ? (grid & ~1) : grid), dim3(gemm_threads(kW_INT4, CG, DUAL ? 1 : 0)),
+                            smem, s, PAIR ? 2u : 1u, maps, p);
 }
 
 }  // namespace
@@ -1185,8 +1235,8 @@ size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E) {
   return smem_layout(wkind, bn_max, stages, astages, E).total;
 }
 
-int gemm_threads(int wkind, int conv_groups) {
-  return converts(wkind) ? 64 + 128 + 128 * conv_groups : 192;
+int gemm_threads(int wkind, int conv_groups, int dual) {
+  return converts(wkind) ? 64 + 128 + 128 * conv_groups + (dual ? 32 : 0) : 192;
 }
 
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
@@ -1200,7 +1250,10 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
       if (p.slot_kb == 4) {
         if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 4>(maps, p, grid, smem, s);
         if (p.pair && p.conv_groups == 2) return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
-        if (!p.pair && p.conv_groups == 2) return launch_wna16<4, 2, false, 4>(maps, p, grid, smem, s);
+        if (!p.pair && p.conv_groups == 2) {
+          if (p.dual) return launch_wna16<4, 2, false, 4, true>(maps, p, grid, smem, s);
+          return launch_wna16<4, 2, false, 4>(maps, p, grid, smem, s);
+        }
       } else if (p.slot_kb == 2) {
         if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 2>(maps, p, grid, smem, s);
         if (p.pair && p.conv_groups == 2) return launch_wna16<4, 2, true, 2>(maps, p, grid, smem, s);
@@ -1211,6 +1264,7 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
       if (p.conv_groups != 2) return cudaErrorInvalidValue;
       if (p.slot_kb == 4) {
         if (p.pair) return launch_wna16<8, 2, true, 4>(maps, p, grid, smem, s);
+        if (p.dual) return launch_wna16<8, 2, false, 4, true>(maps, p, grid, smem, s);
         return launch_wna16<8, 2, false, 4>(maps, p, grid, smem, s);
       } else if (p.slot_kb == 2) {
         if (p.pair) return launch_wna16<8, 2, true, 2>(maps, p, grid, smem, s);

@@ -121,12 +121,14 @@ struct GemmParams {
   int stages;              // operand ring depth (int4 / int8: ring of packed A + token tiles)
   int astages;             // int4 / int8 only: ring of converted bf16 A tiles
   int slot_kb;             // int4 / int8 only: k-blocks per converted tile (2 or 4)
-  int full_box;            // 1: always load bn_max token rows (tuning)
+  int full_box;            // 1: always load bn_max token rows, one box per stage (int4 / int8 default)
   int conv_groups;         // int4 / int8 only: converter warp groups (2, or 3 with CTA pairs)
   int ksplit;              // int4 / int8, 2 groups, whole-stage slots: both groups convert every
                            // stage, group g its k-blocks 2g and 2g + 1 (else groups alternate stages)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
+  int dual;                // int4 / int8, one CTA, whole-stage slots: two MMA-issuing threads, each
+                           // its half of every stage's k-blocks into its own partial accumulator
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
   int epi;                 // EpiKind
   int is_up;
@@ -145,7 +147,7 @@ struct GemmMaps {
 };
 
 size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E);
-int gemm_threads(int wkind, int conv_groups);
+int gemm_threads(int wkind, int conv_groups, int dual);
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s);
 

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
-    assert ctypes.sizeof(binding.Plan) == 60
+    assert ctypes.sizeof(binding.Plan) == 68
 
 
 def test_status_strings(lib):
@@ -152,35 +152,62 @@ def _all_problems():
                                  act_scale=s.act_scale)
 
 
+def _check_plan(shape, pl):
+    for side in ("up", "down"):
+        bn = getattr(pl, f"bn_max_{side}")
+        assert 16 <= bn <= 256 and bn % 16 == 0
+        assert 1 <= getattr(pl, f"splits_{side}") <= 16
+        st, ast = getattr(pl, f"stages_{side}"), getattr(pl, f"astages_{side}")
+        assert st >= 2
+        assert getattr(pl, f"smem_{side}") <= 232448
+        issuers = getattr(pl, f"issuers_{side}")
+        assert issuers in (1, 2)
+        if shape.wdtype in ("int4", "int8"):
+            # TMEM holds two accumulators per issuing thread and the converted-weight slot ring
+            sk = getattr(pl, f"slot_kb_{side}")
+            assert bn <= 128 and sk in (2, 4)
+            assert 2 <= ast <= 7 and issuers * 2 * ((bn + 31) // 32 * 32) + 32 * sk * ast <= 512
+            # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
+            # stage count that is a multiple of g; g = 2 always satisfies both here
+            assert ast >= 4 // sk + 1
+            if sk == 4:
+                # whole-stage slots reuse the stage ring's barriers; an odd depth only
+                # with both groups converting every stage (k-split, for a shallow ring)
+                assert st >= ast and (st % 2 == 0 or st == 3)
+            else:
+                assert st % 2 == 0 or st % 3 == 0
+            if issuers == 2:  # one CTA, whole-stage slots, tiles of <= 64 tokens
+                assert sk == 4 and bn <= 64 and getattr(pl, f"pair_{side}") == 0
+        else:
+            assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0 and issuers == 1
+    return pl
+
+
 @pytest.mark.parametrize("sms", [148, 152, 160])
 def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
     for shape, p in _all_problems():
-        pl = moe.get_plan(p, num_sms=sms)
+        pl = _check_plan(shape, moe.get_plan(p, num_sms=sms))
         for side in ("up", "down"):
+            # int4 / int8 tiles of <= 32 tokens (int4: <= 64) run one CTA per 128
+            # weight rows with two MMA-issuing threads; otherwise CTA pairs exactly
+            # when the weight blocks pair up
             bn = getattr(pl, f"bn_max_{side}")
-            assert 16 <= bn <= 256 and bn % 16 == 0
-            assert 1 <= getattr(pl, f"splits_{side}") <= 16
-            st, ast = getattr(pl, f"stages_{side}"), getattr(pl, f"astages_{side}")
-            assert st >= 2
-            assert getattr(pl, f"smem_{side}") <= 232448
-            if shape.wdtype in ("int4", "int8"):
-                # TMEM holds two accumulators and the converted-weight slot ring
-                sk = getattr(pl, f"slot_kb_{side}")
-                assert bn <= 128 and sk in (2, 4)
-                assert 2 <= ast <= 7 and 2 * ((bn + 31) // 32 * 32) + 32 * sk * ast <= 512
-                # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
-                # stage count that is a multiple of g; g = 2 always satisfies both here
-                assert ast >= 4 // sk + 1
-                if sk == 4:
-                    # whole-stage slots reuse the stage ring's barriers; an odd depth only
-                    # with both groups converting every stage (k-split, for a shallow ring)
-                    assert st >= ast and (st % 2 == 0 or st == 3)
-                else:
-                    assert st % 2 == 0 or st % 3 == 0
-            else:
-                assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0
-            # CTA pairs exactly when the 128-row weight blocks pair up (int4 decode
-            # tiles of <= 32 tokens run one CTA per weight block)
             fb = shape.I // 64 if side == "up" else shape.H // 128
-            int4_decode = shape.wdtype == "int4" and bn <= 32
-            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not int4_decode else 0)
+            two = shape.wdtype in ("int4", "int8") and (bn <= 32 or (shape.wdtype == "int4" and bn <= 64))
+            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not two else 0)
+            assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
+
+
+def test_plans_with_two_mma_issuers(lib, monkeypatch):
+    # forced on one CTA: every int4 / int8 GEMM with tiles of <= 64 tokens takes
+    # two issuing threads, the rest keep one; the invariants above still hold
+    monkeypatch.setenv("MOE_DUAL", "1")
+    monkeypatch.setenv("MOE_PAIR", "0")
+    seen = 0
+    for shape, p in _all_problems():
+        pl = _check_plan(shape, moe.get_plan(p, num_sms=152))
+        for side in ("up", "down"):
+            two = shape.wdtype in ("int4", "int8") and getattr(pl, f"bn_max_{side}") <= 64
+            assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
+            seen += two
+    assert seen > 0

@@ -211,8 +211,9 @@ def test_full_size_sampled(dev, name, T):
 
 # Kernel variants the planner does not pick for these shapes, forced through the
 # library's tuning knobs (read from the environment at every plan): the single-CTA
-# bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's non-pair,
-# two-k-block-slot, three-converter-group and alternating-stage (no k-split) modes.
+# bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's pair / non-pair,
+# one / two MMA-issuer, two-k-block-slot, three-converter-group, k-split /
+# alternating-stage and per-64/16-row token box (no full box) modes.
 @pytest.mark.parametrize("name,knobs", [
     ("mixtral", {"MOE_PAIR": "0"}),
     ("qwen2", {"MOE_PAIR": "0"}),
@@ -230,6 +231,16 @@ def test_full_size_sampled(dev, name, T):
     ("mixtral_w8", {"MOE_SLOT_KB": "2"}),
     ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
     ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "64"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "32", "MOE_KSPLIT": "1"}),
+    ("dsv3_awq", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "48"}),
+    ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "64"}),
+    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "32"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "0"}),
+    ("dsv3", {"MOE_FULL_BOX": "0", "MOE_DUAL": "0"}),
+    ("dsv3_awq", {"MOE_FULL_BOX": "0"}),
+    ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "0", "MOE_FULL_BOX": "0"}),
 ])
 def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
     for k, v in knobs.items():
@@ -238,7 +249,28 @@ def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
     plan = moe.get_plan(gc.lib_problem(shape, 300))
     if "MOE_SLOT_KB" in knobs:
         assert plan.slot_kb_up == int(knobs["MOE_SLOT_KB"])
+    if "MOE_DUAL" in knobs:  # tiles of <= 64 tokens
+        plan = moe.get_plan(gc.lib_problem(shape, 37))
+        assert plan.issuers_up == 2 and plan.issuers_down == 2
     for T in (37, 300):
+        gc.full_check(shape, T, dev)
+
+
+@pytest.mark.parametrize("splits", [None, "3"])
+def test_two_issuers_short_k_ranges(dev, monkeypatch, splits):
+    # k ranges that leave the second MMA-issuing thread (k-blocks 2 and 3 of a
+    # stage) without work in a stage (split-K tails of one or two k-blocks) or in
+    # a whole unit (the down GEMM's K = 128 is two k-blocks)
+    monkeypatch.setenv("MOE_PAIR", "0")
+    monkeypatch.setenv("MOE_DUAL", "1")
+    if splits:
+        monkeypatch.setenv("MOE_SPLITS", splits)
+    shape = dataclasses.replace(small("dsv3"), name="dsv3_short_k", I=128)
+    for T in (1, 37):
+        plan = moe.get_plan(gc.lib_problem(shape, T))
+        assert plan.issuers_up == 2 and plan.issuers_down == 2
+        if splits:
+            assert plan.splits_up == 3
         gc.full_check(shape, T, dev)
 
 
