@@ -126,7 +126,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 // ---------------------------------------------------------------- planning
 
 struct GemmPlan {
-  int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, pair, dual, full_box, FB, KB;
+  int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, acc_bufs, pair, dual, full_box, FB, KB;
   size_t smem;
 };
 
@@ -207,6 +207,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   g.conv_groups = 0;
   g.ksplit = 0;
   g.dual = 0;
+  g.acc_bufs = 2;
   // int4 / int8: one CTA per 128 weight rows with two MMA-issuing threads for
   // small token tiles (<= 32 tokens; int4 <= 64), CTA pairs (M = 256 per MMA)
   // above that, as for bf16 / fp8 whenever the weight blocks pair up.  Measured
@@ -232,19 +233,23 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // Whole-stage slots (one wait and one commit per 16 MMAs) when TMEM holds
     // one per group; else two-k-block slots.
     g.acc_cols = (g.bn_max + 31) / 32 * 32;
-    // Two MMA-issuing threads (one CTA, whole-stage slots, tiles of <= 64
-    // tokens): each keeps its own pair of partial accumulators, so four
-    // accumulators and at least two whole-stage slots must fit.
+    // Two MMA-issuing threads (whole-stage slots): each keeps its own partial
+    // accumulators, two buffers of them where that leaves room for two
+    // whole-stage slots (<= 64 columns), else one buffer (<= 128 columns; the
+    // epilogue of a unit then no longer overlaps the next unit's MMAs).
     const int dual_env = env_int("MOE_DUAL", -1);
-    if (!g.pair && g.acc_cols <= 64 && (dual_env == 1 || (dual_env != 0 && dual_fit))) g.dual = 1;
-    const int free_cols = 512 - (g.dual ? 4 : 2) * g.acc_cols;
+    if (g.acc_cols <= 128 && (dual_env == 1 || (dual_env != 0 && dual_fit))) {
+      g.dual = 1;
+      g.acc_bufs = g.acc_cols <= 64 ? 2 : 1;
+    }
+    const int free_cols = 512 - (g.dual ? 2 : 1) * g.acc_bufs * g.acc_cols;
     const int cg_env = env_int("MOE_CONV_GROUPS", 0);
     const int sk_env = env_int("MOE_SLOT_KB", 0);
     // Two converter groups: the single MMA-issuing thread, not conversion, sets
     // the pace once slots hold whole stages (three groups measured no faster);
     // three are available with CTA pairs for tuning.
     g.conv_groups = 2;
-    if (cg_env == 3 && g.pair && wk == kW_INT4) g.conv_groups = 3;
+    if (cg_env == 3 && g.pair && wk == kW_INT4 && !g.dual) g.conv_groups = 3;
     auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
     auto slots_fit = [&](int sk) { return std::min(kMaxSlotsInt4, free_cols / (32 * sk)); };
     g.slot_kb = (slots_fit(4) >= slots_needed(4)) ? 4 : 2;
@@ -512,6 +517,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.slot_kb = g.slot_kb;
   gp.conv_groups = g.conv_groups;
   gp.dual = g.dual;
+  gp.acc_bufs = g.acc_bufs;
   gp.ksplit = g.ksplit;
   gp.acc_cols = g.acc_cols;
   gp.full_box = g.full_box;

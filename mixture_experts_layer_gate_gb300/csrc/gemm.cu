@@ -240,7 +240,8 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
 // that frees an accumulator goes, one per warp, to the shared::cluster address
 // `tempty_cl0` (+8 for buffer 1).  DUAL: buffer b is two partial accumulators
 // (columns 2b and 2b + 1 times acc_cols) from two MMA-issuing threads, the
-// second written only for units of more than two k-blocks; the epilogue adds them.
+// second written only for units of more than two k-blocks; the epilogue adds them;
+// the ring then has p.acc_bufs (1 or 2) buffers, else always 2.
 template <int WK, bool DUAL = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
                                              int units, int first, int stride, int pair_rank,
@@ -248,6 +249,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
                                              volatile int* abort_flag, uint8_t* stg_all, int warp, int lane) {
   const int q = warp & 3;  // TMEM lane quarter this warp may read
   uint8_t* stg = stg_all + q * kStgBytesPerWarp;
+  const uint32_t nbuf = DUAL ? static_cast<uint32_t>(p.acc_bufs) : 2u;
   uint32_t acc = 0, accph = 0;
   for (int u = first; u < units; u += stride) {
     Unit t = decode_unit(u, tile_base, off, p);
@@ -380,8 +382,10 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(tempty_cl0 + 8u * acc);
-    acc ^= 1u;
-    if (acc == 0u) accph ^= 1u;
+    if (++acc == nbuf) {
+      acc = 0u;
+      accph ^= 1u;
+    }
   }
 }
 
@@ -744,17 +748,20 @@ __global__ void __launch_bounds__(192, 1)
 // converting its own 128 weight rows into its own TMEM and staging half of the
 // token rows; converter groups of both CTAs report to the leader's AFULL, the
 // leader's commits are multicast to both CTAs.
-// DUAL (one CTA, whole-stage slots): one thread issues MMAs at a fixed rate
-// however idle the tensor pipe is, and the converters' integer work slows it
-// further, so a second issuing thread (an extra warp) takes k-blocks 2 and 3
-// of every stage into its own partial accumulator while warp 1 takes k-blocks
-// 0 and 1.  Both wait for every stage and both report on its REMPTY (count 2)
-// and on the accumulator's TFULL (count 2); a thread with no k-block in a stage
-// or unit (a short end of a K range) arrives without a commit.
+// DUAL (whole-stage slots): one thread issues MMAs at a fixed rate however idle
+// the tensor pipe is, and the converters' integer work slows it further, so a
+// second issuing thread (an extra warp; with PAIR, of the leader CTA) takes
+// k-blocks 2 and 3 of every stage into its own partial accumulator while warp 1
+// takes k-blocks 0 and 1.  Both wait for every stage and both report on its
+// REMPTY (count 2) and on the accumulator's TFULL (count 2), in every CTA of the
+// cluster; a thread with no k-block in a stage or unit (a short end of a K
+// range) arrives without a commit.  Accumulator columns: p.acc_bufs buffers (2,
+// or 1 when two pairs of partials do not fit beside two converted slots) of two
+// partials each.
 template <int BITS, int CG, bool PAIR, int SK, bool DUAL>
 __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     grouped_gemm_wna16_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  static_assert(!DUAL || (!PAIR && SK == kSuper), "two issuers: one CTA, whole-stage slots");
+  static_assert(!DUAL || SK == kSuper, "two issuers: whole-stage slots");
   constexpr int WKQ = BITS == 8 ? kW_INT8 : kW_INT4;
   constexpr uint32_t kRaw = static_cast<uint32_t>(raw_stage_bytes(WKQ));  // codes per ring stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -782,14 +789,15 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t acc_cols = static_cast<uint32_t>(p.acc_cols);
-  const uint32_t a_col0 = (DUAL ? 4u : 2u) * acc_cols;  // TMEM column of converted slot 0
+  const uint32_t nbuf = DUAL ? static_cast<uint32_t>(p.acc_bufs) : 2u;  // accumulator buffers
+  const uint32_t a_col0 = (DUAL ? 2u : 1u) * nbuf * acc_cols;            // TMEM column of converted slot 0
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
   // k-split: both groups convert every stage (group g its k-blocks 2g, 2g + 1)
   const bool ks = p.ksplit != 0;
-  if (p.slot_kb != SK || p.dual != (DUAL ? 1 : 0) || (SK == kSuper && ns < na) ||
+  if (p.slot_kb != SK || p.dual != (DUAL ? 1 : 0) || nbuf < 1u || nbuf > 2u || (SK == kSuper && ns < na) ||
       (ks && (SK != kSuper || CG != 2)) ||
       (!ks && (na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0)) ||
       a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
@@ -956,12 +964,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
             const uint32_t a_tm_n = a_tmem0 + slot_cols * static_cast<uint32_t>(as_n);
             for (int jj = jb0 + 1; jj < jend; ++jj)
               mma_kblock_tmem_a<PAIR>(d, a_tm + 32u * jj, b_lo + btile16 * jj, bd_hi, idesc, 1u);
-            if (PAIR)
-              mma_commit_pair(rempty, 0x3);
-            else if (mine)
-              mma_commit(rempty);
-            else
-              mbar_arrive_cluster(map_to_rank(rempty, 0));  // read nothing of this stage
+            if (mine) {
+              if (PAIR) mma_commit_pair(rempty, 0x3); else mma_commit(rempty);
+            } else {
+              // read nothing of this stage
+              for (uint32_t r = 0; r < kCtas; ++r) mbar_arrive_cluster(map_to_rank(rempty, r));
+            }
             any = any || mine;
             unit_any = unit_any || mine;
             st = st_n;
@@ -1010,14 +1018,15 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
           }
         }
         if (!ok) break;
-        if (PAIR)
-          mma_commit_pair(tfull0 + 8u * acc, 0x3);
-        else if (unit_any)
-          mma_commit(tfull0 + 8u * acc);
-        else
-          mbar_arrive_cluster(map_to_rank(tfull0 + 8u * acc, 0));
-        acc ^= 1u;
-        if (acc == 0u) accph ^= 1u;
+        if (unit_any) {
+          if (PAIR) mma_commit_pair(tfull0 + 8u * acc, 0x3); else mma_commit(tfull0 + 8u * acc);
+        } else {
+          for (uint32_t r = 0; r < kCtas; ++r) mbar_arrive_cluster(map_to_rank(tfull0 + 8u * acc, r));
+        }
+        if (++acc == nbuf) {
+          acc = 0u;
+          accph ^= 1u;
+        }
       }
       if (!ok && any) {
         const uint32_t db = drain_bar + 8u * static_cast<uint32_t>(j);
@@ -1249,7 +1258,10 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_INT4:
       if (p.slot_kb == 4) {
         if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 4>(maps, p, grid, smem, s);
-        if (p.pair && p.conv_groups == 2) return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
+        if (p.pair && p.conv_groups == 2) {
+          if (p.dual) return launch_wna16<4, 2, true, 4, true>(maps, p, grid, smem, s);
+          return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
+        }
         if (!p.pair && p.conv_groups == 2) {
           if (p.dual) return launch_wna16<4, 2, false, 4, true>(maps, p, grid, smem, s);
           return launch_wna16<4, 2, false, 4>(maps, p, grid, smem, s);
@@ -1263,7 +1275,10 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_INT8:  // two converter groups only
       if (p.conv_groups != 2) return cudaErrorInvalidValue;
       if (p.slot_kb == 4) {
-        if (p.pair) return launch_wna16<8, 2, true, 4>(maps, p, grid, smem, s);
+        if (p.pair) {
+          if (p.dual) return launch_wna16<8, 2, true, 4, true>(maps, p, grid, smem, s);
+          return launch_wna16<8, 2, true, 4>(maps, p, grid, smem, s);
+        }
         if (p.dual) return launch_wna16<8, 2, false, 4, true>(maps, p, grid, smem, s);
         return launch_wna16<8, 2, false, 4>(maps, p, grid, smem, s);
       } else if (p.slot_kb == 2) {

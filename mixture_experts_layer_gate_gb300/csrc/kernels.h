@@ -127,8 +127,9 @@ struct GemmParams {
                            // stage, group g its k-blocks 2g and 2g + 1 (else groups alternate stages)
   int acc_cols;            // TMEM columns per accumulator buffer
   int pair;                // 1: CTA-pair kernel (FB counts 256-row weight blocks)
-  int dual;                // int4 / int8, one CTA, whole-stage slots: two MMA-issuing threads, each
-                           // its half of every stage's k-blocks into its own partial accumulator
+  int dual;                // int4 / int8, whole-stage slots: two MMA-issuing threads, each its half
+                           // of every stage's k-blocks into its own partial accumulator
+  int acc_bufs;            // accumulator buffers in TMEM (2; 1 with two issuers and > 64 columns)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
   int epi;                 // EpiKind
   int is_up;

@@ -163,10 +163,14 @@ def _check_plan(shape, pl):
         issuers = getattr(pl, f"issuers_{side}")
         assert issuers in (1, 2)
         if shape.wdtype in ("int4", "int8"):
-            # TMEM holds two accumulators per issuing thread and the converted-weight slot ring
+            # TMEM holds the accumulators (two buffers, or with two issuing threads
+            # two partials per buffer and one buffer above 64 columns) and the
+            # converted-weight slot ring
             sk = getattr(pl, f"slot_kb_{side}")
             assert bn <= 128 and sk in (2, 4)
-            assert 2 <= ast <= 7 and issuers * 2 * ((bn + 31) // 32 * 32) + 32 * sk * ast <= 512
+            acc = (bn + 31) // 32 * 32
+            bufs = 2 if issuers == 1 or acc <= 64 else 1
+            assert 2 <= ast <= 7 and issuers * bufs * acc + 32 * sk * ast <= 512
             # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
             # stage count that is a multiple of g; g = 2 always satisfies both here
             assert ast >= 4 // sk + 1
@@ -176,8 +180,8 @@ def _check_plan(shape, pl):
                 assert st >= ast and (st % 2 == 0 or st == 3)
             else:
                 assert st % 2 == 0 or st % 3 == 0
-            if issuers == 2:  # one CTA, whole-stage slots, tiles of <= 64 tokens
-                assert sk == 4 and bn <= 64 and getattr(pl, f"pair_{side}") == 0
+            if issuers == 2:  # whole-stage slots, two converter groups' ring
+                assert sk == 4
         else:
             assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0 and issuers == 1
     return pl
@@ -198,16 +202,17 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
 
 
-def test_plans_with_two_mma_issuers(lib, monkeypatch):
-    # forced on one CTA: every int4 / int8 GEMM with tiles of <= 64 tokens takes
-    # two issuing threads, the rest keep one; the invariants above still hold
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_plans_with_two_mma_issuers(lib, monkeypatch, pair):
+    # forced, on one CTA or CTA pairs: every int4 / int8 GEMM takes two issuing
+    # threads (bf16 / fp8 keep one); the invariants above still hold
     monkeypatch.setenv("MOE_DUAL", "1")
-    monkeypatch.setenv("MOE_PAIR", "0")
+    monkeypatch.setenv("MOE_PAIR", pair)
     seen = 0
     for shape, p in _all_problems():
         pl = _check_plan(shape, moe.get_plan(p, num_sms=152))
         for side in ("up", "down"):
-            two = shape.wdtype in ("int4", "int8") and getattr(pl, f"bn_max_{side}") <= 64
+            two = shape.wdtype in ("int4", "int8")
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
-            seen += two
+            seen += two and getattr(pl, f"pair_{side}") == int(pair)
     assert seen > 0

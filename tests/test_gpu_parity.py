@@ -241,6 +241,11 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"MOE_FULL_BOX": "0", "MOE_DUAL": "0"}),
     ("dsv3_awq", {"MOE_FULL_BOX": "0"}),
     ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "0", "MOE_FULL_BOX": "0"}),
+    ("dsv3", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
+    ("dsv3_awq", {"MOE_PAIR": "1", "MOE_DUAL": "1", "MOE_KSPLIT": "1"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "128"}),
+    ("mixtral_w8", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
+    ("mixtral_w8_zp", {"MOE_PAIR": "1", "MOE_DUAL": "1", "MOE_BN_MAX": "128"}),
 ])
 def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
     for k, v in knobs.items():
@@ -257,12 +262,14 @@ def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
         gc.full_check(shape, T, dev)
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("splits", [None, "3"])
-def test_two_issuers_short_k_ranges(dev, monkeypatch, splits):
+def test_two_issuers_short_k_ranges(dev, monkeypatch, splits, pair):
     # k ranges that leave the second MMA-issuing thread (k-blocks 2 and 3 of a
     # stage) without work in a stage (split-K tails of one or two k-blocks) or in
-    # a whole unit (the down GEMM's K = 128 is two k-blocks)
-    monkeypatch.setenv("MOE_PAIR", "0")
+    # a whole unit (the down GEMM's K = 128 is two k-blocks), on one CTA and on
+    # CTA pairs (whose arrivals then go to both CTAs)
+    monkeypatch.setenv("MOE_PAIR", pair)
     monkeypatch.setenv("MOE_DUAL", "1")
     if splits:
         monkeypatch.setenv("MOE_SPLITS", splits)
