@@ -208,19 +208,22 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   g.ksplit = 0;
   g.dual = 0;
   g.acc_bufs = 2;
-  // int4 / int8: one CTA per 128 weight rows with two MMA-issuing threads for
-  // small token tiles (<= 32 tokens; int4 <= 64), CTA pairs (M = 256 per MMA)
-  // above that, as for bf16 / fp8 whenever the weight blocks pair up.  Measured
-  // on DeepSeek-V3 int4 (T = 1 to 512) and Mixtral int8 (T = 1, 32; pairs win
-  // at 64 tokens, where int8's larger stages leave one CTA a shallow ring).
+  // int4 / int8: one CTA per 128 weight rows for small token tiles (<= 32
+  // tokens), CTA pairs (M = 256 per MMA) above that, as for bf16 / fp8 whenever
+  // the weight blocks pair up.  Two MMA-issuing threads for every int4 GEMM and
+  // for int8 tiles of <= 32 tokens.  Measured on DeepSeek-V3 int4 (T = 1 to
+  // 4096: two issuers 8-20% faster up to T = 1024, 2% at 4096) and Mixtral int8
+  // (T = 1 to 4096: 8-11% faster at <= 32 tokens, neutral to 1.6% slower above;
+  // one CTA at 64 tokens leaves int8's larger stages a shallow ring).
   // Converting kernels always load whole token tiles: one TMA per stage keeps
   // the producer thread, which shares its SM sub-partition with integer-bound
   // converter warps, short of instructions (ragged tiles otherwise take one box
   // per 64 / 16 rows and k-block).
-  const bool dual_fit = converts(wk) && (g.bn_max <= 32 || (wk == kW_INT4 && g.bn_max <= 64));
+  const bool small_tile = converts(wk) && g.bn_max <= 32;
+  const bool dual_fit = wk == kW_INT4 || (wk == kW_INT8 && small_tile);
   g.pair = 0;
   const int pair_env = env_int("MOE_PAIR", -1);
-  if (g.FB % 2 == 0 && (pair_env == 1 || (pair_env != 0 && !dual_fit))) {
+  if (g.FB % 2 == 0 && (pair_env == 1 || (pair_env != 0 && !small_tile))) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }

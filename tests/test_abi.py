@@ -192,13 +192,14 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
     for shape, p in _all_problems():
         pl = _check_plan(shape, moe.get_plan(p, num_sms=sms))
         for side in ("up", "down"):
-            # int4 / int8 tiles of <= 32 tokens (int4: <= 64) run one CTA per 128
-            # weight rows with two MMA-issuing threads; otherwise CTA pairs exactly
-            # when the weight blocks pair up
+            # int4 / int8 tiles of <= 32 tokens run one CTA per 128 weight rows,
+            # otherwise CTA pairs exactly when the weight blocks pair up; two
+            # MMA-issuing threads for int4, and for int8 tiles of <= 32 tokens
             bn = getattr(pl, f"bn_max_{side}")
             fb = shape.I // 64 if side == "up" else shape.H // 128
-            two = shape.wdtype in ("int4", "int8") and (bn <= 32 or (shape.wdtype == "int4" and bn <= 64))
-            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not two else 0)
+            small = shape.wdtype in ("int4", "int8") and bn <= 32
+            two = shape.wdtype == "int4" or (shape.wdtype == "int8" and small)
+            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not small else 0)
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
 
 

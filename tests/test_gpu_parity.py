@@ -219,18 +219,18 @@ def test_full_size_sampled(dev, name, T):
     ("qwen2", {"MOE_PAIR": "0"}),
     ("dsv3", {"MOE_PAIR": "0"}),
     ("dsv3", {"MOE_PAIR": "1"}),
-    ("dsv3", {"MOE_SLOT_KB": "2"}),
-    ("dsv3", {"MOE_CONV_GROUPS": "3"}),
-    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
+    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
+    ("dsv3", {"MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
+    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
+    ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
     ("dsv3_awq", {"MOE_PAIR": "0"}),
     ("mixtral_w8", {"MOE_PAIR": "0"}),
     ("qwen2_dyn", {"MOE_PAIR": "0"}),
     ("dsv3", {"MOE_KSPLIT": "1"}),
     ("mixtral_w8", {"MOE_KSPLIT": "0", "MOE_PAIR": "0"}),
-    ("mixtral_w8", {"MOE_SLOT_KB": "2"}),
-    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2"}),
-    ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3"}),
+    ("mixtral_w8", {"MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
+    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
+    ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "64"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "32", "MOE_KSPLIT": "1"}),
@@ -242,6 +242,7 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3_awq", {"MOE_FULL_BOX": "0"}),
     ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "0", "MOE_FULL_BOX": "0"}),
     ("dsv3", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
+    ("dsv3", {"MOE_PAIR": "1", "MOE_DUAL": "0"}),
     ("dsv3_awq", {"MOE_PAIR": "1", "MOE_DUAL": "1", "MOE_KSPLIT": "1"}),
     ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "128"}),
     ("mixtral_w8", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
