@@ -248,9 +248,9 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     const int free_cols = 512 - (g.dual ? 2 : 1) * g.acc_bufs * g.acc_cols;
     const int cg_env = env_int("MOE_CONV_GROUPS", 0);
     const int sk_env = env_int("MOE_SLOT_KB", 0);
-    // Two converter groups: the single MMA-issuing thread, not conversion, sets
-    // the pace once slots hold whole stages (three groups measured no faster);
-    // three are available with CTA pairs for tuning.
+    // Two converter groups: with whole-stage slots a third measured no faster
+    // (single-thread issue, of TMA copies and of MMAs, set the pace there); three
+    // remain available with CTA pairs and one MMA issuer for tuning.
     g.conv_groups = 2;
     if (cg_env == 3 && g.pair && wk == kW_INT4 && !g.dual) g.conv_groups = 3;
     auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
