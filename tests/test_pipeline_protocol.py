@@ -490,3 +490,170 @@ def test_model_catches_planted_protocol_mistakes(monkeypatch, mistake):
         except ProtocolError:
             failures += 1
     assert failures > 0
+
+
+# ------------------------------------------ the kernel's cursor bookkeeping
+#
+# The kernel does not compute barrier indices and phases from the definitions
+# the model uses (stage i in ring position i mod stages, phase i div stages);
+# each role keeps incremental ring cursors.  The functions below restate that
+# bookkeeping step by step (csrc/gemm.cu: the producer, converter, MMA-issuer
+# and epilogue loops of grouped_gemm_wna16_kernel, and ring_advance) and the
+# test requires the barrier / parity sequence they produce to be exactly the
+# one the model above verified.
+
+def _ring_advance(pos, phase, idx, target, n):
+    d = target - idx
+    idx = target
+    while d >= n:
+        d -= n
+        phase ^= 1
+    pos += d
+    if pos >= n:
+        pos -= n
+        phase ^= 1
+    return pos, phase, idx
+
+
+def _unit_stages(nkb):
+    return [(kbs, min(4, nkb - kbs)) for kbs in range(0, nkb, 4)]
+
+
+def _kernel_producer(pl, units):
+    ev, st, ph = [], 0, 0
+    for nkb in units:
+        for _ in _unit_stages(nkb):
+            ev.append(("wait", "REMPTY", st, ph ^ 1))
+            ev.append(("arrive", "RFULL", st))
+            ev.append(("tma", "RFULL", st))
+            st += 1
+            if st == pl.ns:
+                st, ph = 0, ph ^ 1
+    return ev
+
+
+def _kernel_converter(pl, units, grp):
+    ev = []
+    ci = cst = cs = ca = 0
+    cph = cap = 0
+    pi = pst = 0
+    pph = 0
+    ui = us = 0
+    spp = 4 // pl.sk
+    for nkb in units:
+        nst = (nkb + 3) // 4
+        l = 0 if pl.ks else grp - ui % pl.cg
+        if l < 0:
+            l += pl.cg
+        while l < nst:
+            cst, cph, ci = _ring_advance(cst, cph, ci, ui + l, pl.ns)
+            ca, cap, cs = _ring_advance(ca, cap, cs, us + spp * l, pl.na)
+            nk = min(4, nkb - 4 * l)
+            ev.append(("wait", "RFULL", cst, cph))
+            if pl.sk == 4 and ui + l >= pl.na:
+                pst, pph, pi = _ring_advance(pst, pph, pi, ui + l - pl.na, pl.ns)
+                ev.append(("wait", "REMPTY", pst, pph))
+            a, ap = ca, cap
+            j0, j1 = (2 * grp, min(nk, 2 * grp + 2)) if pl.ks else (0, nk)
+            for j in range(j0, j1):
+                js = j & (pl.sk - 1)
+                if pl.sk != 4 and js == 0:
+                    ev.append(("wait", "AEMPTY", a, ap ^ 1))
+                if not pl.ks and (js == pl.sk - 1 or j == nk - 1):
+                    ev.append(("arrive", "AFULL", a))
+                    a += 1
+                    if a == pl.na:
+                        a, ap = 0, ap ^ 1
+            if pl.ks:
+                ev.append(("arrive", "AFULL", a))
+            l += 1 if pl.ks else pl.cg
+        if nst > 0:
+            ui += nst
+            us += spp * (nst - 1) + (nkb - 4 * (nst - 1) + pl.sk - 1) // pl.sk
+    return ev
+
+
+def _kernel_issuer(pl, units, j):
+    ev = []
+    jb0 = 2 * j if pl.dual else 0
+    nbuf = pl.nbuf if pl.dual else 2
+    st = as_ = 0
+    ph = aph = acc = accph = 0
+    for nkb in units:
+        ev.append(("wait", "TEMPTY", acc, accph ^ 1))
+        unit_any = not pl.dual
+        for kbs, nk in _unit_stages(nkb):
+            if pl.sk == 4:
+                jend = min(nk, jb0 + 2) if pl.dual else nk
+                mine = (not pl.dual) or jb0 < jend
+                ev.append(("wait", "AFULL", as_, aph))
+                ev.append(("commit" if mine else "arrive", "REMPTY", st))
+                unit_any = unit_any or mine
+                st += 1
+                if st == pl.ns:
+                    st, ph = 0, ph ^ 1
+                as_ += 1
+                if as_ == pl.na:
+                    as_, aph = 0, aph ^ 1
+            else:
+                for jp in range(0, nk, pl.sk):
+                    ev.append(("wait", "AFULL", as_, aph))
+                    ev.append(("commit", "AEMPTY", as_))
+                    as_ += 1
+                    if as_ == pl.na:
+                        as_, aph = 0, aph ^ 1
+                ev.append(("commit", "REMPTY", st))
+                st += 1
+                if st == pl.ns:
+                    st, ph = 0, ph ^ 1
+        ev.append(("commit" if unit_any else "arrive", "TFULL", acc))
+        acc += 1
+        if acc == nbuf:
+            acc, accph = 0, accph ^ 1
+    return ev
+
+
+def _kernel_epilogue(pl, units):
+    ev = []
+    nbuf = pl.nbuf if pl.dual else 2
+    acc = accph = 0
+    for _ in units:
+        ev.append(("wait", "TFULL", acc, accph))
+        ev.append(("arrive", "TEMPTY", acc))
+        acc += 1
+        if acc == nbuf:
+            acc, accph = 0, accph ^ 1
+    return ev
+
+
+def _model_events(gen):
+    """The model role's barrier operations as (op, barrier kind, ring index[, parity])."""
+    ev = []
+    for op in gen:
+        if op[0] == "wait":
+            ev.append(("wait", op[1][0], op[1][-1], op[2] & 1))
+        elif op[0] in ("arrive", "tma"):
+            ev.append((op[0], op[1][0], op[1][-1]))
+        elif op[0] == "commit":
+            name = op[1][0][0]
+            ev.append(("commit", name[0], name[-1]))
+    return ev
+
+
+def test_kernel_bookkeeping_matches_the_model():
+    rng = random.Random(7)
+    checked = 0
+    for pl in ACCEPTED:
+        if pl.ctas != 1:
+            continue  # the leader's cursors are the same with a CTA pair
+        for _ in range(3):
+            units = [rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 12, 16, 17]) for _ in range(rng.randint(1, 7))]
+            sim = Sim(pl, units, random.Random(0))
+            assert _kernel_producer(pl, units) == _model_events(sim.producer(0)), pl
+            for g in range(pl.cg):
+                assert _kernel_converter(pl, units, g) == _model_events(sim.converter(0, g, 0)), (pl, g, units)
+            for j in range(2 if pl.dual else 1):
+                assert _kernel_issuer(pl, units, j) == _model_events(sim.issuer(j)), (pl, j, units)
+            assert _kernel_epilogue(pl, units) == _model_events(sim.epilogue(0, 0)), pl
+            checked += 1
+    assert checked > 100
