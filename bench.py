@@ -320,6 +320,39 @@ def run_ours(args):
     roof["l2_flushed"] = kflush is not None
     roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
 
+    # per-stage times: each entry point on its own, CUDA events between them on the
+    # stream, no graph (L2 flushed before each rep where the step is flushed)
+    y_perm = torch.empty((S, shape.H), dtype=torch.bfloat16, device=dev)
+    out_s = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(max(5, args.steps))]
+    with torch.cuda.stream(stream):
+        for evs in sev:
+            if flush is not None:
+                flush()
+            evs[0].record(stream)
+            moe.gate_topk(p, tok.logits, tok.bias, ids, tw, stream.cuda_stream)
+            evs[1].record(stream)
+            moe.align_permute(p, ids, tok.x, tok.a1_scale, counts_t, offsets, perm, inv, x_perm, ws,
+                              stream.cuda_stream)
+            evs[2].record(stream)
+            moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
+            evs[3].record(stream)
+            moe.grouped_gemm_down(p, wts, act, offsets, y_perm, ws, stream.cuda_stream)
+            evs[4].record(stream)
+            moe.unpermute_reduce(p, y_perm, inv, tw, out_s, ws, stream.cuda_stream)
+            evs[5].record(stream)
+    stream.synchronize()
+    if moe.get_device_error(ws, stream.cuda_stream) != 0:
+        raise RuntimeError("device error in the staged run")
+    stage_names = ("gate_topk", "align_permute", "gate_up_swiglu", "down", "unpermute_reduce")
+    stages_us = {n: sum(e[i].elapsed_time(e[i + 1]) for e in sev) / len(sev) * 1e3
+                 for i, n in enumerate(stage_names)}
+    # bytes the intermediates move (written once, read once): overhead, not algorithmic
+    act_rw = S * shape.I * abytes * 2 + (S * shape.I * 2 * 2 if shape.act_scale == "dynamic" else 0)
+    inter_bytes = {"x_perm": S * shape.H * abytes * 2, "act": act_rw, "y_perm": S * shape.H * 2 * 2,
+                   "split_k_partials": (plan.splits_up * S * 2 * shape.I * 4 * 2 if plan.splits_up > 1 else 0) +
+                   (plan.splits_down * S * shape.H * 4 * 2 if plan.splits_down > 1 else 0)}
+
     # end to end through the public call with host buffers: every step uploads its
     # inputs (x, logits) from pinned host memory, runs moe_forward and reads its
     # output back.  Steps are pipelined the way a serving loop would run them:
@@ -393,6 +426,9 @@ def run_ours(args):
                                                 "sms": plan.num_sms}},
         "layer_roofline": {"t_roof_us": t_roof * 1e6, "frac": layer_frac, "touched_experts": touched,
                            "bytes": B, "flops": F},
+        "stages_us": stages_us,
+        "stages_note": "each entry point alone, CUDA events between them, no graph or PDL overlap",
+        "intermediate_bytes": inter_bytes,
         "roofline": roof,
         "e2e": {"value": job_throughput(world, T, e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + l_h.numel() * 4),
