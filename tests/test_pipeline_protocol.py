@@ -17,7 +17,10 @@ roles interleaved at random, and checks for each plan shape the kernel accepts:
 - no deadlock.
 
 Shapes that break the planner's ring rules (stages not a multiple of the
-converter groups, too few slots) are shown to fail the same checks.
+converter groups, too few slots) are shown to fail the same checks.  The bf16 /
+fp8 kernels (one CTA or a CTA pair) are checked the same way, and for both
+families the kernel's incremental ring-cursor bookkeeping, restated here, must
+produce the barrier / parity sequence the model verified.
 """
 import random
 
@@ -240,9 +243,7 @@ class Sim:
             d *= self.rng.randint(10, 60)
         return d
 
-    def run(self):
-        """Timed event simulation: roles take a random time per step, copies and
-        MMAs complete after random latencies (MMAs of one thread in issue order)."""
+    def roles(self):
         pl = self.pl
         gens = {}
         for c in range(pl.ctas):
@@ -253,12 +254,19 @@ class Sim:
             for w in range(4):
                 gens[("epilogue", c, w)] = self.epilogue(c, w)
         for j in range(2 if pl.dual else 1):
-            k = ("issuer", j)
-            gens[k] = self.issuer(j)
-            self.mma_queue[k] = []
-            self.issued[k] = 0
-            self.completed[k] = 0
-            self.commits[k] = []
+            gens[("issuer", j)] = self.issuer(j)
+        return gens
+
+    def run(self):
+        """Timed event simulation: roles take a random time per step, copies and
+        MMAs complete after random latencies (MMAs of one thread in issue order)."""
+        gens = self.roles()
+        for k in gens:
+            if k[0] == "issuer":
+                self.mma_queue[k] = []
+                self.issued[k] = 0
+                self.completed[k] = 0
+                self.commits[k] = []
         nxt = {k: next(g, None) for k, g in gens.items()}
         self.t_role = t_role = {k: self._delay(5) for k in gens}
         self.state = state = {}   # role -> "waiting" while its next op is an unmet wait
@@ -657,3 +665,152 @@ def test_kernel_bookkeeping_matches_the_model():
             assert _kernel_epilogue(pl, units) == _model_events(sim.epilogue(0, 0)), pl
             checked += 1
     assert checked > 100
+
+
+
+# ------------------------------------------------ bf16 / fp8 grouped GEMMs
+#
+# grouped_gemm_kernel (one CTA) and grouped_gemm_pair_kernel (two CTAs sharing
+# M = 256 MMAs): the producer of each CTA loads its weight rows and token rows
+# per k-block into a ring of `ns` stages whose FULL barrier is the leader's
+# (one expect-tx arrival for both CTAs' bytes, completed by each CTA's copies),
+# the leader's single issuer waits for it, and its commits free the stage in
+# both CTAs (EMPTY) and hand the accumulator to both CTAs' epilogues (TFULL).
+
+class DenseSim(Sim):
+    def __init__(self, ns, ctas, units, rng):
+        self.pl = Plan(ns, 2, ctas=ctas)
+        self.units, self.rng = units, rng
+        self.kblocks = [(u, kb) for u, nkb in enumerate(units) for kb in range(nkb)]
+        self.bars = {}
+        for c in range(ctas):
+            for st in range(ns):
+                self.bars[("EMPTY", c, st)] = Barrier(("EMPTY", c, st), 1)
+            for b in range(2):
+                self.bars[("TFULL", c, b)] = Barrier(("TFULL", c, b), 1)
+        for st in range(ns):
+            self.bars[("FULL", st)] = Barrier(("FULL", st), 1 + ctas)   # leader's
+        for b in range(2):
+            self.bars[("TEMPTY", b)] = Barrier(("TEMPTY", b), 4 * ctas)
+        self.res, self.mma_queue, self.issued, self.completed, self.commits = {}, {}, {}, {}, {}
+        self.async_ops = []
+
+    def roles(self):
+        gens = {}
+        for c in range(self.pl.ctas):
+            gens[("producer", c)] = self.dense_producer(c)
+            for w in range(4):
+                gens[("epilogue", c, w)] = self.dense_epilogue(c, w)
+        gens[("issuer", 0)] = self.dense_issuer()
+        return gens
+
+    def dense_producer(self, c):
+        ns = self.pl.ns
+        for i, _ in enumerate(self.kblocks):
+            st, use = i % ns, i // ns
+            yield ("wait", ("EMPTY", c, st), use - 1)
+            if c == 0:
+                yield ("arrive", ("FULL", st), use)      # the leader's expect-tx for both CTAs
+            yield ("tma", ("FULL", st), use, self.r("stage", c, st), use)
+
+    def dense_issuer(self):
+        ns, C = self.pl.ns, range(self.pl.ctas)
+        i = 0
+        for uu, nkb in enumerate(self.units):
+            b, use_b = uu % 2, uu // 2
+            yield ("wait", ("TEMPTY", b), use_b - 1)
+            for _ in range(nkb):
+                st, use = i % ns, i // ns
+                yield ("wait", ("FULL", st), use)
+                yield ("mma", [(self.r("stage", c, st), use) for c in C], [self.r("acc", c, b, 0) for c in C], uu)
+                yield ("commit", [(("EMPTY", c, st), use) for c in C])
+                i += 1
+            yield ("commit", [(("TFULL", c, b), use_b) for c in C])
+
+    def dense_epilogue(self, c, w):
+        for uu, _ in enumerate(self.units):
+            b, use_b = uu % 2, uu // 2
+            yield ("wait", ("TFULL", c, b), use_b)
+            yield ("read", self.r("acc", c, b, 0), uu)
+            yield ("arrive", ("TEMPTY", b), use_b)
+
+
+def _dense_units(rng):
+    return [rng.choice([1, 2, 3, 5, 8, 13, 28, 56]) for _ in range(rng.randint(1, 6))]
+
+
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_dense_protocol_holds(ctas):
+    for ns in range(2, 9):
+        for seed in range(6):
+            rng = random.Random(100 * ns + seed)
+            try:
+                DenseSim(ns, ctas, _dense_units(rng), rng).run()
+            except ProtocolError as e:
+                raise ProtocolError(f"ns={ns}, ctas={ctas}, seed {seed}: {e}") from None
+
+
+def test_dense_model_catches_a_stage_freed_before_its_mmas_complete(monkeypatch):
+    orig = DenseSim.dense_issuer
+
+    def issuer(self):
+        for op in orig(self):
+            if op[0] == "commit" and op[1][0][0][0] == "EMPTY":
+                for bar, phase in op[1]:
+                    yield ("arrive", bar, phase)
+            else:
+                yield op
+    monkeypatch.setattr(DenseSim, "dense_issuer", issuer)
+    failures = 0
+    for seed in range(30):
+        rng = random.Random(seed)
+        try:
+            DenseSim(4, 2, _dense_units(rng), rng).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
+
+
+def _kernel_dense(ns, units):
+    """The dense kernels' cursor bookkeeping (producer, issuer, epilogue loops)."""
+    prod, iss, epi = [], [], []
+    st = ph = 0
+    for nkb in units:
+        for _ in range(nkb):
+            prod.append(("wait", "EMPTY", st, ph ^ 1))
+            st += 1
+            if st == ns:
+                st, ph = 0, ph ^ 1
+    st = ph = acc = accph = 0
+    for nkb in units:
+        iss.append(("wait", "TEMPTY", acc, accph ^ 1))
+        for _ in range(nkb):
+            iss.append(("wait", "FULL", st, ph))
+            iss.append(("commit", "EMPTY", st))
+            st += 1
+            if st == ns:
+                st, ph = 0, ph ^ 1
+        iss.append(("commit", "TFULL", acc))
+        acc ^= 1
+        if acc == 0:
+            accph ^= 1
+    acc = accph = 0
+    for _ in units:
+        epi.append(("wait", "TFULL", acc, accph))
+        epi.append(("arrive", "TEMPTY", acc))
+        acc ^= 1
+        if acc == 0:
+            accph ^= 1
+    return prod, iss, epi
+
+
+def test_dense_kernel_bookkeeping_matches_the_model():
+    rng = random.Random(11)
+    for ns in range(2, 9):
+        for _ in range(5):
+            units = _dense_units(rng)
+            sim = DenseSim(ns, 1, units, random.Random(0))
+            prod, iss, epi = _kernel_dense(ns, units)
+            assert prod == [e for e in _model_events(sim.dense_producer(0)) if e[0] == "wait"]
+            assert iss == _model_events(sim.dense_issuer())
+            assert epi == _model_events(sim.dense_epilogue(0, 0))
