@@ -19,6 +19,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -83,7 +84,9 @@ def _env_int(name, default):
 class ClockSampler:
     """nvidia-smi clock / throttle samples every 50 ms; `mark()` brackets the
     timed region, whose samples the summary keeps (all samples if none fell
-    inside, e.g. a region shorter than the interval, flagged in the summary)."""
+    inside, e.g. a region shorter than the interval, flagged in the summary).
+    The raw samples go to MOE_CLOCK_LOG_DIR/clocks_rank<i>.csv when that variable
+    names a directory, else to a temporary file removed after the summary."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
@@ -91,7 +94,13 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        log_dir = os.environ.get("MOE_CLOCK_LOG_DIR")
+        self.keep = bool(log_dir)
+        if self.keep:
+            self.path = os.path.join(log_dir, f"clocks_rank{gpu_index}.csv")
+        else:
+            fd, self.path = tempfile.mkstemp(prefix=f"moe_clocks_rank{gpu_index}_", suffix=".csv")
+            os.close(fd)
         self.t0 = self.t1 = None
 
     def mark(self, start: bool):
@@ -123,6 +132,11 @@ class ClockSampler:
 
     def summary(self):
         if self.proc is None:
+            if not self.keep:
+                try:
+                    os.remove(self.path)
+                except OSError:
+                    pass
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         rows = []
@@ -143,6 +157,11 @@ class ClockSampler:
                 rows.append((ts, sm, smax, [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]))
         except OSError:
             pass
+        if not self.keep:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
         inside = [r for r in rows if r[0] is not None and self.t0 is not None and self.t1 is not None
                   and self.t0 <= r[0] <= self.t1]
         use = inside or rows

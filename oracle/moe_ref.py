@@ -20,7 +20,7 @@ page prints a formula, so each stage below states the plain reading it takes):
   4. Unpermute and top-k weighted reduction (TensorRT-LLM's
      unpermute_and_reduce on "Add deepseek_v3 fused gate").
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * Softmax selection keys are the raw fp32 logits (softmax is monotone).
   * Ids are ordered by key, descending; equal keys go to the lower index.
   * Sigmoid gate: s = sigmoid(l); key = s + bias (bias only steers selection);
