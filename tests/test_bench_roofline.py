@@ -63,3 +63,22 @@ def test_quantised_formats_count_their_scales_and_zero_points():
 def test_job_throughput_counts_every_replica_over_the_slowest_rank():
     assert bench.job_throughput(1, 4096, 2.0) == pytest.approx(2.048e6)
     assert bench.job_throughput(4, 4096, 2.0) == pytest.approx(4 * 2.048e6)
+
+
+def test_clock_sampler_keeps_raw_samples_only_where_asked(tmp_path, monkeypatch):
+    # without a log directory the raw samples live in a temporary file removed by
+    # the summary; with one they stay there (no GPU needed: without nvidia-smi the
+    # summary says so)
+    import os
+    monkeypatch.delenv("MOE_CLOCK_LOG_DIR", raising=False)
+    c = bench.ClockSampler(0)
+    with c:
+        pass
+    c.summary()
+    assert not os.path.exists(c.path)
+    monkeypatch.setenv("MOE_CLOCK_LOG_DIR", str(tmp_path))
+    c = bench.ClockSampler(1)
+    with c:
+        pass
+    c.summary()
+    assert c.path == str(tmp_path / "clocks_rank1.csv")
