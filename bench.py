@@ -573,7 +573,7 @@ class _OracleRunner:
         import numpy as np
         import oracle
         self.np, self.oracle = np, oracle
-        from tests.oracle_io import np_of, bf16_bits
+        from oracle.torch_io import np_of, bf16_bits
         T = tok.x.shape[0]
         n = min(sample, T)
         rows = np.linspace(0, T - 1, n).astype(np.int64)

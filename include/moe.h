@@ -22,7 +22,8 @@
  *   - All tensor pointers are DEVICE pointers, row-major, 16-byte aligned,
  *     owned by the caller.  The library allocates nothing and keeps no state
  *     between calls other than per-device constants (SM count, driver entry
- *     point) looked up on first use.
+ *     point) looked up on first use and the planner overrides a caller sets
+ *     with moe_set_tuning.
  *   - Every call is asynchronous and stream-ordered on `stream` (a
  *     cudaStream_t; NULL = legacy default stream).  No call synchronises with
  *     the host except moe_get_device_error.  Calls can be captured in a CUDA
@@ -187,8 +188,13 @@ moe_status_t moe_align_permute(const moe_problem_t* p, const int32_t* topk_ids, 
  *   the process exits.  Limit: ceil(T*k / 1024) * E <= 65536 (e.g. E = 256 up
  *   to T*k = 262144); larger problems return MOE_ERR_UNSUPPORTED and launch
  *   nothing.  No cudaMalloc/cudaFree or other allocation happens.
- *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   The first call in each CUDA context (e.g. the first per device, in its
+ *   primary context) looks up the array's device address with that context
+ *   current and caches it for the context; make that first call before any
+ *   stream capture.  A context created later (another context on the device,
+ *   or the primary context again after a device reset) gets its own lookup on
+ *   its first call; at most 64 contexts per process are served, later ones get
+ *   MOE_ERR_CUDA.
  *   All calls share the one array: calls whose GPU work can overlap (e.g. on
  *   two unsynchronised streams) race; order them.  Expert ids outside [0, E)
  *   are still routed to expert 0 but are not reported (there is no error
@@ -293,6 +299,34 @@ typedef struct {
   int32_t pair_up, pair_down;
   int32_t issuers_up, issuers_down;
 } moe_plan_t;
+
+/* Planner overrides, for tests and benchmarks that want a kernel variant the
+ * planner would not pick for a problem (results stay within the same
+ * tolerances; only speed changes).  Each field is -1 for the planner's own
+ * choice:
+ *   bn_max      token tile limit, a multiple of 16 in [16, 256] (int4 / int8
+ *               take it only up to 128)
+ *   stages      operand ring depth, 2..8 (only ever lowers the planner's)
+ *   splits      split-K factor, 1..16 (at most K / 256; a workspace sized for
+ *               fewer slices makes the GEMM call return MOE_ERR_UNSUPPORTED)
+ *   pair        1: clusters of two CTAs sharing M = 256 MMAs, 0: one CTA per
+ *               128 weight rows (pairs need an even number of weight blocks)
+ *   conv_groups int4 with CTA pairs and one MMA issuer: 3 converter warp groups
+ *   slot_kb     int4 / int8: k-blocks per converted weight slot, 2 or 4
+ *   ksplit      int4 / int8: 1 = both converter groups convert every stage
+ *   dual        int4 / int8: 1 = two MMA-issuing threads, 0 = one
+ *   full_box    1 = whole token tiles in one TMA box per stage, 0 = 64- and
+ *               16-row boxes for an expert's ragged last tile
+ *   w_stream    1 = weights loaded with the L2 evict-first policy, 0 = normal
+ * The overrides apply to every later plan of the process (all threads) until
+ * the next call; NULL restores the planner's choices.  Values outside those
+ * ranges return MOE_ERR_INVALID_ARG and change nothing.  The library never
+ * reads tuning from the environment. */
+typedef struct {
+  int32_t bn_max, stages, splits, pair, conv_groups, slot_kb, ksplit, dual, full_box, w_stream;
+} moe_tuning_t;
+
+moe_status_t moe_set_tuning(const moe_tuning_t* t);
 
 /* Plan on the current device. */
 moe_status_t moe_get_plan(const moe_problem_t* p, moe_plan_t* plan);

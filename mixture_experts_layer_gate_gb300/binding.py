@@ -24,7 +24,7 @@ EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "mo
             "moe_align_permute", "moe_align_block_size", "moe_grouped_gemm_swiglu",
             "moe_grouped_gemm_down", "moe_unpermute_reduce", "moe_forward", "moe_get_device_error",
             "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms", "moe_align_permute_noalloc",
-            "moe_dynamic_scales", "moe_launch_count")
+            "moe_dynamic_scales", "moe_launch_count", "moe_set_tuning")
 
 
 class MoEError(RuntimeError):
@@ -62,6 +62,13 @@ class Plan(ctypes.Structure):
                 ("issuers_up", ctypes.c_int32), ("issuers_down", ctypes.c_int32)]
 
 
+class Tuning(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("bn_max", "stages", "splits", "pair", "conv_groups", "slot_kb",
+                                             "ksplit", "dual", "full_box", "w_stream")]
+
+
+TUNING_KNOBS = tuple(n for n, _ in Tuning._fields_)
+
 _lib = None
 
 
@@ -93,6 +100,7 @@ def load(path: str = LIB_PATH):
         "moe_get_plan_for_sms": (st, [P, i32, ctypes.POINTER(Plan)]),
         "moe_dynamic_scales": (vp, [vp]),
         "moe_launch_count": (ctypes.c_uint64, []),
+        "moe_set_tuning": (st, [ctypes.POINTER(Tuning)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -240,6 +248,33 @@ def get_plan(p: Problem, num_sms: int | None = None) -> Plan:
         _check(load().moe_get_plan_for_sms(ctypes.byref(p), int(num_sms), ctypes.byref(plan)),
                "moe_get_plan_for_sms")
     return plan
+
+
+def set_tuning(**knobs):
+    """Planner overrides (moe_set_tuning): keyword per knob, e.g. pair=0, dual=1;
+    no keywords restores the planner's choices.  For tests and benchmarks."""
+    unknown = set(knobs) - set(TUNING_KNOBS)
+    if unknown:
+        raise ValueError(f"unknown tuning knobs {sorted(unknown)}")
+    if not knobs:
+        _check(load().moe_set_tuning(None), "moe_set_tuning")
+        return
+    t = Tuning(*[int(knobs.get(n, -1)) for n in TUNING_KNOBS])
+    _check(load().moe_set_tuning(ctypes.byref(t)), "moe_set_tuning")
+
+
+class tuning:
+    """Context manager: planner overrides inside the block, defaults after it."""
+
+    def __init__(self, **knobs):
+        self.knobs = knobs
+
+    def __enter__(self):
+        set_tuning(**self.knobs)
+        return self
+
+    def __exit__(self, *exc):
+        set_tuning()
 
 
 class MoELayer:

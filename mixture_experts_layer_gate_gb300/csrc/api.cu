@@ -6,7 +6,6 @@
 
 #include <algorithm>
 #include <atomic>
-#include <cstdlib>
 #include <cmath>
 #include <mutex>
 
@@ -39,7 +38,9 @@ inline int roundup16(int x) { return (x + 15) & ~15; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-moe_status_t validate_problem(const moe_problem_t* p) {
+}  // namespace
+
+moe_status_t moe::validate_problem(const moe_problem_t* p) {
   if (p == nullptr) return MOE_ERR_INVALID_ARG;
   if (p->T < 0 || p->H <= 0 || p->I <= 0 || p->E <= 0 || p->top_k <= 0) return MOE_ERR_INVALID_ARG;
   if (p->H % 128 != 0 || p->I % 128 != 0) return MOE_ERR_INVALID_ARG;
@@ -68,6 +69,8 @@ moe_status_t validate_problem(const moe_problem_t* p) {
   if (p->act_scale == MOE_ACT_SCALE_DYNAMIC && p->wdtype != MOE_W_FP8_E4M3) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
+
+namespace {
 
 // ------------------------------------------------------------ device facts
 
@@ -130,14 +133,19 @@ struct GemmPlan {
   size_t smem;
 };
 
-// Tuning overrides (benchmarking and tests only; the defaults are the planner's):
-// MOE_BN_MAX, MOE_STAGES, MOE_SPLITS, MOE_PAIR, MOE_CONV_GROUPS, MOE_SLOT_KB,
-// MOE_KSPLIT, MOE_DUAL, MOE_FULL_BOX, MOE_W_STREAM.
-int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  if (v == nullptr || *v == 0) return dflt;
-  return std::atoi(v);
+// Planner overrides set through moe_set_tuning (tests and benchmarks only; a
+// field of -1 leaves the planner's choice).  Nothing is read from the
+// environment: a process gets these only by calling moe_set_tuning.
+std::mutex g_tuning_mu;
+moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+
+moe_tuning_t current_tuning() {
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  return g_tuning;
 }
+
+// The override of one knob, or `dflt` when it is unset.
+inline int knob(int32_t v, int dflt) { return v < 0 ? dflt : v; }
 
 int wkind_of(const moe_problem_t& p) {
   switch (p.wdtype) {
@@ -194,13 +202,14 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   GemmPlan g;
   const int wk = wkind_of(p);
   g.bn_max = plan_bn_max(p);
-  const int bn_env = env_int("MOE_BN_MAX", 0);
+  const moe_tuning_t tu = current_tuning();
+  const int bn_env = knob(tu.bn_max, 0);
   if (bn_env >= 16 && bn_env <= (converts(wk) ? 128 : 256) && bn_env % 16 == 0) g.bn_max = bn_env;
   g.FB = up ? p.I / 64 : p.H / 128;
   const int K = up ? p.H : p.I;
   g.KB = K / (wk == kW_FP8 ? 128 : 64);
   g.P = plan_splits(p, up, g.bn_max, g.KB, std::min(sms, kSmsForSizing));
-  const int p_env = env_int("MOE_SPLITS", 0);
+  const int p_env = knob(tu.splits, 0);
   if (p_env >= 1 && p_env <= kMaxSplits && p_env <= std::max(1, g.KB / 4)) g.P = p_env;
   size_t per_stage;
   int cap;
@@ -222,12 +231,12 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   const bool small_tile = converts(wk) && g.bn_max <= 32;
   const bool dual_fit = wk == kW_INT4 || (wk == kW_INT8 && small_tile);
   g.pair = 0;
-  const int pair_env = env_int("MOE_PAIR", -1);
+  const int pair_env = knob(tu.pair, -1);
   if (g.FB % 2 == 0 && (pair_env == 1 || (pair_env != 0 && !small_tile))) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
-  g.full_box = env_int("MOE_FULL_BOX", converts(wk) ? 1 : 0) != 0 ? 1 : 0;
+  g.full_box = knob(tu.full_box, converts(wk) ? 1 : 0) != 0 ? 1 : 0;
   if (converts(wk)) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of
     // slot_kb k-blocks (32 columns each).  A converter group that fills the
@@ -240,14 +249,14 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // accumulators, two buffers of them where that leaves room for two
     // whole-stage slots (<= 64 columns), else one buffer (<= 128 columns; the
     // epilogue of a unit then no longer overlaps the next unit's MMAs).
-    const int dual_env = env_int("MOE_DUAL", -1);
+    const int dual_env = knob(tu.dual, -1);
     if (g.acc_cols <= 128 && (dual_env == 1 || (dual_env != 0 && dual_fit))) {
       g.dual = 1;
       g.acc_bufs = g.acc_cols <= 64 ? 2 : 1;
     }
     const int free_cols = 512 - (g.dual ? 2 : 1) * g.acc_bufs * g.acc_cols;
-    const int cg_env = env_int("MOE_CONV_GROUPS", 0);
-    const int sk_env = env_int("MOE_SLOT_KB", 0);
+    const int cg_env = knob(tu.conv_groups, 0);
+    const int sk_env = knob(tu.slot_kb, 0);
     // Two converter groups: with whole-stage slots a third measured no faster
     // (single-thread issue, of TMA copies and of MMAs, set the pace there); three
     // remain available with CTA pairs and one MMA issuer for tuning.
@@ -272,7 +281,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   const int brows = g.pair ? g.bn_max / 2 : g.bn_max;
   const size_t fixed = gemm_smem_bytes(wk, brows, 0, g.astages, p.E);
   g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed) / per_stage));
-  const int st_env = env_int("MOE_STAGES", 0);
+  const int st_env = knob(tu.stages, 0);
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
   while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E) > kMaxDynSmem)
     --g.stages;
@@ -284,7 +293,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // depth), so it is taken only where rounding down would leave a shallow ring
     // (int8 codes with 128-token tiles: three stages instead of two).
     const int alt = g.stages - g.stages % g.conv_groups;
-    const int ks_env = env_int("MOE_KSPLIT", -1);
+    const int ks_env = knob(tu.ksplit, -1);
     const bool can_ks = g.conv_groups == 2 && g.slot_kb == kSuper;
     g.ksplit = (can_ks && (ks_env == 1 || (ks_env != 0 && alt < 4 && g.stages > alt))) ? 1 : 0;
     if (!g.ksplit) g.stages = alt;
@@ -509,7 +518,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const long long touched = std::max(1ll, std::min<long long>(p.E, Sl));
     const long long m_avg = (Sl + touched - 1) / touched;
     gp.w_stream = (m_avg <= g.bn_max) ? 1 : 0;
-    const int ws_env = env_int("MOE_W_STREAM", -1);
+    const int ws_env = knob(current_tuning().w_stream, -1);
     if (ws_env == 0 || ws_env == 1) gp.w_stream = ws_env;
   }
   gp.KB = g.KB;
@@ -799,6 +808,22 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->pair_down = d.pair;
   plan->issuers_up = u.dual ? 2 : 1;
   plan->issuers_down = d.dual ? 2 : 1;
+  return MOE_OK;
+}
+
+moe_status_t moe_set_tuning(const moe_tuning_t* t) {
+  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (t != nullptr) {
+    v = *t;
+    auto ok = [](int32_t x, int32_t lo, int32_t hi) { return x == -1 || (x >= lo && x <= hi); };
+    if (!ok(v.bn_max, 16, 256) || (v.bn_max > 0 && v.bn_max % 16 != 0) || !ok(v.stages, 2, kMaxStages) ||
+        !ok(v.splits, 1, kMaxSplits) || !ok(v.pair, 0, 1) || !ok(v.conv_groups, 2, 3) ||
+        !(v.slot_kb == -1 || v.slot_kb == 2 || v.slot_kb == 4) || !ok(v.ksplit, 0, 1) || !ok(v.dual, 0, 1) ||
+        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1))
+      return MOE_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  g_tuning = v;
   return MOE_OK;
 }
 

@@ -9,6 +9,12 @@
 
 namespace moe {
 
+#ifdef MOE_GB300_H
+// Problem checks shared by every entry point: MOE_OK, MOE_ERR_INVALID_ARG for a
+// malformed problem, MOE_ERR_UNSUPPORTED for one beyond the library's limits.
+moe_status_t validate_problem(const moe_problem_t* p);
+#endif
+
 // ------------------------------------------------------------------- gate
 struct GateArgs {
   const float* logits;  // [T, E]

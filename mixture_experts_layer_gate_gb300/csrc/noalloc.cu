@@ -3,6 +3,8 @@
 // per-CTA expert histograms it needs between its two passes live in a
 // fixed-size array that is part of the library's own device image instead of
 // a caller-provided workspace.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -20,25 +22,61 @@ constexpr size_t kNoAllocScratchBytes = 256 * 1024;
 // it names a host-side shadow, so its device address is looked up below.
 static __device__ __align__(256) unsigned char g_align_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
+// The array's device address is cached per CUDA context (the address belongs to
+// the module as loaded into one context: another context on the same device,
+// or the primary context re-created after a device reset, has its own copy).
+constexpr int kMaxContexts = 64;
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct CachedAddress {
+  CUcontext ctx;
+  void* addr;
+};
+CachedAddress g_cache[kMaxContexts] = {};
+int g_cached = 0;
 
-// Device address of g_align_scratch on the current device, looked up once per
-// device (with that device current) and cached.
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static std::once_flag once;
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// Device address of g_align_scratch in the current context, looked up with
+// cudaGetSymbolAddress the first time a context calls (the runtime makes the
+// device's primary context current if none is) and cached for it.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_align_scratch);
+  auto get_ctx = ctx_get_current_fn();
+  if (get_ctx == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  void* fresh = nullptr;
+  if (ctx == nullptr) {
+    // no context bound to this thread yet: the symbol lookup binds the current
+    // device's primary context, which is then the one to key the address by
+    const cudaError_t err = cudaGetSymbolAddress(&fresh, g_align_scratch);
     if (err != cudaSuccess) return err;
-    g_scratch_addr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
   }
-  *out = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_cached; ++i) {
+    if (g_cache[i].ctx == ctx) {
+      *out = g_cache[i].addr;
+      return cudaSuccess;
+    }
+  }
+  if (g_cached == kMaxContexts) return cudaErrorNotSupported;  // cache full: refuse, never guess
+  if (fresh == nullptr) {
+    const cudaError_t err = cudaGetSymbolAddress(&fresh, g_align_scratch);
+    if (err != cudaSuccess) return err;
+  }
+  g_cache[g_cached++] = CachedAddress{ctx, fresh};
+  *out = fresh;
   return cudaSuccess;
 }
 
@@ -51,9 +89,9 @@ extern "C" moe_status_t moe_align_permute_noalloc(const moe_problem_t* p, const 
                                                   int32_t* counts, int32_t* offsets, int32_t* perm,
                                                   int32_t* inv, void* x_perm,
                                                   moe_stream_t stream) {
-  // Same problem checks as every other entry point (moe_scratch_size returns 0
-  // for an invalid problem).
-  if (p == nullptr || moe_scratch_size(p) == 0) return MOE_ERR_INVALID_ARG;
+  // Same problem checks and statuses as every other entry point.
+  const moe_status_t st = moe::validate_problem(p);
+  if (st != MOE_OK) return st;
   const long long S = static_cast<long long>(p->T) * p->top_k;
   const long long need = static_cast<long long>(moe::align_blocks(static_cast<int>(S))) * p->E * 4;
   if (need > static_cast<long long>(kNoAllocScratchBytes)) return MOE_ERR_UNSUPPORTED;

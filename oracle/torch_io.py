@@ -1,8 +1,13 @@
-"""Moves synthetic torch inputs into the numpy arrays the oracle reads."""
+"""Moves synthetic torch inputs into the numpy arrays the oracle reads.
+
+TEST INFRASTRUCTURE ONLY, like the rest of this package: argument marshalling
+for tests/, __graft_entry__.smoke() and the CPU-baseline leg of bench.py.  It is
+not imported by the package's __init__, so the oracle itself needs no torch.
+"""
 import numpy as np
 import torch
 
-from oracle import Problem, ExpertWeights
+from .moe_ref import Problem, ExpertWeights
 
 
 def problem_for(shape, T) -> Problem:

@@ -10,7 +10,7 @@ import torch
 import mixture_experts_layer_gate_gb300 as moe
 import oracle
 from synth import make_tokens, make_weights
-from tests.oracle_io import np_of, oracle_inputs
+from oracle.torch_io import np_of, oracle_inputs
 
 TOL = {"bf16": 1e-2, "fp8": 3e-2, "int4": 4e-2, "int8": 2e-2}
 

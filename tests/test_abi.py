@@ -203,17 +203,37 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_plans_with_two_mma_issuers(lib, monkeypatch, pair):
+@pytest.mark.parametrize("pair", [0, 1])
+def test_plans_with_two_mma_issuers(lib, pair):
     # forced, on one CTA or CTA pairs: every int4 / int8 GEMM takes two issuing
     # threads (bf16 / fp8 keep one); the invariants above still hold
-    monkeypatch.setenv("MOE_DUAL", "1")
-    monkeypatch.setenv("MOE_PAIR", pair)
     seen = 0
-    for shape, p in _all_problems():
-        pl = _check_plan(shape, moe.get_plan(p, num_sms=152))
-        for side in ("up", "down"):
-            two = shape.wdtype in ("int4", "int8")
-            assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
-            seen += two and getattr(pl, f"pair_{side}") == int(pair)
+    with moe.tuning(dual=1, pair=pair):
+        for shape, p in _all_problems():
+            pl = _check_plan(shape, moe.get_plan(p, num_sms=152))
+            for side in ("up", "down"):
+                two = shape.wdtype in ("int4", "int8")
+                assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
+                seen += two and getattr(pl, f"pair_{side}") == int(pair)
     assert seen > 0
+
+
+def test_tuning_overrides_are_explicit_and_validated(lib, monkeypatch):
+    p = moe.problem(37, 1024, 256, 64, 8, scoring="sigmoid", n_group=8, topk_group=4, wdtype="int4")
+    base = moe.get_plan(p, num_sms=152)
+    # the environment is never read
+    for k in ("MOE_PAIR", "MOE_DUAL", "MOE_BN_MAX", "MOE_STAGES", "MOE_SPLITS", "MOE_SLOT_KB"):
+        monkeypatch.setenv(k, "1" if k in ("MOE_PAIR", "MOE_DUAL") else "2")
+    again = moe.get_plan(p, num_sms=152)
+    assert bytes(again) == bytes(base)
+    with moe.tuning(pair=1 - base.pair_up, stages=2):
+        forced = moe.get_plan(p, num_sms=152)
+        assert forced.pair_up == 1 - base.pair_up and forced.stages_up == 2
+    assert bytes(moe.get_plan(p, num_sms=152)) == bytes(base)  # restored on exit
+    for bad in (dict(bn_max=24), dict(bn_max=512), dict(slot_kb=3), dict(pair=2), dict(splits=17),
+                dict(stages=1), dict(conv_groups=4)):
+        with pytest.raises(moe.MoEError):
+            moe.set_tuning(**bad)
+        assert bytes(moe.get_plan(p, num_sms=152)) == bytes(base)  # a rejected call changes nothing
+    with pytest.raises(ValueError):
+        moe.set_tuning(no_such_knob=1)

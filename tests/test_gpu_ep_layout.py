@@ -14,7 +14,7 @@ import mixture_experts_layer_gate_gb300 as moe
 import oracle
 from synth import SHAPES, make_weights, shrink
 from tests.gpu_cases import TOL
-from tests.oracle_io import LazyExperts, bf16_bits, np_of, problem_for
+from oracle.torch_io import LazyExperts, bf16_bits, np_of, problem_for
 
 pytestmark = pytest.mark.gpu
 

@@ -210,77 +210,74 @@ def test_full_size_sampled(dev, name, T):
 
 
 # Kernel variants the planner does not pick for these shapes, forced through the
-# library's tuning knobs (read from the environment at every plan): the single-CTA
+# library's planner overrides (moe_set_tuning): the single-CTA
 # bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's pair / non-pair,
 # one / two MMA-issuer, two-k-block-slot, three-converter-group, k-split /
 # alternating-stage and per-64/16-row token box (no full box) modes.
 @pytest.mark.parametrize("name,knobs", [
-    ("mixtral", {"MOE_PAIR": "0"}),
-    ("qwen2", {"MOE_PAIR": "0"}),
-    ("dsv3", {"MOE_PAIR": "0"}),
-    ("dsv3", {"MOE_PAIR": "1"}),
-    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
-    ("dsv3", {"MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
-    ("dsv3", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
-    ("dsv3_awq", {"MOE_PAIR": "0"}),
-    ("mixtral_w8", {"MOE_PAIR": "0"}),
-    ("qwen2_dyn", {"MOE_PAIR": "0"}),
-    ("dsv3", {"MOE_KSPLIT": "1"}),
-    ("mixtral_w8", {"MOE_KSPLIT": "0", "MOE_PAIR": "0"}),
-    ("mixtral_w8", {"MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
-    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_SLOT_KB": "2", "MOE_DUAL": "0"}),
-    ("dsv3_awq", {"MOE_SLOT_KB": "2", "MOE_CONV_GROUPS": "3", "MOE_DUAL": "0"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "64"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "32", "MOE_KSPLIT": "1"}),
-    ("dsv3_awq", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "48"}),
-    ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "64"}),
-    ("mixtral_w8_zp", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "32"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "0"}),
-    ("dsv3", {"MOE_FULL_BOX": "0", "MOE_DUAL": "0"}),
-    ("dsv3_awq", {"MOE_FULL_BOX": "0"}),
-    ("mixtral_w8", {"MOE_PAIR": "0", "MOE_DUAL": "0", "MOE_FULL_BOX": "0"}),
-    ("dsv3", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
-    ("dsv3", {"MOE_PAIR": "1", "MOE_DUAL": "0"}),
-    ("dsv3_awq", {"MOE_PAIR": "1", "MOE_DUAL": "1", "MOE_KSPLIT": "1"}),
-    ("dsv3", {"MOE_PAIR": "0", "MOE_DUAL": "1", "MOE_BN_MAX": "128"}),
-    ("mixtral_w8", {"MOE_PAIR": "1", "MOE_DUAL": "1"}),
-    ("mixtral_w8_zp", {"MOE_PAIR": "1", "MOE_DUAL": "1", "MOE_BN_MAX": "128"}),
+    ("mixtral", {"pair": 0}),
+    ("qwen2", {"pair": 0}),
+    ("dsv3", {"pair": 0}),
+    ("dsv3", {"pair": 1}),
+    ("dsv3", {"slot_kb": 2, "dual": 0}),
+    ("dsv3", {"conv_groups": 3, "dual": 0}),
+    ("dsv3", {"slot_kb": 2, "conv_groups": 3, "dual": 0}),
+    ("dsv3", {"pair": 0, "slot_kb": 2, "dual": 0}),
+    ("dsv3_awq", {"pair": 0}),
+    ("mixtral_w8", {"pair": 0}),
+    ("qwen2_dyn", {"pair": 0}),
+    ("dsv3", {"ksplit": 1}),
+    ("mixtral_w8", {"ksplit": 0, "pair": 0}),
+    ("mixtral_w8", {"slot_kb": 2, "dual": 0}),
+    ("mixtral_w8_zp", {"pair": 0, "slot_kb": 2, "dual": 0}),
+    ("dsv3_awq", {"slot_kb": 2, "conv_groups": 3, "dual": 0}),
+    ("dsv3", {"pair": 0, "dual": 1}),
+    ("dsv3", {"pair": 0, "dual": 1, "bn_max": 64}),
+    ("dsv3", {"pair": 0, "dual": 1, "bn_max": 32, "ksplit": 1}),
+    ("dsv3_awq", {"pair": 0, "dual": 1, "bn_max": 48}),
+    ("mixtral_w8", {"pair": 0, "dual": 1, "bn_max": 64}),
+    ("mixtral_w8_zp", {"pair": 0, "dual": 1, "bn_max": 32}),
+    ("dsv3", {"pair": 0, "dual": 0}),
+    ("dsv3", {"full_box": 0, "dual": 0}),
+    ("dsv3_awq", {"full_box": 0}),
+    ("mixtral_w8", {"pair": 0, "dual": 0, "full_box": 0}),
+    ("dsv3", {"pair": 1, "dual": 1}),
+    ("dsv3", {"pair": 1, "dual": 0}),
+    ("dsv3_awq", {"pair": 1, "dual": 1, "ksplit": 1}),
+    ("dsv3", {"pair": 0, "dual": 1, "bn_max": 128}),
+    ("mixtral_w8", {"pair": 1, "dual": 1}),
+    ("mixtral_w8_zp", {"pair": 1, "dual": 1, "bn_max": 128}),
 ])
-def test_forced_kernel_variants(dev, monkeypatch, name, knobs):
-    for k, v in knobs.items():
-        monkeypatch.setenv(k, v)
+def test_forced_kernel_variants(dev, name, knobs):
     shape = small(name)
-    plan = moe.get_plan(gc.lib_problem(shape, 300))
-    if "MOE_SLOT_KB" in knobs:
-        assert plan.slot_kb_up == int(knobs["MOE_SLOT_KB"])
-    if "MOE_DUAL" in knobs:  # tiles of <= 64 tokens
-        plan = moe.get_plan(gc.lib_problem(shape, 37))
-        want = 2 if knobs["MOE_DUAL"] == "1" else 1
-        assert plan.issuers_up == want and plan.issuers_down == want
-    for T in (37, 300):
-        gc.full_check(shape, T, dev)
+    with moe.tuning(**knobs):
+        plan = moe.get_plan(gc.lib_problem(shape, 300))
+        if "slot_kb" in knobs:
+            assert plan.slot_kb_up == knobs["slot_kb"]
+        if "dual" in knobs:  # tiles of <= 64 tokens
+            plan = moe.get_plan(gc.lib_problem(shape, 37))
+            want = 2 if knobs["dual"] == 1 else 1
+            assert plan.issuers_up == want and plan.issuers_down == want
+        for T in (37, 300):
+            gc.full_check(shape, T, dev)
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-@pytest.mark.parametrize("splits", [None, "3"])
-def test_two_issuers_short_k_ranges(dev, monkeypatch, splits, pair):
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("splits", [None, 3])
+def test_two_issuers_short_k_ranges(dev, splits, pair):
     # k ranges that leave the second MMA-issuing thread (k-blocks 2 and 3 of a
     # stage) without work in a stage (split-K tails of one or two k-blocks) or in
     # a whole unit (the down GEMM's K = 128 is two k-blocks), on one CTA and on
     # CTA pairs (whose arrivals then go to both CTAs)
-    monkeypatch.setenv("MOE_PAIR", pair)
-    monkeypatch.setenv("MOE_DUAL", "1")
-    if splits:
-        monkeypatch.setenv("MOE_SPLITS", splits)
     shape = dataclasses.replace(small("dsv3"), name="dsv3_short_k", I=128)
-    for T in (1, 37):
-        plan = moe.get_plan(gc.lib_problem(shape, T))
-        assert plan.issuers_up == 2 and plan.issuers_down == 2
-        if splits:
-            assert plan.splits_up == 3
-        gc.full_check(shape, T, dev)
+    knobs = dict(pair=pair, dual=1) if splits is None else dict(pair=pair, dual=1, splits=splits)
+    with moe.tuning(**knobs):
+        for T in (1, 37):
+            plan = moe.get_plan(gc.lib_problem(shape, T))
+            assert plan.issuers_up == 2 and plan.issuers_down == 2
+            if splits:
+                assert plan.splits_up == 3
+            gc.full_check(shape, T, dev)
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 64), ("tiny", 2000), ("qwen2_dyn", 37)])

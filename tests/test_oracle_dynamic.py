@@ -15,7 +15,7 @@ import torch
 import oracle
 from oracle import Problem
 from synth import SHAPES, make_weights, make_tokens, shrink
-from tests.oracle_io import oracle_inputs
+from oracle.torch_io import oracle_inputs
 
 
 def test_encode_bf16_matches_torch_cast_on_float32_values():

@@ -16,7 +16,7 @@ import torch
 import oracle
 from oracle import Problem, ExpertWeights
 from synth import SHAPES, make_weights, make_tokens, shrink
-from tests.oracle_io import oracle_inputs, problem_for, np_of, bf16_bits
+from oracle.torch_io import oracle_inputs, problem_for, np_of, bf16_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 

@@ -64,6 +64,42 @@ def test_noalloc_align_permute_matches_workspace_entry_point(name):
             assert torch.equal(got[key], ref[key]), (name, T, key)
 
 
+def test_noalloc_empty_batch_and_exactly_full_array():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda:0")
+    moe.load()
+    # T = 0: nothing to sort; counts and offsets come back all zero
+    shape = shrink(SHAPES["tiny"], H=128, I=128)
+    p = _problem(shape, 0)
+    got = _outputs(shape, 0, dev)
+    none = torch.empty(0, dtype=torch.int32, device=dev)
+    moe.align_permute_noalloc(p, none, none, None, got["counts"], got["offsets"], none, none, none)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(got["counts"]).item() == 0
+    assert torch.count_nonzero(got["offsets"]).item() == 0
+    # the largest accepted problem: ceil(T*k / 1024) * E == 65536 histogram
+    # entries exactly fills the 256 KiB array (E = 1024, T*k = 65536)
+    shape = dataclasses.replace(SHAPES["tiny"], name="fill", H=128, I=128, E=1024, top_k=2)
+    T = 32768
+    tok = make_tokens(shape, T, dev, 2)
+    p = _problem(shape, T)
+    ids = torch.empty((T, 2), dtype=torch.int32, device=dev)
+    w = torch.empty((T, 2), dtype=torch.float32, device=dev)
+    moe.gate_topk(p, tok.logits, tok.bias, ids, w)
+    ref = _outputs(shape, T, dev)
+    ws = moe.alloc_workspace(p, dev, full=False)
+    moe.align_permute(p, ids, tok.x, None, ref["counts"], ref["offsets"], ref["perm"], ref["inv"],
+                      ref["x_perm"], ws)
+    got = _outputs(shape, T, dev)
+    moe.align_permute_noalloc(p, ids, tok.x, None, got["counts"], got["offsets"], got["perm"], got["inv"],
+                              got["x_perm"])
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == 0
+    for key in ref:
+        assert torch.equal(got[key], ref[key]), ("fill", key)
+
+
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -75,3 +111,12 @@ def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
     with pytest.raises(moe.MoEError) as ei:
         moe.align_permute_noalloc(p, x, x, None, x, x, x, x, x)
     assert ei.value.status == 2
+    # a problem beyond the library's own limits gets the status moe_align_permute gives
+    big = moe.problem(70000, 256, 256, 8, 2)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.align_permute_noalloc(big, x, x, None, x, x, x, x, x)
+    assert ei.value.status == 2
+    bad = moe.problem(8, 100, 256, 8, 2)  # H % 128 != 0
+    with pytest.raises(moe.MoEError) as ei:
+        moe.align_permute_noalloc(bad, x, x, None, x, x, x, x, x)
+    assert ei.value.status == 1
