@@ -295,49 +295,10 @@ def run_ours(args):
     adt = torch.uint8 if shape.wdtype == "fp8" else torch.bfloat16
     x_perm = torch.empty((S, shape.H), dtype=adt, device=dev)
     act = torch.empty((S, shape.I), dtype=adt, device=dev)
-    moe.align_permute(p, ids, tok.x, tok.a1_scale, counts_t, offsets, perm, inv, x_perm, ws, stream.cuda_stream)
-    for _ in range(3):
-        moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
-    up_flops = 2.0 * S * (2 * shape.I) * shape.H
-    gbytes = (3.0 if shape.zero_point else 2.0) / shape.group_size  # scale (+ zero point) per group
-    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0, "int4": 0.5 + gbytes, "int8": 1.0 + gbytes}[shape.wdtype]
     abytes = 1 if shape.wdtype == "fp8" else 2
-    up_bytes = touched * (2 * shape.I * shape.H * wbytes_per_elem) + S * shape.H * abytes + S * shape.I * abytes
-    reps = max(5, args.steps)
-    kflush = (flush or l2_flusher(torch, dev, l2)) if up_bytes < 2 * l2 else None
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    with torch.cuda.stream(stream):
-        for e0, e1 in kev:
-            if kflush is not None:
-                kflush()
-            e0.record(stream)
-            moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
-            e1.record(stream)
-    stream.synchronize()
-    if kflush is not None:
-        k_ms = sum(e0.elapsed_time(e1) for e0, e1 in kev) / reps
-    else:
-        k_ms = kev[0][0].elapsed_time(kev[-1][1]) / reps
-    tensor_peak = dtype_peak
-    t_tensor = up_flops / (tensor_peak * 1e12)
-    t_hbm = up_bytes / (hbm * 1e9)
-    if t_tensor >= t_hbm:
-        roof = {"bound": "tensor", "achieved": up_flops / (k_ms / 1e3) / 1e12, "peak": tensor_peak,
-                "unit": "TFLOP/s",
-                "peak_kind": ("fp8 dense = 2x bf16 dense burst, " if shape.wdtype == "fp8" else "bf16 dense burst, ")
-                + peak_src}
-    else:
-        roof = {"bound": "hbm", "achieved": up_bytes / (k_ms / 1e3) / 1e9, "peak": hbm,
-                "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = (f"grouped_gemm_wna16_kernel<{shape.wdtype}>" if shape.wdtype in ("int4", "int8")
-                      else f"grouped_gemm_{'pair_' if plan.pair_up else ''}kernel<{shape.wdtype}>") + \
-        (" (clusters of 2 CTAs)" if plan.pair_up else "") + \
-        (" (2 MMA-issuing threads)" if plan.issuers_up == 2 else "") + " (gate_up + SwiGLU)" + \
-        (" + absmax + e4m3 pass (dynamic scales)" if shape.act_scale == "dynamic" else "")
-    roof["kernel_ms"] = k_ms
-    roof["l2_flushed"] = kflush is not None
-    roof["traffic"] = _traffic_for("grouped_gemm_up", args.config, T)
+    roof = dominant_kernel(moe, torch, shape, args.config, T, p, wts, tok, ids, touched, ws, stream, dev,
+                           max(5, args.steps), flush, l2, hbm, bf16_peak, peak_src, plan,
+                           (counts_t, offsets, perm, inv, x_perm, act))
 
     # per-stage times: each entry point on its own, CUDA events between them on the
     # stream, no graph (L2 flushed before each rep where the step is flushed)
@@ -422,8 +383,17 @@ def run_ours(args):
     e2e_ok = bool(torch.equal(o_h[(2 + args.steps - 1) & 1], out.cpu()))  # same inputs -> same output
 
     sweep = []
+    sweeps = {}
     if args.sweep and rank == 0:
-        sweep = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+        with ClockSampler(local) as sclk:
+            sclk.mark(True)
+            sweep = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+            sclk.mark(False)
+        sweeps[args.config] = {"workload": WORKLOADS.get(args.config, args.config), "rows": sweep,
+                               "clocks": sclk.summary(), "dominant_kernel_T4096": roof if T == 4096 else None}
+        for cfg in args.sweep_configs:
+            if cfg != args.config:
+                sweeps[cfg] = sweep_config(moe, torch, cfg, dev, stream, local, hbm, bf16_peak, peak_src)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -459,12 +429,72 @@ def run_ours(args):
     }
     if sweep:
         line["sweep"] = sweep
+    if sweeps:
+        line["sweeps"] = sweeps
+        line["sweeps_note"] = ("per workload: layer tokens/s and roofline fraction for T = 1..4096 (CUDA graph, "
+                               "20 reps per T, L2 flushed before each rep when its bytes could stay in L2), "
+                               "nvidia-smi clocks sampled during that workload's sweep, and its gate_up GEMM "
+                               "timed alone at T = 4096 against its bound")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, w, tok, args.cpu_sample)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def dominant_kernel(moe, torch, shape, config, T, p, wts, tok, ids, touched, ws, stream, dev, reps, flush, l2,
+                    hbm, bf16_peak, peak_src, plan, bufs):
+    """The gate_up grouped GEMM (the dominant kernel) timed alone on its stream
+    with CUDA events: achieved rate against its roofline bound, and the DRAM
+    traffic of a committed ncu summary taken on the current GEMM source."""
+    counts_t, offsets, perm, inv, x_perm, act = bufs
+    S = T * shape.top_k
+    moe.align_permute(p, ids, tok.x, tok.a1_scale, counts_t, offsets, perm, inv, x_perm, ws, stream.cuda_stream)
+    for _ in range(3):
+        moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
+    up_flops = 2.0 * S * (2 * shape.I) * shape.H
+    gbytes = (3.0 if shape.zero_point else 2.0) / shape.group_size  # scale (+ zero point) per group
+    wbytes_per_elem = {"bf16": 2.0, "fp8": 1.0, "int4": 0.5 + gbytes, "int8": 1.0 + gbytes}[shape.wdtype]
+    abytes = 1 if shape.wdtype == "fp8" else 2
+    up_bytes = touched * (2 * shape.I * shape.H * wbytes_per_elem) + S * shape.H * abytes + S * shape.I * abytes
+    kflush = (flush or l2_flusher(torch, dev, l2)) if up_bytes < 2 * l2 else None
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in kev:
+            if kflush is not None:
+                kflush()
+            e0.record(stream)
+            moe.grouped_gemm_swiglu(p, wts, x_perm, offsets, act, ws, stream.cuda_stream)
+            e1.record(stream)
+    stream.synchronize()
+    if kflush is not None:
+        k_ms = sum(e0.elapsed_time(e1) for e0, e1 in kev) / reps
+    else:
+        k_ms = kev[0][0].elapsed_time(kev[-1][1]) / reps
+    dtype_peak = bf16_peak * (2.0 if shape.wdtype == "fp8" else 1.0)
+    tensor_peak = dtype_peak
+    t_tensor = up_flops / (tensor_peak * 1e12)
+    t_hbm = up_bytes / (hbm * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": up_flops / (k_ms / 1e3) / 1e12, "peak": tensor_peak,
+                "unit": "TFLOP/s",
+                "peak_kind": ("fp8 dense = 2x bf16 dense burst, " if shape.wdtype == "fp8" else "bf16 dense burst, ")
+                + peak_src}
+    else:
+        roof = {"bound": "hbm", "achieved": up_bytes / (k_ms / 1e3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "peak_kind": f"HBM copy, {peak_src}"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = (f"grouped_gemm_wna16_kernel<{shape.wdtype}>" if shape.wdtype in ("int4", "int8")
+                      else f"grouped_gemm_{'pair_' if plan.pair_up else ''}kernel<{shape.wdtype}>") + \
+        (" (clusters of 2 CTAs)" if plan.pair_up else "") + \
+        (" (2 MMA-issuing threads)" if plan.issuers_up == 2 else "") + " (gate_up + SwiGLU)" + \
+        (" + absmax + e4m3 pass (dynamic scales)" if shape.act_scale == "dynamic" else "")
+    roof["kernel_ms"] = k_ms
+    roof["algorithmic"] = {"flops": up_flops, "bytes": up_bytes}
+    roof["l2_flushed"] = kflush is not None
+    roof["traffic"] = _traffic_for("grouped_gemm_up", config, T)
+    return roof
 
 
 def l2_bytes(torch, dev):
@@ -481,6 +511,47 @@ def l2_flusher(torch, dev, l2):
         state["v"] = (state["v"] + 1) & 0x7F
         buf.fill_(state["v"])
     return flush
+
+
+def sweep_config(moe, torch, cfg, dev, stream, local, hbm, bf16_peak, peak_src):
+    """One more workload's batch sweep in the same process: its own weights
+    (seed 0), its clocks, and its dominant kernel at T = 4096."""
+    from synth import SHAPES, make_tokens, make_weights
+    shape = SHAPES[cfg]
+    w = make_weights(shape, dev, seed=0)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        clk.mark(True)
+        rows = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+        clk.mark(False)
+    T = 4096
+    tok = make_tokens(shape, T, dev, seed=0)
+    p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
+                    renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
+                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                    act_scale=shape.act_scale)
+    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale, w.w13_zero, w.w2_zero)
+    ws = moe.alloc_workspace(p, dev)
+    ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
+    tw = torch.empty((T, shape.top_k), dtype=torch.float32, device=dev)
+    moe.gate_topk(p, tok.logits, tok.bias, ids, tw, stream.cuda_stream)
+    stream.synchronize()
+    touched = int(torch.unique(ids).numel())
+    S = T * shape.top_k
+    adt = torch.uint8 if shape.wdtype == "fp8" else torch.bfloat16
+    bufs = (torch.empty(shape.E, dtype=torch.int32, device=dev), torch.empty(shape.E + 1, dtype=torch.int32, device=dev),
+            torch.empty(S, dtype=torch.int32, device=dev), torch.empty(S, dtype=torch.int32, device=dev),
+            torch.empty((S, shape.H), dtype=adt, device=dev), torch.empty((S, shape.I), dtype=adt, device=dev))
+    l2 = l2_bytes(torch, dev)
+    roof = dominant_kernel(moe, torch, shape, cfg, T, p, wts, tok, ids, touched, ws, stream, dev, 10, None, l2,
+                           hbm, bf16_peak, peak_src, moe.get_plan(p), bufs)
+    if moe.get_device_error(ws, stream.cuda_stream) != 0:
+        raise RuntimeError(f"device error in the {cfg} sweep")
+    out = {"workload": WORKLOADS.get(cfg, cfg), "rows": rows, "clocks": clk.summary(),
+           "dominant_kernel_T4096": roof}
+    del w, wts, ws, bufs, tok
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak):
@@ -695,6 +766,9 @@ def main():
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling small cases)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--sweep-configs", default=None,
+                    help="comma-separated further workloads to sweep in the same run (default with the "
+                         "Mixtral headline: qwen2,dsv3,scout,tiny; else none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=4096)
     ap.add_argument("--ref-sample", type=int, default=16)
@@ -703,6 +777,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep_configs is None:
+        args.sweep_configs = "qwen2,dsv3,scout,tiny" if args.config == CONFIG_NAME else ""
+    args.sweep_configs = [c for c in args.sweep_configs.split(",") if c]
     if args.measure_tensor_peaks:
         measure_tensor_peaks()
         return

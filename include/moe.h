@@ -150,7 +150,10 @@ size_t moe_workspace_size(const moe_problem_t* p);
  * bias is NULL); with n_group > 0 the experts form n_group contiguous groups,
  * each scored by the sum of its two largest keys, and only the topk_group best
  * groups (ties to the lower group) compete; weight = s, renormalised if asked,
- * times routed_scaling_factor.  NaN logits rank lowest. */
+ * times routed_scaling_factor.  A NaN logit is read as -inf: softmax
+ * probability 0 (left out of the normalising sum), sigmoid score 0, and the
+ * key of a -inf logit (with a bias, the bias alone), so it ranks after every
+ * finite logit of equal bias.  Each softmax row needs one finite logit. */
 moe_status_t moe_gate_topk(const moe_problem_t* p, const float* logits, const float* bias,
                            int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 

@@ -89,20 +89,33 @@ def _topk_desc_lower_index(keys: np.ndarray, k: int) -> np.ndarray:
     return order[:, :k]
 
 
-def softmax_fp64(logits: np.ndarray) -> np.ndarray:
+def logits_fp64(logits: np.ndarray) -> np.ndarray:
+    """Router logits as float64, a NaN read as -infinity.
+
+    The pages say nothing about NaN logits.  Reading: a NaN logit is an expert
+    the router scores lowest, i.e. -inf: softmax probability 0 (and left out of
+    the normalising sum), sigmoid score 0, selection key of a -inf logit (with
+    a bias the key is then the bias alone).  Rows must keep at least one finite
+    logit for the softmax to be defined."""
     l = np.asarray(logits, dtype=np.float64)
+    return np.where(np.isnan(l), -np.inf, l)
+
+
+def softmax_fp64(logits: np.ndarray) -> np.ndarray:
+    l = logits_fp64(logits)
     m = l.max(axis=1, keepdims=True)
     z = np.exp(l - m)
     return z / z.sum(axis=1, keepdims=True)
 
 
 def sigmoid_fp64(logits: np.ndarray) -> np.ndarray:
-    l = np.asarray(logits, dtype=np.float64)
-    return 1.0 / (1.0 + np.exp(-l))
+    l = logits_fp64(logits)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-l))
 
 
 def _keys(p: Problem, logits: np.ndarray, bias):
-    l = np.asarray(logits, dtype=np.float64)
+    l = logits_fp64(logits)
     if p.scoring == "softmax":
         return l, True
     if p.n_group == 0 and bias is None:

@@ -124,10 +124,26 @@ class _NoWeights:
     w13 = w2 = w13_scale = w2_scale = w13_zero = w2_zero = None
 
 
-def full_check(shape, T, device, seed=0, check_stages=True):
+def plant_nan_logits(tok, frac, seed):
+    """Sets a seeded fraction of the router logits to NaN, keeping one finite
+    logit per row (column t mod E) so every softmax row stays defined; a few
+    rows lose all but that one, so NaN experts get selected there."""
+    T, E = tok.logits.shape
+    g = torch.Generator(device="cpu")
+    g.manual_seed(1234 + seed)
+    mask = torch.rand((T, E), generator=g) < frac
+    mask[: max(1, T // 16)] = True
+    mask[torch.arange(T), torch.arange(T) % E] = False
+    tok.logits[mask.to(tok.logits.device)] = float("nan")
+    return int(mask.sum())
+
+
+def full_check(shape, T, device, seed=0, check_stages=True, nan_logits=0.0):
     """Whole-layer parity on a size the oracle computes completely."""
     w = make_weights(shape, device, seed)
     tok = make_tokens(shape, T, device, seed)
+    if nan_logits:
+        plant_nan_logits(tok, nan_logits, seed)
     g = run_stages(shape, T, w, tok, device)
     assert torch.equal(g.out, g.out_forward), "moe_forward differs from the staged calls"
     ids_g, n_mism, n_amb = check_gate(shape, T, tok, g)

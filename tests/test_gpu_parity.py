@@ -56,6 +56,15 @@ def test_small_shapes_all_stages(dev, name, T):
     gc.full_check(small(name), T, dev)
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen2", "dsv3", "scout"])
+@pytest.mark.parametrize("T", [5, 300])
+def test_nan_logits(dev, name, T):
+    # NaN router logits read as -inf on both sides: softmax probability 0, sigmoid
+    # score 0 (with a bias the key is the bias), ranked after every finite key;
+    # ids bit-exact, weights and outputs within tolerance
+    gc.full_check(small(name), T, dev, nan_logits=0.2)
+
+
 @pytest.mark.parametrize("name", ["mixtral", "scout"])
 def test_multiple_token_tiles_per_expert(dev, name):
     # about 250 rows per expert (mixtral) / 500 for expert 0 (scout): more than one 256-row tile
@@ -194,6 +203,14 @@ FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), 
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
               ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("scout_tp8", 32), ("scout_tp8", 4096)]
+
+
+def test_dynamic_scales_full_size_multi_tile_exact(dev):
+    # Qwen2-57B-A14B at full size with 700 tokens (5600 rows, several token
+    # tiles per expert): the oracle computes every row, so a2 is compared to
+    # 2^-7 and the outputs with the second quantisation applied
+    r = gc.full_check(SHAPES["qwen2_dyn"], 700, dev)
+    print(f"qwen2_dyn T=700: err={r['err']:.3e}")
 
 
 def test_dynamic_scales_full_size_exact(dev):

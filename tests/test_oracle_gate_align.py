@@ -231,3 +231,76 @@ def test_align_empty():
     counts, offsets, perm, inv = oracle.align(np.zeros((0, 2), dtype=np.int32), 4)
     assert counts.tolist() == [0, 0, 0, 0] and offsets.tolist() == [0] * 5
     assert perm.size == 0 and inv.size == 0
+
+
+# ------------------------------------------------------------------ NaN logits
+# Reading: a NaN logit is read as -inf (the pages are silent on NaN).  The pins
+# below never feed a NaN to a library routine: they drop the NaN experts and
+# solve the remaining problem by brute force or scipy.
+
+@pytest.mark.parametrize("k,renorm", [(1, True), (2, True), (3, False)])
+def test_nan_softmax_logits_equal_dropping_those_experts(k, renorm):
+    rng = np.random.default_rng(40 + k)
+    E = 8
+    l = rng.standard_normal((120, E)).astype(np.float32)
+    nan = rng.random((120, E)) < 0.25
+    nan[:, 5] = False  # every row keeps a finite logit
+    nan[:10, :] = True  # rows with fewer finite experts than k: NaN experts are then selected
+    nan[:10, 5] = False
+    l[nan] = np.nan
+    ids, w, _ = oracle.gate(_prob(E, k, renormalize=renorm), l)
+    for t in range(l.shape[0]):
+        fin = np.nonzero(~nan[t])[0]
+        pf = scipy.special.softmax(l[t, fin].astype(np.float64))
+        if fin.size >= k:
+            # the best k-subset of the finite experts, in descending logit order
+            best, bs = None, -np.inf
+            for c in itertools.combinations(fin.tolist(), k):
+                s = float(np.sum(l[t, list(c)].astype(np.float64)))
+                if s > bs:
+                    best, bs = c, s
+            assert set(ids[t].tolist()) == set(best), t
+            sel = pf[np.searchsorted(fin, ids[t])]
+            want = sel / sel.sum() if renorm else sel
+            assert np.allclose(w[t], want, rtol=1e-14), t
+        else:
+            # all finite experts first (descending), then the NaN experts by index, weight 0
+            order = fin[np.argsort(-l[t, fin].astype(np.float64), kind="stable")]
+            rest = [e for e in range(E) if nan[t, e]][: k - fin.size]
+            assert ids[t].tolist() == order.tolist() + rest, t
+            assert np.all(w[t, fin.size:] == 0.0)
+            want = pf[np.argsort(-l[t, fin].astype(np.float64), kind="stable")]
+            assert np.allclose(w[t, :fin.size], want / want.sum() if renorm else want, rtol=1e-14)
+
+
+def test_nan_sigmoid_grouped_key_is_the_bias():
+    # E = 8, 2 groups of 4 keep 1, k = 2.  Expert 6's logit is NaN: its score is 0
+    # and its key is bias[6] = 0.95.  Group 1 = {4..7} has keys
+    # sigmoid(0) + 0 = 0.5, sigmoid(-1) = 0.2689, 0.95, sigmoid(-2) = 0.1192 -> score
+    # 0.95 + 0.5 = 1.45; group 0 = {0..3}: sigmoid(1) = 0.7311, sigmoid(0.5) = 0.6225,
+    # sigmoid(0) = 0.5, sigmoid(-0.5) = 0.3775 -> 1.3536.  Group 1 wins; its best
+    # two keys are expert 6 (0.95) then expert 4 (0.5); weights 0 and sigmoid(0),
+    # renormalised: 0 and 1, times 2.5.
+    l = np.array([[1.0, 0.5, 0.0, -0.5, 0.0, -1.0, np.nan, -2.0]], dtype=np.float32)
+    bias = np.array([0, 0, 0, 0, 0, 0, 0.95, 0], dtype=np.float32)
+    p = _prob(8, 2, scoring="sigmoid", renormalize=True, n_group=2, topk_group=1, routed_scaling_factor=2.5)
+    ids, w, _ = oracle.gate(p, l, bias)
+    assert ids[0].tolist() == [6, 4]
+    assert w[0].tolist() == [0.0, 2.5]
+
+
+def test_nan_sigmoid_raw_keys_rank_last():
+    # no bias, no groups (the Llama-4-Scout gate): a NaN expert is chosen only
+    # after every finite one; the weight is sigmoid of the chosen logit
+    rng = np.random.default_rng(50)
+    l = rng.standard_normal((80, 16)).astype(np.float32)
+    nan = rng.random((80, 16)) < 0.3
+    nan[:, 0] = False
+    l[nan] = np.nan
+    p = _prob(16, 1, scoring="sigmoid", renormalize=False)
+    ids, w, _ = oracle.gate(p, l)
+    for t in range(80):
+        fin = np.nonzero(~nan[t])[0]
+        best = fin[np.argmax(l[t, fin])]
+        assert ids[t, 0] == best
+        assert w[t, 0] == pytest.approx(scipy.special.expit(float(l[t, best])), rel=1e-15)

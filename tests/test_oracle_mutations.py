@@ -115,6 +115,11 @@ def _scale_of_first_row(values):
     return _ORIG["dynamic_scale"](v[:1] if v.ndim > 1 else v)
 
 
+def _nan_logits_rank_first(logits):
+    l = np.asarray(logits, dtype=np.float64)
+    return np.where(np.isnan(l), np.inf, l)
+
+
 _ORIG = {name: getattr(moe_ref, name, None) or getattr(codecs, name)
          for name in ("gate_weights", "align", "reduce", "encode_bf16", "encode_e4m3", "dynamic_scale")}
 
@@ -146,6 +151,10 @@ MUTATIONS = {
         "encode_bf16", _bf16_through_float32, [t_dynamic.test_encode_bf16_rounds_once_from_the_exact_value]),
     "e4m3 rounded toward zero": (
         "encode_e4m3", _e4m3_toward_zero, [t_codecs.test_e4m3_encode_matches_torch_cast_in_range]),
+    "NaN logits ranked first instead of last": (
+        "logits_fp64", _nan_logits_rank_first,
+        [lambda: t_gate.test_nan_softmax_logits_equal_dropping_those_experts(2, True),
+         t_gate.test_nan_sigmoid_grouped_key_is_the_bias, t_gate.test_nan_sigmoid_raw_keys_rank_last]),
     "dynamic scale over one row instead of the tensor": (
         "dynamic_scale", _scale_of_first_row, [t_dynamic.test_dynamic_forward_matches_dense_bruteforce]),
 }
