@@ -204,7 +204,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   g.bn_max = plan_bn_max(p);
   const moe_tuning_t tu = current_tuning();
   const int bn_env = knob(tu.bn_max, 0);
-  if (bn_env >= 16 && bn_env <= (converts(wk) ? 128 : 256) && bn_env % 16 == 0) g.bn_max = bn_env;
+  if (bn_env >= 16 && bn_env <= 256 && bn_env % 16 == 0) g.bn_max = bn_env;
   g.FB = up ? p.I / 64 : p.H / 128;
   const int K = up ? p.H : p.I;
   g.KB = K / (wk == kW_FP8 ? 128 : 64);
@@ -236,6 +236,9 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     g.pair = 1;
     g.bn_max = std::max(32, (g.bn_max + 31) / 32 * 32);
   }
+  // int4 / int8 on one CTA stage all of a tile's token rows for four k-blocks
+  // per ring stage: above 128 rows no second stage fits in shared memory
+  if (converts(wk) && !g.pair) g.bn_max = std::min(g.bn_max, 128);
   g.full_box = knob(tu.full_box, converts(wk) ? 1 : 0) != 0 ? 1 : 0;
   if (converts(wk)) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of
@@ -249,8 +252,15 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // accumulators, two buffers of them where that leaves room for two
     // whole-stage slots (<= 64 columns), else one buffer (<= 128 columns; the
     // epilogue of a unit then no longer overlaps the next unit's MMAs).
+    // Tiles of more than 128 tokens (CTA pairs only): one issuer and one
+    // accumulator of up to 256 columns beside two whole-stage slots.  Each
+    // converted weight tile then serves up to 256 tokens, so an expert with
+    // 129..256 rows is converted once instead of twice, and the MMAs of a
+    // stage (M = 256, N up to 256) outlast its conversion.
     const int dual_env = knob(tu.dual, -1);
-    if (g.acc_cols <= 128 && (dual_env == 1 || (dual_env != 0 && dual_fit))) {
+    if (g.acc_cols > 128) {
+      g.acc_bufs = 1;
+    } else if (dual_env == 1 || (dual_env != 0 && dual_fit)) {
       g.dual = 1;
       g.acc_bufs = g.acc_cols <= 64 ? 2 : 1;
     }
@@ -467,15 +477,15 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   }
   if (!ok) return MOE_ERR_CUDA;
   {
-    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path), three box heights.
+    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path), five box heights.
     const uint64_t K = up ? H : I;
     const bool f8 = wk == kW_FP8;
     uint64_t dims[2] = {K, static_cast<uint64_t>(S)};
     uint64_t str[1] = {K * (f8 ? 1 : 2)};
     const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap* dst[3] = {&maps.b, &maps.b64, &maps.b16};
-    const uint32_t rows[3] = {static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 64u, 16u};
-    for (int i = 0; i < 3; ++i) {
+    CUtensorMap* dst[5] = {&maps.b, &maps.b128, &maps.b64, &maps.b32, &maps.b16};
+    const uint32_t rows[5] = {static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 128u, 64u, 32u, 16u};
+    for (int i = 0; i < 5; ++i) {
       uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
       if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
     }

@@ -102,8 +102,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   const int local = tile - tile_base[lo];
   t.fb = local / nb;
   const int tb = local - t.fb * nb;
-  t.row0 = off[lo] + tb * p.bn_max;
-  t.nvalid = min(p.bn_max, cnt - tb * p.bn_max);
+  // An expert's rows are split into nb tiles of equal height (a multiple of 16,
+  // or of 32 for CTA pairs), not into full tiles plus a short tail: a tail of a
+  // few rows would cost a whole pass of the tensor core over the weight tile
+  // (an MMA instruction takes as long for 16 rows as for 64), balanced tiles
+  // only what the rows need.  (nb - 1) * tsz < cnt, so no tile is empty.
+  const int gran = p.pair ? 32 : 16;
+  const int tsz = ((cnt + nb - 1) / nb + gran - 1) / gran * gran;
+  t.row0 = off[lo] + tb * tsz;
+  t.nvalid = min(tsz, cnt - tb * tsz);
   t.n = (t.nvalid + 15) & ~15;
   t.kb0 = static_cast<int>((static_cast<long long>(t.sp) * p.KB) / p.P);
   t.kb1 = static_cast<int>((static_cast<long long>(t.sp + 1) * p.KB) / p.P);
@@ -202,21 +209,36 @@ __device__ __forceinline__ void ring_advance(int& pos, uint32_t& phase, int& idx
   }
 }
 
+// `n` token rows (a multiple of 16) of one k-block as the fewest boxes of 128,
+// 64, 32 and 16 rows (few, large TMA requests keep the pipe fed).  PAIR: the
+// completion is counted on the barrier at shared::cluster address `bar`,
+// possibly in the peer CTA.
+template <bool PAIR>
+__device__ __forceinline__ void load_rows_split(const GemmMaps& maps, uint32_t dst, uint32_t bar, int kcoord,
+                                                int row0, int n, uint64_t pol) {
+  int r = 0;
+  auto one = [&](const CUtensorMap* m, int h) {
+    if (PAIR)
+      tma_load_2d_pair(dst + static_cast<uint32_t>(r) * 128u, m, bar, kcoord, row0 + r, pol);
+    else
+      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, m, bar, kcoord, row0 + r, pol);
+    r += h;
+  };
+  while (n - r >= 128) one(&maps.b128, 128);
+  if (n - r >= 64) one(&maps.b64, 64);
+  if (n - r >= 32) one(&maps.b32, 32);
+  if (n - r >= 16) one(&maps.b16, 16);
+}
+
 // Token-row loads of one k-block into a B tile: a single box for a full tile,
-// 64- and 16-row boxes for an expert's ragged last tile (few, large TMA
-// requests keep the pipe fed).
+// else the fewest smaller boxes.
 __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const GemmParams& p,
                                                 const Unit& t, uint32_t dst, uint32_t bar, int kcoord,
                                                 uint64_t pol) {
-  if (t.n == p.bn_max || p.full_box) {
+  if (t.n == p.bn_max || p.full_box)
     tma_load_2d_hint(dst, &maps.b, bar, kcoord, t.row0, pol);
-  } else {
-    int r = 0;
-    for (; r + 64 <= t.n; r += 64)
-      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, t.row0 + r, pol);
-    for (; r < t.n; r += 16)
-      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, t.row0 + r, pol);
-  }
+  else
+    load_rows_split<false>(maps, dst, bar, kcoord, t.row0, t.n, pol);
 }
 
 // Weight tile of k-block kb (bf16 / e4m3: 64 / 128 K), or the codes of the
@@ -249,7 +271,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
                                              volatile int* abort_flag, uint8_t* stg_all, int warp, int lane) {
   const int q = warp & 3;  // TMEM lane quarter this warp may read
   uint8_t* stg = stg_all + q * kStgBytesPerWarp;
-  const uint32_t nbuf = DUAL ? static_cast<uint32_t>(p.acc_bufs) : 2u;
+  const uint32_t nbuf = static_cast<uint32_t>(p.acc_bufs);
   uint32_t acc = 0, accph = 0;
   for (int u = first; u < units; u += stride) {
     Unit t = decode_unit(u, tile_base, off, p);
@@ -429,7 +451,9 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
@@ -594,7 +618,9 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
@@ -641,15 +667,10 @@ __global__ void __launch_bounds__(192, 1)
           else
             tma_load_3d_pair(adst, &maps.a, full_cl, kb * kelem, fb * 128, t.e, pol_w);
           const uint32_t bdst = sR + st * L.r_stride;
-          if (half == half_max) {
+          if (half == half_max)
             tma_load_2d_pair(bdst, &maps.b, full_cl, kb * kelem, r0, pol_t);
-          } else {
-            int r = 0;
-            for (; r + 64 <= half; r += 64)
-              tma_load_2d_pair(bdst + static_cast<uint32_t>(r) * 128u, &maps.b64, full_cl, kb * kelem, r0 + r, pol_t);
-            for (; r < half; r += 16)
-              tma_load_2d_pair(bdst + static_cast<uint32_t>(r) * 128u, &maps.b16, full_cl, kb * kelem, r0 + r, pol_t);
-          }
+          else
+            load_rows_split<true>(maps, bdst, full_cl, kb * kelem, r0, half, pol_t);
           if (++st == ns) {
             st = 0;
             ph ^= 1u;
@@ -789,7 +810,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t acc_cols = static_cast<uint32_t>(p.acc_cols);
-  const uint32_t nbuf = DUAL ? static_cast<uint32_t>(p.acc_bufs) : 2u;  // accumulator buffers
+  const uint32_t nbuf = static_cast<uint32_t>(p.acc_bufs);  // accumulator buffers (1 or 2)
   const uint32_t a_col0 = (DUAL ? 2u : 1u) * nbuf * acc_cols;            // TMEM column of converted slot 0
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   const bool leader = (rank == 0);
@@ -825,7 +846,9 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
+    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
+    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
@@ -884,17 +907,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
           if (full) {
             tma_load_3d_hint(stage + kRaw, &maps.b, RFULL(st), 0, t.row0, kbs, pol_t);
           } else {
-            // ragged last tile of an expert: 64- and 16-row boxes per k-block
-            for (int j = 0; j < nk; ++j) {
-              const uint32_t dst = stage + kRaw + j * btile;
-              int r = 0;
-              for (; r + 64 <= t.n; r += 64)
-                tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, RFULL(st),
-                                 (kbs + j) * 64, t.row0 + r, pol_t);
-              for (; r < t.n; r += 16)
-                tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, RFULL(st),
-                                 (kbs + j) * 64, t.row0 + r, pol_t);
-            }
+            // a tile below the full height: the fewest smaller boxes per k-block
+            for (int j = 0; j < nk; ++j)
+              load_rows_split<false>(maps, stage + kRaw + j * btile, RFULL(st), (kbs + j) * 64, t.row0, t.n,
+                                     pol_t);
           }
           issued |= 1u << st;
           issued_par = (issued_par & ~(1u << st)) | (ph << st);

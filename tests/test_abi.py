@@ -167,9 +167,12 @@ def _check_plan(shape, pl):
             # two partials per buffer and one buffer above 64 columns) and the
             # converted-weight slot ring
             sk = getattr(pl, f"slot_kb_{side}")
-            assert bn <= 128 and sk in (2, 4)
+            assert sk in (2, 4) and (bn <= 128 or getattr(pl, f"pair_{side}") == 1)
             acc = (bn + 31) // 32 * 32
-            bufs = 2 if issuers == 1 or acc <= 64 else 1
+            # one buffer above 128 columns (one issuer) or with two issuers above 64
+            bufs = 1 if acc > 128 else (2 if issuers == 1 or acc <= 64 else 1)
+            if acc > 128:
+                assert issuers == 1
             assert 2 <= ast <= 7 and issuers * bufs * acc + 32 * sk * ast <= 512
             # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
             # stage count that is a multiple of g; g = 2 always satisfies both here

@@ -279,6 +279,21 @@ def test_forced_kernel_variants(dev, name, knobs):
             gc.full_check(shape, T, dev)
 
 
+@pytest.mark.parametrize("name,bn", [("dsv3", 256), ("dsv3_awq", 192), ("mixtral_w8", 256),
+                                     ("mixtral_w8_zp", 160)])
+def test_converted_weights_wide_token_tiles(dev, name, bn):
+    # int4 / int8 tiles of more than 128 tokens (CTA pairs, one MMA issuer, one
+    # accumulator of up to 256 columns beside two whole-stage slots): about 250
+    # rows per expert, so tiles run full and ragged
+    shape = small(name)
+    T = 2000 if shape.top_k == 8 and shape.E == 64 else 1000
+    with moe.tuning(bn_max=bn, pair=1):
+        plan = moe.get_plan(gc.lib_problem(shape, T))
+        assert plan.bn_max_up == bn and plan.pair_up == 1 and plan.issuers_up == 1
+        r = gc.full_check(shape, T, dev)
+    assert r["counts"].max() > 128
+
+
 @pytest.mark.parametrize("pair", [0, 1])
 @pytest.mark.parametrize("splits", [None, 3])
 def test_two_issuers_short_k_ranges(dev, splits, pair):

@@ -389,8 +389,6 @@ def _accepted_plans():
                 for ks in (False, True):
                     for dual in (False, True):
                         for nbuf in (1, 2):
-                            if nbuf == 1 and not dual:
-                                continue        # one accumulator buffer only with two issuers
                             if dual and cg != 2:
                                 continue        # the planner keeps two issuers to two groups
                             for ns in range(2, 9):
@@ -421,6 +419,7 @@ def test_protocol_holds_for_every_accepted_plan(chunk):
     Plan(ns=6, na=3, dual=True, nbuf=2),              # int4 decode tile (bn 32), one CTA
     Plan(ns=4, na=2, dual=True, nbuf=1, ctas=2),      # int4 CTA pair, 128-token tile
     Plan(ns=3, na=2, ks=True, ctas=2),                # int8 CTA pair, k-split ring
+    Plan(ns=2, na=2, nbuf=1, ctas=2),                 # int4 CTA pair, 256-token tile, one issuer
     Plan(ns=6, na=5, cg=3, sk=2, ctas=2),             # three groups, two-k-block slots
 ])
 def test_protocol_holds_for_planner_shapes_over_many_schedules(pl):
@@ -584,7 +583,7 @@ def _kernel_converter(pl, units, grp):
 def _kernel_issuer(pl, units, j):
     ev = []
     jb0 = 2 * j if pl.dual else 0
-    nbuf = pl.nbuf if pl.dual else 2
+    nbuf = pl.nbuf
     st = as_ = 0
     ph = aph = acc = accph = 0
     for nkb in units:
@@ -623,7 +622,7 @@ def _kernel_issuer(pl, units, j):
 
 def _kernel_epilogue(pl, units):
     ev = []
-    nbuf = pl.nbuf if pl.dual else 2
+    nbuf = pl.nbuf
     acc = accph = 0
     for _ in units:
         ev.append(("wait", "TFULL", acc, accph))
