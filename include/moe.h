@@ -153,7 +153,9 @@ size_t moe_workspace_size(const moe_problem_t* p);
  * times routed_scaling_factor.  A NaN logit is read as -inf: softmax
  * probability 0 (left out of the normalising sum), sigmoid score 0, and the
  * key of a -inf logit (with a bias, the bias alone), so it ranks after every
- * finite logit of equal bias.  Each softmax row needs one finite logit. */
+ * finite logit of equal bias.  Each softmax row needs one finite logit.  If
+ * renormalisation meets selected scores that are all zero (every selected
+ * logit NaN), the token's weights are zero. */
 moe_status_t moe_gate_topk(const moe_problem_t* p, const float* logits, const float* bias,
                            int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 

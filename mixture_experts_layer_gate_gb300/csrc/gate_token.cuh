@@ -63,7 +63,7 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
     float l = -INFINITY;
     if (e < a.E) {
       l = lrow[e];
-      if (l != l) l = -INFINITY;  // NaN ranks lowest
+      if (l != l) l = -INFINITY;  // a NaN logit is read as -inf
     } else {
       taken |= 1u << i;
     }
@@ -166,7 +166,9 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
   if (lane == 0) {
     int32_t* ids = a.ids + static_cast<size_t>(t) * a.k;
     float* w = a.w + static_cast<size_t>(t) * a.k;
-    const float inv = a.renormalize ? 1.0f / total : 1.0f;
+    // selected scores that are all zero (every selected logit NaN) give zero
+    // weights instead of 0 / 0
+    const float inv = a.renormalize ? (total > 0.f ? 1.0f / total : 0.f) : 1.0f;
 #pragma unroll 1
     for (int j = 0; j < a.k; ++j) {
       ids[j] = sel_idx[j];

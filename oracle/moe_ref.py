@@ -96,7 +96,9 @@ def logits_fp64(logits: np.ndarray) -> np.ndarray:
     the router scores lowest, i.e. -inf: softmax probability 0 (and left out of
     the normalising sum), sigmoid score 0, selection key of a -inf logit (with
     a bias the key is then the bias alone).  Rows must keep at least one finite
-    logit for the softmax to be defined."""
+    logit for the softmax to be defined.  When renormalisation meets selected
+    scores that are all zero (every selected logit NaN: with groups, a row's
+    finite experts may all sit in groups that lost), the weights are zero."""
     l = np.asarray(logits, dtype=np.float64)
     return np.where(np.isnan(l), -np.inf, l)
 
@@ -175,7 +177,10 @@ def gate_weights(p: Problem, logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
         score = sigmoid_fp64(logits)
     w = np.take_along_axis(score, ids.astype(np.int64), axis=1)
     if p.renormalize:
-        w = w / w.sum(axis=1, keepdims=True)
+        # a token whose selected scores are all zero (possible only when every
+        # selected logit is NaN) gets zero weights rather than 0 / 0
+        tot = w.sum(axis=1, keepdims=True)
+        w = np.divide(w, tot, out=np.zeros_like(w), where=tot > 0)
     return w * float(p.routed_scaling_factor)
 
 

@@ -304,3 +304,17 @@ def test_nan_sigmoid_raw_keys_rank_last():
         best = fin[np.argmax(l[t, fin])]
         assert ids[t, 0] == best
         assert w[t, 0] == pytest.approx(scipy.special.expit(float(l[t, best])), rel=1e-15)
+
+
+def test_nan_only_selection_gets_zero_weights():
+    # E = 8, 2 groups of 4 keep 1, k = 2, bias 0.3 on group 1 only.  Expert 0 is
+    # the only finite logit (0.0, score 0.5, key 0.5): group 0 scores 0.5 + 0
+    # (the NaN experts' keys are their zero bias), group 1 scores 0.3 + 0.3 = 0.6
+    # and wins, so experts 4 and 5 (both NaN, score 0) are selected; renormalising
+    # two zero scores gives zero weights, not 0 / 0.
+    l = np.array([[0.0] + [np.nan] * 7], dtype=np.float32)
+    bias = np.array([0, 0, 0, 0, 0.3, 0.3, 0.3, 0.3], dtype=np.float32)
+    p = _prob(8, 2, scoring="sigmoid", renormalize=True, n_group=2, topk_group=1, routed_scaling_factor=2.5)
+    ids, w, _ = oracle.gate(p, l, bias)
+    assert ids[0].tolist() == [4, 5]
+    assert w[0].tolist() == [0.0, 0.0]
