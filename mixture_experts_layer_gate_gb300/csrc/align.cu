@@ -14,6 +14,7 @@
 //   gather_rows   : x_perm[inv[t*k + j]] = x[t] for each of token t's k slots
 //                   (fp8: e4m3 of x / a1, quantised once per token).
 #include "common.cuh"
+#include "gather_token.cuh"
 #include "kernels.h"
 
 namespace moe {
@@ -171,36 +172,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(AlignArgs a
   pdl_trigger();
   if (threadIdx.x < a.k) rows[threadIdx.x] = a.inv[static_cast<size_t>(t) * a.k + threadIdx.x];
   __syncthreads();
-  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
-                                                    static_cast<size_t>(t) * a.H);
-  const int nvec = a.H / 8;
-  if (!FP8) {
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.x_perm);
-    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) {
-      const uint4 v = __ldg(src + c);
-      for (int j = 0; j < a.k; ++j)
-        reinterpret_cast<uint4*>(dst + static_cast<size_t>(rows[j]) * a.H)[c] = v;
-    }
-  } else {
-    const float s = a.a1[0];
-    uint8_t* dst = static_cast<uint8_t*>(a.x_perm);
-    for (int c = threadIdx.x; c < nvec; c += kGatherThreads) {
-      const uint4 v = __ldg(src + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t q[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint16_t lo = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h]), s),
-                                            __fdiv_rn(bf16_hi(w[2 * h]), s));
-        const uint16_t hi = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[2 * h + 1]), s),
-                                            __fdiv_rn(bf16_hi(w[2 * h + 1]), s));
-        q[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      }
-      const uint2 qv = make_uint2(q[0], q[1]);
-      for (int j = 0; j < a.k; ++j)
-        reinterpret_cast<uint2*>(dst + static_cast<size_t>(rows[j]) * a.H)[c] = qv;
-    }
-  }
+  gather_token<FP8>(a, t, rows, threadIdx.x, kGatherThreads);
 }
 
 __global__ void __launch_bounds__(256)

@@ -318,7 +318,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
 // ---------------------------------------------------------- workspace layout
 
 struct Layout {
-  size_t hdr, align_counts, partial, act_bf16, scratch_end;
+  size_t hdr, align_counts, partial, tile_cnt, tile_cnt_n, act_bf16, scratch_end;
   size_t ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, total;
 };
 
@@ -341,7 +341,18 @@ Layout layout_of(const moe_problem_t& p) {
   L.align_counts = o;
   o = align256(o + static_cast<size_t>(std::max(1, align_blocks(static_cast<int>(S)))) * p.E * 4);
   L.partial = o;
-  o = align256(o + std::max(partial_bytes(p, true), partial_bytes(p, false)));
+  const size_t pbytes = std::max(partial_bytes(p, true), partial_bytes(p, false));
+  o = align256(o + pbytes);
+  // split-K arrival counters, one per (tile, CTA of a pair, epilogue warp): a
+  // GEMM has at most (S / 16 + min(E, S)) token tiles per weight block
+  L.tile_cnt = o;
+  L.tile_cnt_n = 0;
+  if (pbytes > 0) {
+    const size_t tiles = (S + 15) / 16 + std::min<size_t>(p.E, S);
+    const size_t fb = std::max<size_t>(p.I / 64, p.H / 128);
+    L.tile_cnt_n = tiles * fb * 8;
+    o = align256(o + L.tile_cnt_n * sizeof(uint32_t));
+  }
   // dynamic fp8 scales: the SwiGLU output in bf16 before its scale is known
   L.act_bf16 = o;
   if (p.act_scale == MOE_ACT_SCALE_DYNAMIC) o = align256(o + S * p.I * 2);
@@ -552,6 +563,10 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const size_t need = static_cast<size_t>(g.P) * S * N * sizeof(float);
     if (g.P > 1 && need > L.scratch_end - L.partial) return MOE_ERR_UNSUPPORTED;  // plan/size mismatch
   }
+  gp.tile_cnt = nullptr;
+  gp.tile_cnt_cap = 0;
+  gp.fin_out = nullptr;
+  gp.fin_ld = 0;
   if (g.P == 1) {
     gp.epi = up ? kEpiSwiglu : kEpiStore;
     gp.out = out;
@@ -562,20 +577,20 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     gp.out = part;
     gp.out_ld = up ? 2 * static_cast<int64_t>(p.I) : p.H;
     gp.part_stride = static_cast<int64_t>(S) * gp.out_ld;
+    if (defer == nullptr) {
+      // the last slice of each tile finishes it inside the GEMM (no separate pass)
+      gp.tile_cnt = at<uint32_t>(ws, L.tile_cnt);
+      gp.tile_cnt_cap = static_cast<int64_t>(L.tile_cnt_n);
+      gp.fin_out = out;
+      gp.fin_ld = up ? p.I : p.H;
+    }
   }
   cudaError_t err = launch_grouped_gemm(wk, maps, gp, di.sms, g.smem, s);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  if (g.P > 1) {
-    if (up) {
-      err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8 && !dyn, out,
-                                 gp.amax, s);
-    } else if (defer != nullptr) {
-      defer->part = part;  // the caller folds the slice sum into its reduce
-      defer->P = g.P;
-      defer->pstride = gp.part_stride;
-    } else {
-      err = launch_down_finish(part, g.P, gp.part_stride, S, p.H, out, s);
-    }
+  if (g.P > 1 && defer != nullptr) {
+    defer->part = part;  // the caller folds the slice sum into its reduce
+    defer->P = g.P;
+    defer->pstride = gp.part_stride;
   }
   if (err == cudaSuccess && dyn && up)
     err = launch_quantize_e4m3_dynamic(out, static_cast<int64_t>(S) * p.I, ds, 1, final_out, s);
@@ -745,11 +760,10 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
     a1 = &dyn_of(ws)->scale[0];
   }
   if (p->T * p->top_k <= kRouteMaxSlots) {
-    // small batch: gate, histogram, offsets and permutation in one CTA (results
-    // identical to the two-step path below), then the row gather
+    // small batch: gate, histogram, offsets, permutation and row gather in one
+    // kernel (results identical to the path below)
     const AlignArgs aa = align_args(*p, ids, x, a1, counts, offsets, perm, inv, x_perm, ws);
     MOE_TRY(cuda_status(launch_route_small(gate_args(*p, logits, bias, ids, tw), aa, s)));
-    MOE_TRY(cuda_status(launch_gather(aa, s)));
   } else {
     MOE_TRY(run_gate(*p, logits, bias, ids, tw, s));
     MOE_TRY(run_align(*p, ids, x, a1, counts, offsets, perm, inv, x_perm, ws, s));

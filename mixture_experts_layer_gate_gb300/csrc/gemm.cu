@@ -255,6 +255,57 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
     tma_load_3d_hint(dst, &maps.a, bar, kc, t.fb * 128, t.e, pol);
 }
 
+// Split-K tile finish, run by the epilogue warp whose arrival completed the
+// tile's count: its 32 weight rows of every token row of the tile, the P fp32
+// slices summed in slice order from zero, then (gate_up) act = silu(g) * u
+// stored as bf16 (with the dynamic-scale maximum) or as the e4m3 code of
+// act / a2 (float32 division), or (down) y stored as bf16 -- the operations and
+// order of swiglu_finish_kernel / down_finish_kernel, so the results are the
+// same bits.  Slices written by other CTAs are read through L2 (ld.global.cg).
+template <int WK>
+__device__ __noinline__ void splitk_finish(const GemmParams& p, const Unit& t, int q, int lane) {
+  const float* part = static_cast<const float*>(p.out);
+  if (p.is_up) {
+    const int f = lane & 15, h = lane >> 4;  // lanes 0-15 even token rows, 16-31 odd ones
+    const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16 + f;
+    const bool q8 = WK == kW_FP8 && p.q_scale != nullptr;
+    uint32_t mx = 0;
+    for (int tok = h; tok < t.nvalid; tok += 2) {
+      const size_t r = static_cast<size_t>(t.row0 + tok);
+      const float* gp = part + r * p.out_ld + col;
+      float g = 0.f, u = 0.f;
+#pragma unroll 4
+      for (int sl = 0; sl < p.P; ++sl) {
+        g += __ldcg(gp + sl * p.part_stride);
+        u += __ldcg(gp + sl * p.part_stride + p.I);
+      }
+      const float a = silu_f32(g) * u;
+      if (q8) {
+        static_cast<uint8_t*>(p.fin_out)[r * p.fin_ld + col] =
+            static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(a, p.q_scale[0]), 0.f) & 0xFF);
+      } else {
+        const __nv_bfloat16 ab = __float2bfloat16_rn(a);
+        static_cast<__nv_bfloat16*>(p.fin_out)[r * p.fin_ld + col] = ab;
+        mx = max(mx, static_cast<uint32_t>(__bfloat16_as_ushort(ab)) & 0x7FFFu);
+      }
+    }
+    if (p.amax != nullptr) {
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0 && mx != 0u) atomicMax(p.amax, mx);
+    }
+  } else {
+    const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32 + lane;
+    for (int tok = 0; tok < t.nvalid; ++tok) {
+      const size_t r = static_cast<size_t>(t.row0 + tok);
+      const float* yp = part + r * p.out_ld + col;
+      float y = 0.f;
+#pragma unroll 4
+      for (int sl = 0; sl < p.P; ++sl) y += __ldcg(yp + sl * p.part_stride);
+      static_cast<__nv_bfloat16*>(p.fin_out)[r * p.fin_ld + col] = __float2bfloat16_rn(y);
+    }
+  }
+}
+
 // Epilogue role (warps 2..5): drains each unit's accumulator from TMEM and
 // writes act (SwiGLU), y_perm, or fp32 split-K partials.
 // Units are taken from `first` in steps of `stride`; `pair_rank` >= 0 marks a
@@ -407,6 +458,27 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
     if (++acc == nbuf) {
       acc = 0u;
       accph ^= 1u;
+    }
+    if (p.epi == kEpiPartial && p.tile_cnt != nullptr) {
+      // this warp's slice of the tile is in memory: count it; the last of the
+      // tile's P slices finishes the tile's rows (after the accumulator was
+      // handed back, so the next unit's MMAs do not wait for it)
+      const int64_t ci = (static_cast<int64_t>(u / p.P) * 2 + (pair_rank > 0 ? 1 : 0)) * 4 + q;
+      __threadfence();
+      __syncwarp();
+      uint32_t prior = 0;
+      if (lane == 0) {
+        if (ci < p.tile_cnt_cap)
+          prior = atomicAdd(p.tile_cnt + ci, 1u);
+        else
+          record_error(p.err, kErrBadIndex, 0x600u);  // counters sized from the same bound: never
+      }
+      prior = __shfl_sync(0xffffffffu, prior, 0);
+      if (ci < p.tile_cnt_cap && prior == static_cast<uint32_t>(p.P - 1)) {
+        __threadfence();
+        splitk_finish<WK>(p, t, q, lane);
+        if (lane == 0) p.tile_cnt[ci] = 0u;  // every slice arrived: ready for the next call
+      }
     }
   }
 }

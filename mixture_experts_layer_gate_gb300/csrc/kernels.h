@@ -51,9 +51,10 @@ cudaError_t launch_align(const AlignArgs& a, cudaStream_t s);
 // x_perm rows only (perm must be ready).
 cudaError_t launch_gather(const AlignArgs& a, cudaStream_t s);
 
-// Gate + histogram + offsets + stable permutation in one CTA, for batches of
-// at most kRouteMaxSlots (token, expert) slots; ids / w / counts / offsets /
-// perm / inv are bit-identical to launch_gate followed by launch_align.
+// Gate + histogram + offsets + stable permutation + row gather in one kernel,
+// for batches of at most kRouteMaxSlots (token, expert) slots; ids / w /
+// counts / offsets / perm / inv / x_perm are bit-identical to launch_gate
+// followed by launch_align.
 constexpr int kRouteMaxSlots = 1024;
 cudaError_t launch_route_small(const GateArgs& g, const AlignArgs& a, cudaStream_t s);
 
@@ -65,13 +66,8 @@ cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm,
 cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, const float* w,
                                     int T, int H, int k, void* out, cudaStream_t s);
 
-// Split-K finishing passes (fixed summation order over the P slices).
-// amax: dynamic fp8 scales only (bf16 act): running max of the stored |act| bits, else null.
-cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
-                                 const float* a2, int fp8, void* act, uint32_t* amax, cudaStream_t s);
-cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H,
-                               void* y, cudaStream_t s);
-// down_finish + unpermute_reduce in one pass, bit-identical to the pair.
+// The down GEMM's split-K slice sum + unpermute_reduce in one pass, bit-identical
+// to the GEMM finishing its own tiles followed by unpermute_reduce.
 cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pstride, const int32_t* inv,
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s);
 
@@ -119,6 +115,14 @@ struct GemmParams {
   const uint8_t* w4_zero;  // int4 / int8: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
   int64_t out_ld;          // elements per output row
   int64_t part_stride;     // elements between split-K slices
+  // Split-K finished inside the GEMM (null: a separate pass adds the slices):
+  // one arrival counter per (tile, CTA of the pair, epilogue warp), zero between
+  // calls; the last of a tile's P arrivals sums the slices in slice order and
+  // writes fin_out (act through SwiGLU, or y) with fin_ld elements per row.
+  uint32_t* tile_cnt;
+  int64_t tile_cnt_cap;
+  void* fin_out;
+  int64_t fin_ld;
   int E, S, I;
   int FB;                  // feature blocks (I/64 for gate_up, H/128 for down)
   int KB;                  // k blocks of the reduction

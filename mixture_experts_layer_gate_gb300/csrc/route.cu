@@ -1,11 +1,16 @@
-// Stages 1 + 2 for small batches in one CTA: the gate (one warp per token), the
-// per-expert histogram, the offsets scan and the stable ranking of the (token,
-// expert) slots, with no kernel boundary in between.  A decode step would
-// otherwise pay three dependent launches for a few microseconds of work.  The
-// gate is the same per-token routine as gate_topk_kernel and the ranking gives
-// the same unique stable order as align_count + align_scatter, so the results
-// are bit-identical to that path.
+// Stages 1 + 2 for small batches in one kernel: the gate (one warp per token),
+// the per-expert histogram, the offsets scan, the stable ranking of the
+// (token, expert) slots and the row gather, with no kernel boundary in between.
+// A decode step would otherwise pay four dependent launches for a few
+// microseconds of work.  Every CTA computes the whole routing in its own shared
+// memory (at most kRouteMaxSlots slots: cheaper than waiting for another CTA),
+// CTA 0 alone writes ids, weights, counts, offsets, perm and inv, and CTA b
+// gathers tokens b, b + G, ...  The gate is the same per-token routine as
+// gate_topk_kernel, the ranking gives the same unique stable order as
+// align_count + align_scatter and the gather is the same per-token copy, so the
+// results are bit-identical to that path.
 #include "gate_token.cuh"
+#include "gather_token.cuh"
 
 namespace moe {
 
@@ -15,18 +20,33 @@ constexpr int kRouteThreads = 1024;  // one thread per slot (S <= kRouteMaxSlots
 constexpr int kRouteWarps = kRouteThreads / 32;
 static_assert(kRouteThreads >= kRouteMaxSlots, "one slot per thread");
 
-template <int EPL>
-__global__ void __launch_bounds__(kRouteThreads, 1) route_small_kernel(GateArgs g, AlignArgs a) {
+template <int EPL, bool FP8>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_small_kernel(GateArgs g, AlignArgs a, int scratch_bytes) {
   extern __shared__ __align__(16) unsigned char route_smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
+  const bool writer = blockIdx.x == 0;
+  // per-slot ids, weights and permuted rows, private to this CTA
+  int32_t* s_ids = reinterpret_cast<int32_t*>(route_smem + scratch_bytes);
+  float* s_w = reinterpret_cast<float*>(s_ids + kRouteMaxSlots);
+  int* s_pos = reinterpret_cast<int*>(s_w + kRouteMaxSlots);
   pdl_wait();
   pdl_trigger();
 
-  // gate: warp w takes tokens w, w + 32, ...; ids go to global memory
+  // gate: warp w takes tokens w, w + 32, ...; ids and weights into shared memory
+  GateArgs gl = g;
+  gl.ids = s_ids;
+  gl.w = s_w;
   float* skeys = reinterpret_cast<float*>(route_smem) + warp * (32 * EPL);
-  for (int t = warp; t < g.T; t += kRouteWarps) gate_detail::gate_token<EPL>(g, t, lane, skeys);
-  __syncthreads();  // the block's ids writes are visible to the block from here on
+  for (int t = warp; t < g.T; t += kRouteWarps) gate_detail::gate_token<EPL>(gl, t, lane, skeys);
+  __syncthreads();
+  if (writer) {
+    for (int i = tid; i < a.S; i += kRouteThreads) {
+      g.ids[i] = s_ids[i];
+      g.w[i] = s_w[i];
+    }
+  }
 
   // the gate's shared memory is reused for the histogram and rank tables
   int* hist = reinterpret_cast<int*>(route_smem);        // [E]
@@ -40,9 +60,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_small_kernel(GateArgs 
   const bool valid = f < a.S;
   int e = -1;
   if (valid) {
-    e = __ldcg(a.ids + f);  // L2 load: written by this block above
+    e = s_ids[f];
     if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-      record_error(a.err, kErrBadIndex, static_cast<uint32_t>(f));
+      if (writer) record_error(a.err, kErrBadIndex, static_cast<uint32_t>(f));
       e = 0;
     }
     atomicAdd(&hist[e], 1);
@@ -73,10 +93,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_small_kernel(GateArgs 
   if (tid < E) {
     const int o0 = warp_sums[warp] + incl - v;
     off[tid] = o0;
-    a.counts[tid] = v;
-    a.offsets[tid] = o0;
+    if (writer) {
+      a.counts[tid] = v;
+      a.offsets[tid] = o0;
+    }
   }
-  if (tid == 0) a.offsets[E] = a.S;
+  if (writer && tid == 0) a.offsets[E] = a.S;
 
   // stable rank: slots of one expert in ascending slot order
   const unsigned same = __match_any_sync(0xffffffffu, e);
@@ -94,27 +116,49 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_small_kernel(GateArgs 
   __syncthreads();
   if (valid) {
     const int pos = off[e] + wc[warp * E + e] + rank;
-    a.perm[pos] = f;
-    a.inv[f] = pos;
+    s_pos[f] = pos;
+    if (writer) {
+      a.perm[pos] = f;
+      a.inv[f] = pos;
+    }
   }
+  __syncthreads();
+
+  // gather: this CTA's tokens, each to the rows its k slots landed on
+  for (int t = blockIdx.x; t < g.T; t += gridDim.x)
+    gather_token<FP8>(a, t, s_pos + static_cast<size_t>(t) * a.k, tid, kRouteThreads);
 }
 
 template <int EPL>
 cudaError_t launch_route(const GateArgs& g, const AlignArgs& a, cudaStream_t s) {
   const size_t gate_bytes = sizeof(float) * kRouteWarps * 32 * EPL;
   const size_t align_bytes = sizeof(int) * (2 * a.E + 32) + sizeof(uint16_t) * kRouteWarps * a.E;
-  const size_t smem = gate_bytes > align_bytes ? gate_bytes : align_bytes;
+  const size_t scratch = ((gate_bytes > align_bytes ? gate_bytes : align_bytes) + 15) & ~static_cast<size_t>(15);
+  const size_t slots = 3 * sizeof(int32_t) * kRouteMaxSlots;
+  const size_t smem = scratch + slots;
   static int configured = -1;  // attribute set once per device (single-device processes)
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (configured != dev) {
-    err = cudaFuncSetAttribute(route_small_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(sizeof(float) * kRouteWarps * 32 * 32));
+    const int most = static_cast<int>(sizeof(float) * kRouteWarps * 32 * 32 + slots);
+    err = cudaFuncSetAttribute(route_small_kernel<EPL, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(route_small_kernel<EPL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (err != cudaSuccess) return err;
     configured = dev;
   }
-  return launch_pdl(route_small_kernel<EPL>, dim3(1), dim3(kRouteThreads), smem, s, g, a);
+  // one CTA per token up to the SM count: every CTA repeats the routing, so
+  // more CTAs only shorten the gather
+  int sms = 0;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int grid = g.T < sms ? g.T : sms;
+  if (a.fp8)
+    return launch_pdl(route_small_kernel<EPL, true>, dim3(grid), dim3(kRouteThreads), smem, s, g, a,
+                      static_cast<int>(scratch));
+  return launch_pdl(route_small_kernel<EPL, false>, dim3(grid), dim3(kRouteThreads), smem, s, g, a,
+                    static_cast<int>(scratch));
 }
 
 }  // namespace

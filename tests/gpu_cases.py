@@ -172,13 +172,21 @@ def full_check(shape, T, device, seed=0, check_stages=True, nan_logits=0.0):
         # act from the same x_perm
         act_g = to_f64(g.act, shape.wdtype, a2_g)
         if shape.wdtype == "fp8":
-            # compare in e4m3 steps (each side's codes): neighbours allowed on a small fraction
+            # compare in e4m3 steps (each side's codes): neighbours allowed on a small
+            # fraction.  Near zero the code is decided by the gate_up sums' own error
+            # (the e4m3 tensor-core product accumulates thousands of terms in its
+            # internal precision; the oracle is exact), not by the rounding: there a
+            # difference of up to 2^-7 (four subnormal steps, in units of a2) is
+            # accepted instead of one step.
             vals = np.sort(oracle.decode_e4m3(np.arange(256, dtype=np.uint8)))
             vals = vals[np.isfinite(vals)]
-            idx_g = np.searchsorted(vals, act_g / float(np.float32(a2_g)))
-            idx_o = np.searchsorted(vals, res["act"] / float(np.float32(a2)))
+            sg = act_g / float(np.float32(a2_g))
+            so = res["act"] / float(np.float32(a2))
+            idx_g = np.searchsorted(vals, sg)
+            idx_o = np.searchsorted(vals, so)
             diff = np.abs(idx_g - idx_o)
-            assert diff.max() <= 1, diff.max()
+            near_zero = np.abs(sg - so) <= 2.0 ** -7
+            assert diff[~near_zero].max(initial=0) <= 1, diff[~near_zero].max(initial=0)
             assert np.mean(diff > 0) < 0.02, np.mean(diff > 0)
         else:
             assert rel_err(act_g, res["act"]) <= tol, rel_err(act_g, res["act"])
