@@ -316,7 +316,7 @@ typedef struct {
  * tolerances; only speed changes).  Each field is -1 for the planner's own
  * choice:
  *   bn_max      token tile limit, a multiple of 16 in [16, 256] (int4 / int8
- *               take it only up to 128)
+ *               above 128 only on CTA pairs)
  *   stages      operand ring depth, 2..8 (only ever lowers the planner's)
  *   splits      split-K factor, 1..16 (at most K / 256; a workspace sized for
  *               fewer slices makes the GEMM call return MOE_ERR_UNSUPPORTED)
@@ -329,12 +329,14 @@ typedef struct {
  *   full_box    1 = whole token tiles in one TMA box per stage, 0 = 64- and
  *               16-row boxes for an expert's ragged last tile
  *   w_stream    1 = weights loaded with the L2 evict-first policy, 0 = normal
+ *   unit_order  0 = GEMM work units expert by expert, 1 = weight block by
+ *               weight block across experts
  * The overrides apply to every later plan of the process (all threads) until
  * the next call; NULL restores the planner's choices.  Values outside those
  * ranges return MOE_ERR_INVALID_ARG and change nothing.  The library never
  * reads tuning from the environment. */
 typedef struct {
-  int32_t bn_max, stages, splits, pair, conv_groups, slot_kb, ksplit, dual, full_box, w_stream;
+  int32_t bn_max, stages, splits, pair, conv_groups, slot_kb, ksplit, dual, full_box, w_stream, unit_order;
 } moe_tuning_t;
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t);

@@ -64,7 +64,7 @@ class Plan(ctypes.Structure):
 
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("bn_max", "stages", "splits", "pair", "conv_groups", "slot_kb",
-                                             "ksplit", "dual", "full_box", "w_stream")]
+                                             "ksplit", "dual", "full_box", "w_stream", "unit_order")]
 
 
 TUNING_KNOBS = tuple(n for n, _ in Tuning._fields_)

@@ -137,7 +137,7 @@ struct GemmPlan {
 // field of -1 leaves the planner's choice).  Nothing is read from the
 // environment: a process gets these only by calling moe_set_tuning.
 std::mutex g_tuning_mu;
-moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 moe_tuning_t current_tuning() {
   std::lock_guard<std::mutex> lock(g_tuning_mu);
@@ -542,6 +542,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const int ws_env = knob(current_tuning().w_stream, -1);
     if (ws_env == 0 || ws_env == 1) gp.w_stream = ws_env;
   }
+  gp.fb_major = knob(current_tuning().unit_order, 0);
   gp.KB = g.KB;
   gp.P = g.P;
   gp.bn_max = g.bn_max;
@@ -836,14 +837,14 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
 }
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t) {
-  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
   if (t != nullptr) {
     v = *t;
     auto ok = [](int32_t x, int32_t lo, int32_t hi) { return x == -1 || (x >= lo && x <= hi); };
     if (!ok(v.bn_max, 16, 256) || (v.bn_max > 0 && v.bn_max % 16 != 0) || !ok(v.stages, 2, kMaxStages) ||
         !ok(v.splits, 1, kMaxSplits) || !ok(v.pair, 0, 1) || !ok(v.conv_groups, 2, 3) ||
         !(v.slot_kb == -1 || v.slot_kb == 2 || v.slot_kb == 4) || !ok(v.ksplit, 0, 1) || !ok(v.dual, 0, 1) ||
-        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1))
+        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 1))
       return MOE_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_tuning_mu);

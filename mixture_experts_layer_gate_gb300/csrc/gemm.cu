@@ -91,17 +91,33 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   Unit t;
   const int tile = u / p.P;
   t.sp = u - tile * p.P;
-  int lo = 0, hi = p.E;  // largest e with tile_base[e] <= tile
+  // Expert-major order: an expert's units are consecutive (weight block fb, then
+  // its token tiles).  Weight-block-major order: for each fb, every expert's
+  // token tiles; concurrent units then mix experts, e.g. one expert's
+  // tensor-bound tiles with the weight streams of experts that have few rows.
+  int key = tile, fbm = 0;
+  if (p.fb_major) {
+    const int nt = tile_base[p.E] / p.FB;  // token tiles over all experts
+    fbm = tile / nt;
+    key = (tile - fbm * nt) * p.FB;
+  }
+  int lo = 0, hi = p.E;  // largest e with tile_base[e] <= key
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (tile_base[mid] <= tile) lo = mid; else hi = mid;
+    if (tile_base[mid] <= key) lo = mid; else hi = mid;
   }
   t.e = lo;
   const int cnt = off[lo + 1] - off[lo];
   const int nb = (cnt + p.bn_max - 1) / p.bn_max;
-  const int local = tile - tile_base[lo];
-  t.fb = local / nb;
-  const int tb = local - t.fb * nb;
+  const int local = key - tile_base[lo];
+  int tb;
+  if (p.fb_major) {
+    t.fb = fbm;
+    tb = local / p.FB;
+  } else {
+    t.fb = local / nb;
+    tb = local - t.fb * nb;
+  }
   // An expert's rows are split into nb tiles of equal height (a multiple of 16,
   // or of 32 for CTA pairs), not into full tiles plus a short tail: a tail of a
   // few rows would cost a whole pass of the tensor core over the weight tile

@@ -230,7 +230,8 @@ def test_full_size_sampled(dev, name, T):
 # library's planner overrides (moe_set_tuning): the single-CTA
 # bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's pair / non-pair,
 # one / two MMA-issuer, two-k-block-slot, three-converter-group, k-split /
-# alternating-stage and per-64/16-row token box (no full box) modes.
+# alternating-stage and per-64/16-row token box (no full box) modes, and the
+# weight-block-major unit order.
 @pytest.mark.parametrize("name,knobs", [
     ("mixtral", {"pair": 0}),
     ("qwen2", {"pair": 0}),
@@ -264,6 +265,11 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"pair": 0, "dual": 1, "bn_max": 128}),
     ("mixtral_w8", {"pair": 1, "dual": 1}),
     ("mixtral_w8_zp", {"pair": 1, "dual": 1, "bn_max": 128}),
+    ("mixtral", {"unit_order": 1}),
+    ("qwen2", {"unit_order": 1, "pair": 0}),
+    ("dsv3", {"unit_order": 1}),
+    ("scout", {"unit_order": 1}),
+    ("dsv3_awq", {"unit_order": 1, "bn_max": 256, "pair": 1}),
 ])
 def test_forced_kernel_variants(dev, name, knobs):
     shape = small(name)
