@@ -36,11 +36,8 @@
  *     memory-safe (but meaningless) results.
  *   - A workspace `ws` of at least moe_scratch_size() bytes (stage calls) or
  *     moe_workspace_size() bytes (moe_forward) is passed to the calls that
- *     need one.  Its first moe_scratch_size() bytes must be zero when the
- *     workspace is first used (allocate it zeroed once): they hold the error
- *     header (the first 256 bytes) and the split-K arrival counters, which
- *     every call that ends without a device error leaves at zero again.
- *     After a device error, zero those bytes before the next call.
+ *     need one.  Its first 256 bytes are the error header and must be zero
+ *     when the workspace is first used (allocate it zeroed once).
  *
  * Shapes: T tokens, H hidden, I intermediate per expert, E experts, k = top_k,
  * S = T*k slots.  Requirements: H % 128 == 0, I % 128 == 0, 1 <= k <= E <= 1024,
@@ -238,9 +235,7 @@ size_t moe_padded_capacity(const moe_problem_t* p, int32_t block);
  *   act[r, i] = silu(h[i]) * h[I + i],  silu(z) = z / (1 + exp(-z))
  * act is bf16 [S, I], or for fp8 the e4m3 code of act / a2 (a2 static, or with
  * dynamic scales computed here from the bf16 act over all S rows).
- * Uses ws for split-K partial sums when the expert row counts are small; the
- * last slice of each tile to finish adds the slices (in slice order, so the
- * result does not depend on scheduling) inside the same kernel.
+ * Uses ws for split-K partial sums when the expert row counts are small.
  * offsets need not come from moe_align_permute: any nondecreasing int32
  * [E + 1] with offsets[0] = 0 and offsets[E] = S works, e.g. rows an
  * expert-parallel dispatch delivered for a rank's E local experts (then set
@@ -251,9 +246,8 @@ moe_status_t moe_grouped_gemm_swiglu(const moe_problem_t* p, const moe_weights_t
 
 /* Stage 3b: grouped down GEMM: y_perm[r] = W2[e] act[r] for rows of expert e
  * (fp8: times a2 * w2_scale[e]).  y_perm is bf16 [S, H].  Small row counts
- * split K across CTAs into fp32 partials in ws; the last slice of each tile
- * to finish sums them in slice order (no floating-point atomics; the result
- * does not depend on scheduling). */
+ * split K across CTAs into fp32 partials in ws, summed in a fixed order
+ * (no atomics; the result does not depend on scheduling). */
 moe_status_t moe_grouped_gemm_down(const moe_problem_t* p, const moe_weights_t* w,
                                    const void* act, const int32_t* offsets, void* y_perm,
                                    void* ws, size_t ws_bytes, moe_stream_t stream);

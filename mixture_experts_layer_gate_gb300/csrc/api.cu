@@ -158,15 +158,23 @@ int wkind_of(const moe_problem_t& p) {
 
 // Token tile limit: generous enough that one tile usually holds all of an
 // expert's tokens (each extra token block re-reads the expert's weights).
-// int4 / int8 keep two accumulators and the converted weight tiles in TMEM,
-// which caps their token tile at 128 columns.
+// int4 / int8 keep the converted weight tiles in TMEM beside the accumulators:
+// up to 128 columns with two accumulator buffers (and two MMA issuers), above
+// that (CTA pairs only) one buffer and one issuer.  Each tile converts the
+// weights once, so many rows per expert favour wide tiles: measured on the
+// DeepSeek-V3 int4 shape (T = 4096, 128 rows per expert on average: 192-token
+// tiles 4% faster than 128, 256 slower: its 80 KB ring stages leave two) and
+// the Mixtral int8 shape (T = 1024 and 4096, 256 and 1024 rows per expert:
+// 256-token tiles 18-25% faster).
 int plan_bn_max(const moe_problem_t& p) {
   const long long S = static_cast<long long>(p.T) * p.top_k;
   if (S <= 0) return 16;
   const long long touched = std::max(1ll, std::min<long long>(p.E, S));
   const long long m_avg = (S + touched - 1) / touched;
   long long bn = std::max(3 * m_avg, m_avg + 24);
-  const long long cap = (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) ? 128 : 256;
+  long long cap = 256;
+  if (p.wdtype == MOE_W_INT4_G128) cap = m_avg >= 128 ? 192 : 128;
+  if (p.wdtype == MOE_W_INT8_G128) cap = m_avg >= 192 ? 256 : 128;
   bn = std::min<long long>(cap, std::max<long long>(16, bn));
   return roundup16(static_cast<int>(bn));
 }
@@ -318,7 +326,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
 // ---------------------------------------------------------- workspace layout
 
 struct Layout {
-  size_t hdr, align_counts, partial, tile_cnt, tile_cnt_n, act_bf16, scratch_end;
+  size_t hdr, align_counts, partial, act_bf16, scratch_end;
   size_t ids, w, counts, offsets, perm, inv, x_perm, act, y_perm, total;
 };
 
@@ -341,18 +349,7 @@ Layout layout_of(const moe_problem_t& p) {
   L.align_counts = o;
   o = align256(o + static_cast<size_t>(std::max(1, align_blocks(static_cast<int>(S)))) * p.E * 4);
   L.partial = o;
-  const size_t pbytes = std::max(partial_bytes(p, true), partial_bytes(p, false));
-  o = align256(o + pbytes);
-  // split-K arrival counters, one per (tile, CTA of a pair, epilogue warp): a
-  // GEMM has at most (S / 16 + min(E, S)) token tiles per weight block
-  L.tile_cnt = o;
-  L.tile_cnt_n = 0;
-  if (pbytes > 0) {
-    const size_t tiles = (S + 15) / 16 + std::min<size_t>(p.E, S);
-    const size_t fb = std::max<size_t>(p.I / 64, p.H / 128);
-    L.tile_cnt_n = tiles * fb * 8;
-    o = align256(o + L.tile_cnt_n * sizeof(uint32_t));
-  }
+  o = align256(o + std::max(partial_bytes(p, true), partial_bytes(p, false)));
   // dynamic fp8 scales: the SwiGLU output in bf16 before its scale is known
   L.act_bf16 = o;
   if (p.act_scale == MOE_ACT_SCALE_DYNAMIC) o = align256(o + S * p.I * 2);
@@ -564,10 +561,6 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const size_t need = static_cast<size_t>(g.P) * S * N * sizeof(float);
     if (g.P > 1 && need > L.scratch_end - L.partial) return MOE_ERR_UNSUPPORTED;  // plan/size mismatch
   }
-  gp.tile_cnt = nullptr;
-  gp.tile_cnt_cap = 0;
-  gp.fin_out = nullptr;
-  gp.fin_ld = 0;
   if (g.P == 1) {
     gp.epi = up ? kEpiSwiglu : kEpiStore;
     gp.out = out;
@@ -578,20 +571,20 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     gp.out = part;
     gp.out_ld = up ? 2 * static_cast<int64_t>(p.I) : p.H;
     gp.part_stride = static_cast<int64_t>(S) * gp.out_ld;
-    if (defer == nullptr) {
-      // the last slice of each tile finishes it inside the GEMM (no separate pass)
-      gp.tile_cnt = at<uint32_t>(ws, L.tile_cnt);
-      gp.tile_cnt_cap = static_cast<int64_t>(L.tile_cnt_n);
-      gp.fin_out = out;
-      gp.fin_ld = up ? p.I : p.H;
-    }
   }
   cudaError_t err = launch_grouped_gemm(wk, maps, gp, di.sms, g.smem, s);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  if (g.P > 1 && defer != nullptr) {
-    defer->part = part;  // the caller folds the slice sum into its reduce
-    defer->P = g.P;
-    defer->pstride = gp.part_stride;
+  if (g.P > 1) {
+    if (up) {
+      err = launch_swiglu_finish(part, g.P, gp.part_stride, S, p.I, wt.a2_scale, wk == kW_FP8 && !dyn, out,
+                                 gp.amax, s);
+    } else if (defer != nullptr) {
+      defer->part = part;  // the caller folds the slice sum into its reduce
+      defer->P = g.P;
+      defer->pstride = gp.part_stride;
+    } else {
+      err = launch_down_finish(part, g.P, gp.part_stride, S, p.H, out, s);
+    }
   }
   if (err == cudaSuccess && dyn && up)
     err = launch_quantize_e4m3_dynamic(out, static_cast<int64_t>(S) * p.I, ds, 1, final_out, s);

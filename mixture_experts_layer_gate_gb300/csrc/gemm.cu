@@ -118,15 +118,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
     t.fb = local / nb;
     tb = local - t.fb * nb;
   }
-  // An expert's rows are split into nb tiles of equal height (a multiple of 16,
-  // or of 32 for CTA pairs), not into full tiles plus a short tail: a tail of a
-  // few rows would cost a whole pass of the tensor core over the weight tile
-  // (an MMA instruction takes as long for 16 rows as for 64), balanced tiles
-  // only what the rows need.  (nb - 1) * tsz < cnt, so no tile is empty.
-  const int gran = p.pair ? 32 : 16;
-  const int tsz = ((cnt + nb - 1) / nb + gran - 1) / gran * gran;
-  t.row0 = off[lo] + tb * tsz;
-  t.nvalid = min(tsz, cnt - tb * tsz);
+  // full tiles of bn_max rows and a shorter last one (tiles of equal height
+  // measured slower for bf16 / fp8: more, smaller token boxes per k-block)
+  t.row0 = off[lo] + tb * p.bn_max;
+  t.nvalid = min(p.bn_max, cnt - tb * p.bn_max);
   t.n = (t.nvalid + 15) & ~15;
   t.kb0 = static_cast<int>((static_cast<long long>(t.sp) * p.KB) / p.P);
   t.kb1 = static_cast<int>((static_cast<long long>(t.sp + 1) * p.KB) / p.P);
@@ -230,20 +225,28 @@ __device__ __forceinline__ void ring_advance(int& pos, uint32_t& phase, int& idx
 // completion is counted on the barrier at shared::cluster address `bar`,
 // possibly in the peer CTA.
 template <bool PAIR>
+__device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* m, uint32_t bar, int kcoord, int row,
+                                         uint64_t pol) {
+  if (PAIR)
+    tma_load_2d_pair(dst, m, bar, kcoord, row, pol);
+  else
+    tma_load_2d_hint(dst, m, bar, kcoord, row, pol);
+}
+
+template <bool PAIR>
 __device__ __forceinline__ void load_rows_split(const GemmMaps& maps, uint32_t dst, uint32_t bar, int kcoord,
                                                 int row0, int n, uint64_t pol) {
   int r = 0;
-  auto one = [&](const CUtensorMap* m, int h) {
-    if (PAIR)
-      tma_load_2d_pair(dst + static_cast<uint32_t>(r) * 128u, m, bar, kcoord, row0 + r, pol);
-    else
-      tma_load_2d_hint(dst + static_cast<uint32_t>(r) * 128u, m, bar, kcoord, row0 + r, pol);
-    r += h;
-  };
-  while (n - r >= 128) one(&maps.b128, 128);
-  if (n - r >= 64) one(&maps.b64, 64);
-  if (n - r >= 32) one(&maps.b32, 32);
-  if (n - r >= 16) one(&maps.b16, 16);
+  for (; r + 128 <= n; r += 128) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b128, bar, kcoord, row0 + r, pol);
+  if (n - r >= 64) {
+    tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, row0 + r, pol);
+    r += 64;
+  }
+  if (n - r >= 32) {
+    tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b32, bar, kcoord, row0 + r, pol);
+    r += 32;
+  }
+  if (n - r >= 16) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, row0 + r, pol);
 }
 
 // Token-row loads of one k-block into a B tile: a single box for a full tile,
@@ -269,57 +272,6 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
     tma_load_5d_hint(dst, &maps.a, bar, kc, 0, 0, t.fb * 4, t.e, pol);
   else
     tma_load_3d_hint(dst, &maps.a, bar, kc, t.fb * 128, t.e, pol);
-}
-
-// Split-K tile finish, run by the epilogue warp whose arrival completed the
-// tile's count: its 32 weight rows of every token row of the tile, the P fp32
-// slices summed in slice order from zero, then (gate_up) act = silu(g) * u
-// stored as bf16 (with the dynamic-scale maximum) or as the e4m3 code of
-// act / a2 (float32 division), or (down) y stored as bf16 -- the operations and
-// order of swiglu_finish_kernel / down_finish_kernel, so the results are the
-// same bits.  Slices written by other CTAs are read through L2 (ld.global.cg).
-template <int WK>
-__device__ __noinline__ void splitk_finish(const GemmParams& p, const Unit& t, int q, int lane) {
-  const float* part = static_cast<const float*>(p.out);
-  if (p.is_up) {
-    const int f = lane & 15, h = lane >> 4;  // lanes 0-15 even token rows, 16-31 odd ones
-    const size_t col = static_cast<size_t>(t.fb) * 64 + q * 16 + f;
-    const bool q8 = WK == kW_FP8 && p.q_scale != nullptr;
-    uint32_t mx = 0;
-    for (int tok = h; tok < t.nvalid; tok += 2) {
-      const size_t r = static_cast<size_t>(t.row0 + tok);
-      const float* gp = part + r * p.out_ld + col;
-      float g = 0.f, u = 0.f;
-#pragma unroll 4
-      for (int sl = 0; sl < p.P; ++sl) {
-        g += __ldcg(gp + sl * p.part_stride);
-        u += __ldcg(gp + sl * p.part_stride + p.I);
-      }
-      const float a = silu_f32(g) * u;
-      if (q8) {
-        static_cast<uint8_t*>(p.fin_out)[r * p.fin_ld + col] =
-            static_cast<uint8_t>(f32x2_to_e4m3x2(__fdiv_rn(a, p.q_scale[0]), 0.f) & 0xFF);
-      } else {
-        const __nv_bfloat16 ab = __float2bfloat16_rn(a);
-        static_cast<__nv_bfloat16*>(p.fin_out)[r * p.fin_ld + col] = ab;
-        mx = max(mx, static_cast<uint32_t>(__bfloat16_as_ushort(ab)) & 0x7FFFu);
-      }
-    }
-    if (p.amax != nullptr) {
-      mx = __reduce_max_sync(0xffffffffu, mx);
-      if (lane == 0 && mx != 0u) atomicMax(p.amax, mx);
-    }
-  } else {
-    const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32 + lane;
-    for (int tok = 0; tok < t.nvalid; ++tok) {
-      const size_t r = static_cast<size_t>(t.row0 + tok);
-      const float* yp = part + r * p.out_ld + col;
-      float y = 0.f;
-#pragma unroll 4
-      for (int sl = 0; sl < p.P; ++sl) y += __ldcg(yp + sl * p.part_stride);
-      static_cast<__nv_bfloat16*>(p.fin_out)[r * p.fin_ld + col] = __float2bfloat16_rn(y);
-    }
-  }
 }
 
 // Epilogue role (warps 2..5): drains each unit's accumulator from TMEM and
@@ -474,27 +426,6 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
     if (++acc == nbuf) {
       acc = 0u;
       accph ^= 1u;
-    }
-    if (p.epi == kEpiPartial && p.tile_cnt != nullptr) {
-      // this warp's slice of the tile is in memory: count it; the last of the
-      // tile's P slices finishes the tile's rows (after the accumulator was
-      // handed back, so the next unit's MMAs do not wait for it)
-      const int64_t ci = (static_cast<int64_t>(u / p.P) * 2 + (pair_rank > 0 ? 1 : 0)) * 4 + q;
-      __threadfence();
-      __syncwarp();
-      uint32_t prior = 0;
-      if (lane == 0) {
-        if (ci < p.tile_cnt_cap)
-          prior = atomicAdd(p.tile_cnt + ci, 1u);
-        else
-          record_error(p.err, kErrBadIndex, 0x600u);  // counters sized from the same bound: never
-      }
-      prior = __shfl_sync(0xffffffffu, prior, 0);
-      if (ci < p.tile_cnt_cap && prior == static_cast<uint32_t>(p.P - 1)) {
-        __threadfence();
-        splitk_finish<WK>(p, t, q, lane);
-        if (lane == 0) p.tile_cnt[ci] = 0u;  // every slice arrived: ready for the next call
-      }
     }
   }
 }

@@ -66,8 +66,13 @@ cudaError_t launch_align_block_size(const int32_t* offsets, const int32_t* perm,
 cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, const float* w,
                                     int T, int H, int k, void* out, cudaStream_t s);
 
-// The down GEMM's split-K slice sum + unpermute_reduce in one pass, bit-identical
-// to the GEMM finishing its own tiles followed by unpermute_reduce.
+// Split-K finishing passes (fixed summation order over the P slices).
+// amax: dynamic fp8 scales only (bf16 act): running max of the stored |act| bits, else null.
+cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
+                                 const float* a2, int fp8, void* act, uint32_t* amax, cudaStream_t s);
+cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H,
+                               void* y, cudaStream_t s);
+// down_finish + unpermute_reduce in one pass, bit-identical to the pair.
 cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pstride, const int32_t* inv,
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s);
 
@@ -115,14 +120,6 @@ struct GemmParams {
   const uint8_t* w4_zero;  // int4 / int8: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
   int64_t out_ld;          // elements per output row
   int64_t part_stride;     // elements between split-K slices
-  // Split-K finished inside the GEMM (null: a separate pass adds the slices):
-  // one arrival counter per (tile, CTA of the pair, epilogue warp), zero between
-  // calls; the last of a tile's P arrivals sums the slices in slice order and
-  // writes fin_out (act through SwiGLU, or y) with fin_ld elements per row.
-  uint32_t* tile_cnt;
-  int64_t tile_cnt_cap;
-  void* fin_out;
-  int64_t fin_ld;
   int E, S, I;
   int FB;                  // feature blocks (I/64 for gate_up, H/128 for down)
   int KB;                  // k blocks of the reduction

@@ -1,5 +1,5 @@
-// Stage 4: unpermute and top-k weighted reduction, with or without the down
-// GEMM's split-K slices folded in.
+// Stage 4: unpermute and top-k weighted reduction, plus the split-K finishing
+// passes of the grouped GEMMs.
 //
 // "Add deepseek_v3 fused gate" (sglang) names TensorRT-LLM's
 // unpermute_and_reduce; "[kernel] introduce fused_moe_triton_splitk to sglang"
@@ -65,9 +65,8 @@ __global__ void __launch_bounds__(256)
 // out[t, h] = sum_j w[t, j] * bf16(sum_p part[p][inv[t, j]][h]): the down
 // GEMM's split-K finish folded into the reduce.  The slice sum, its bf16
 // rounding and the weighted sum run in the same order and precision as
-// the down GEMM's own split-K finish (slice sum in slice order, bf16 y) followed
-// by unpermute_reduce, so the result is bit-identical to that pair (and the
-// permuted expert outputs never go through memory).
+// down_finish followed by unpermute_reduce, so the result is bit-identical to
+// that pair (and the permuted expert outputs never go through memory).
 // Block (64, kSplitSlotThreads): a CTA owns 256 columns of one token.  First
 // every (slot j, 4 columns) pair sums its P slices (threads along y take the
 // slots, so a decode step's few tokens still spread over many warps with many
@@ -121,6 +120,67 @@ __global__ void __launch_bounds__(64 * kSplitSlotThreads)
       make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
 }
 
+// act[r, i] = silu(sum_p part[p][r][i]) * sum_p part[p][r][I + i]; 4 columns per thread.
+// amax (bf16 output only, may be null): running max of the stored |act| bits.
+template <bool FP8>
+__global__ void __launch_bounds__(256)
+    swiglu_finish_kernel(const float* __restrict__ part, int P, int64_t pstride, int I,
+                         const float* __restrict__ a2, void* act, uint32_t* amax) {
+  const int r = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  uint32_t mx = 0;
+  if (c * 4 < I) {
+    const float* row = part + static_cast<size_t>(r) * (2 * static_cast<size_t>(I));
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll 4
+    for (int p = 0; p < P; ++p) {
+      const float4 gg = __ldg(reinterpret_cast<const float4*>(row + p * pstride) + c);
+      const float4 uu = __ldg(reinterpret_cast<const float4*>(row + p * pstride + I) + c);
+      g.x += gg.x; g.y += gg.y; g.z += gg.z; g.w += gg.w;
+      u.x += uu.x; u.y += uu.y; u.z += uu.z; u.w += uu.w;
+    }
+    const float a0 = silu_f32(g.x) * u.x, a1 = silu_f32(g.y) * u.y;
+    const float a2v = silu_f32(g.z) * u.z, a3 = silu_f32(g.w) * u.w;
+    if (!FP8) {
+      const uint2 o = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2v, a3));
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(act) + static_cast<size_t>(r) * I)[c] = o;
+      mx = max(max(o.x & 0x7FFFu, (o.x >> 16) & 0x7FFFu), max(o.y & 0x7FFFu, (o.y >> 16) & 0x7FFFu));
+    } else {
+      const float s = a2[0];
+      const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(a0, s), __fdiv_rn(a1, s));
+      const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(a2v, s), __fdiv_rn(a3, s));
+      reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(act) + static_cast<size_t>(r) * I)[c] =
+          lo | (hi << 16);
+    }
+  }
+  if (amax != nullptr) {  // uniform over the grid: every thread of the warp takes part
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((threadIdx.x & 31) == 0 && mx != 0u) atomicMax(amax, mx);
+  }
+}
+
+// y[r, h] = sum_p part[p][r][h] (bf16 out); 4 columns per thread.
+__global__ void __launch_bounds__(256)
+    down_finish_kernel(const float* __restrict__ part, int P, int64_t pstride, int H,
+                       __nv_bfloat16* y) {
+  const int r = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (c * 4 >= H) return;
+  const float* row = part + static_cast<size_t>(r) * H;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int p = 0; p < P; ++p) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(row + p * pstride) + c);
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  }
+  reinterpret_cast<uint2*>(y + static_cast<size_t>(r) * H)[c] =
+      make_uint2(pack_bf16x2(s.x, s.y), pack_bf16x2(s.z, s.w));
+}
+
 }  // namespace
 
 cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, const float* w, int T,
@@ -138,6 +198,24 @@ cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pst
   const dim3 grid((H / 4 + 63) / 64, T);
   return launch_pdl(unpermute_reduce_splitk_kernel, grid, dim3(64, kSplitSlotThreads), 0, s, part, P, pstride,
                     inv, w, H, k, static_cast<__nv_bfloat16*>(out));
+}
+
+cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
+                                 const float* a2, int fp8, void* act, uint32_t* amax, cudaStream_t s) {
+  if (S == 0) return cudaSuccess;
+  const dim3 grid((I / 4 + 255) / 256, S);
+  if (fp8)
+    return launch_pdl(swiglu_finish_kernel<true>, grid, dim3(256), 0, s, part, P, pstride, I, a2, act,
+                      static_cast<uint32_t*>(nullptr));
+  return launch_pdl(swiglu_finish_kernel<false>, grid, dim3(256), 0, s, part, P, pstride, I, a2, act, amax);
+}
+
+cudaError_t launch_down_finish(const float* part, int P, int64_t pstride, int S, int H, void* y,
+                               cudaStream_t s) {
+  if (S == 0) return cudaSuccess;
+  const dim3 grid((H / 4 + 255) / 256, S);
+  return launch_pdl(down_finish_kernel, grid, dim3(256), 0, s, part, P, pstride, H,
+                    static_cast<__nv_bfloat16*>(y));
 }
 
 }  // namespace moe

@@ -333,7 +333,7 @@ def test_launch_count_of_forward(dev, name, T):
     torch.cuda.synchronize()
     small_path = T * shape.top_k <= 1024
     expect = (1 if small_path else 4)             # route with its gather | gate + count + scatter + gather
-    expect += 1                                   # gate_up GEMM (split-K finished inside it)
+    expect += 1 + (plan.splits_up > 1)            # gate_up GEMM (+ split-K finish)
     expect += 1 + 1                               # down GEMM, reduce (split-K finish folded in)
     expect += 2 if shape.act_scale == "dynamic" else 0  # amax(x), e4m3 pass of act
     assert moe.launch_count() - n0 == expect
