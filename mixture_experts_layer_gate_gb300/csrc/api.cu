@@ -485,15 +485,15 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   }
   if (!ok) return MOE_ERR_CUDA;
   {
-    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path), five box heights.
+    // B: permuted token rows [S, K] (bf16, or e4m3 for the fp8 path), three box heights.
     const uint64_t K = up ? H : I;
     const bool f8 = wk == kW_FP8;
     uint64_t dims[2] = {K, static_cast<uint64_t>(S)};
     uint64_t str[1] = {K * (f8 ? 1 : 2)};
     const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap* dst[5] = {&maps.b, &maps.b128, &maps.b64, &maps.b32, &maps.b16};
-    const uint32_t rows[5] = {static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 128u, 64u, 32u, 16u};
-    for (int i = 0; i < 5; ++i) {
+    CUtensorMap* dst[3] = {&maps.b, &maps.b64, &maps.b16};
+    const uint32_t rows[3] = {static_cast<uint32_t>(g.pair ? g.bn_max / 2 : g.bn_max), 64u, 16u};
+    for (int i = 0; i < 3; ++i) {
       uint32_t box[2] = {f8 ? 128u : 64u, rows[i]};
       if (!encode_map(dst[i], dt, 2, in, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MOE_ERR_CUDA;
     }

@@ -220,10 +220,11 @@ __device__ __forceinline__ void ring_advance(int& pos, uint32_t& phase, int& idx
   }
 }
 
-// `n` token rows (a multiple of 16) of one k-block as the fewest boxes of 128,
-// 64, 32 and 16 rows (few, large TMA requests keep the pipe fed).  PAIR: the
-// completion is counted on the barrier at shared::cluster address `bar`,
-// possibly in the peer CTA.
+// `n` token rows (a multiple of 16) of one k-block as 64-row boxes and then
+// 16-row ones.  (A decomposition into 128-, 64-, 32- and 16-row boxes issued
+// the same copies for most tiles yet made the bf16 / fp8 GEMMs 15% slower at
+// mid-size batches.)  PAIR: the completion is counted on the barrier at
+// shared::cluster address `bar`, possibly in the peer CTA.
 template <bool PAIR>
 __device__ __forceinline__ void tma_rows(uint32_t dst, const CUtensorMap* m, uint32_t bar, int kcoord, int row,
                                          uint64_t pol) {
@@ -237,20 +238,12 @@ template <bool PAIR>
 __device__ __forceinline__ void load_rows_split(const GemmMaps& maps, uint32_t dst, uint32_t bar, int kcoord,
                                                 int row0, int n, uint64_t pol) {
   int r = 0;
-  for (; r + 128 <= n; r += 128) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b128, bar, kcoord, row0 + r, pol);
-  if (n - r >= 64) {
-    tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, row0 + r, pol);
-    r += 64;
-  }
-  if (n - r >= 32) {
-    tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b32, bar, kcoord, row0 + r, pol);
-    r += 32;
-  }
-  if (n - r >= 16) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, row0 + r, pol);
+  for (; r + 64 <= n; r += 64) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b64, bar, kcoord, row0 + r, pol);
+  for (; r < n; r += 16) tma_rows<PAIR>(dst + static_cast<uint32_t>(r) * 128u, &maps.b16, bar, kcoord, row0 + r, pol);
 }
 
 // Token-row loads of one k-block into a B tile: a single box for a full tile,
-// else the fewest smaller boxes.
+// 64- and 16-row boxes for an expert's ragged last tile.
 __device__ __forceinline__ void load_token_rows(const GemmMaps& maps, const GemmParams& p,
                                                 const Unit& t, uint32_t dst, uint32_t bar, int kcoord,
                                                 uint64_t pol) {
@@ -470,9 +463,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
-    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
-    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
@@ -637,9 +628,7 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
-    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
-    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {
@@ -865,9 +854,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     fence_mbar_init();
     tma_prefetch_desc(&maps.a);
     tma_prefetch_desc(&maps.b);
-    tma_prefetch_desc(&maps.b128);
     tma_prefetch_desc(&maps.b64);
-    tma_prefetch_desc(&maps.b32);
     tma_prefetch_desc(&maps.b16);
   }
   if (warp == 1) {

@@ -151,10 +151,8 @@ struct GemmMaps {
                     // (2 k-blocks, two boxes per ring stage); 128-byte swizzle
   CUtensorMap b;    // token rows (x_perm or act), box of bn_max rows: one load per full tile
                     // (int4 / int8: 3-D view [k-block][row][64], box of 4 k-blocks)
-  CUtensorMap b128; // the same rows, 128-, 64-, 32- and 16-row boxes: a tile of any
-  CUtensorMap b64;  // other height (a multiple of 16) is loaded as the fewest of these
-  CUtensorMap b32;
-  CUtensorMap b16;
+  CUtensorMap b64;  // the same rows, 64-row box (ragged last tile of an expert)
+  CUtensorMap b16;  // the same rows, 16-row box (ragged last tile of an expert)
 };
 
 size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E);
