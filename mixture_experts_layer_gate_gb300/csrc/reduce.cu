@@ -67,15 +67,61 @@ __global__ void __launch_bounds__(256)
 // rounding and the weighted sum run in the same order and precision as
 // down_finish followed by unpermute_reduce, so the result is bit-identical to
 // that pair (and the permuted expert outputs never go through memory).
-// Block (64, kSplitSlotThreads): a CTA owns 256 columns of one token.  First
+__global__ void __launch_bounds__(256)
+    unpermute_reduce_splitk_kernel(const float* __restrict__ part, int P, int64_t pstride,
+                                   const int32_t* __restrict__ inv, const float* __restrict__ w, int H,
+                                   int k, __nv_bfloat16* out) {
+  __shared__ int s_inv[kReduceMaxK];
+  __shared__ float s_w[kReduceMaxK];
+  const int t = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  load_slots(inv, w, t, k, s_inv, s_w);
+  if (c * 8 >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int j = 0; j < k; ++j) {
+    const int r = s_inv[j];
+    const float wj = s_w[j];
+    const float* row = part + static_cast<size_t>(r) * H;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll 4
+    for (int q = 0; q < P; ++q) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(row + q * pstride) + 2 * c);
+      const float4 b = __ldg(reinterpret_cast<const float4*>(row + q * pstride) + 2 * c + 1);
+      s0.x += a.x; s0.y += a.y; s0.z += a.z; s0.w += a.w;
+      s1.x += b.x; s1.y += b.y; s1.z += b.z; s1.w += b.w;
+    }
+    const uint32_t u[4] = {pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w), pack_bf16x2(s1.x, s1.y),
+                           pack_bf16x2(s1.z, s1.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wj, bf16_lo(u[i]), acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, bf16_hi(u[i]), acc[2 * i + 1]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
+}
+
+// The same result for small batches, with the work spread over the slots too:
+// block (64, kSplitSlotThreads), a CTA owns 256 columns of one token.  First
 // every (slot j, 4 columns) pair sums its P slices (threads along y take the
 // slots, so a decode step's few tokens still spread over many warps with many
 // loads in flight), rounds to bf16 and parks the result in shared memory; then
-// the 64 threads of row y = 0 form the weighted sum in j order.
+// the 64 threads of row y = 0 form the weighted sum in j order.  (At large
+// batches the idle slot rows cost more than the extra parallelism gains.)
 constexpr int kSplitSlotThreads = 8;
 
 __global__ void __launch_bounds__(64 * kSplitSlotThreads)
-    unpermute_reduce_splitk_kernel(const float* __restrict__ part, int P, int64_t pstride,
+    unpermute_reduce_splitk_slots_kernel(const float* __restrict__ part, int P, int64_t pstride,
                                    const int32_t* __restrict__ inv, const float* __restrict__ w, int H,
                                    int k, __nv_bfloat16* out) {
   __shared__ int s_inv[kReduceMaxK];
@@ -195,9 +241,13 @@ cudaError_t launch_unpermute_reduce(const void* y_perm, const int32_t* inv, cons
 cudaError_t launch_unpermute_reduce_splitk(const float* part, int P, int64_t pstride, const int32_t* inv,
                                            const float* w, int T, int H, int k, void* out, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid((H / 4 + 63) / 64, T);
-  return launch_pdl(unpermute_reduce_splitk_kernel, grid, dim3(64, kSplitSlotThreads), 0, s, part, P, pstride,
-                    inv, w, H, k, static_cast<__nv_bfloat16*>(out));
+  const int col_blocks = (H / 4 + 63) / 64;
+  if (static_cast<long long>(T) * col_blocks <= 1024)  // a few waves at most: spread the slots too
+    return launch_pdl(unpermute_reduce_splitk_slots_kernel, dim3(col_blocks, T), dim3(64, kSplitSlotThreads), 0, s,
+                      part, P, pstride, inv, w, H, k, static_cast<__nv_bfloat16*>(out));
+  const dim3 grid((H / 8 + 255) / 256, T);
+  return launch_pdl(unpermute_reduce_splitk_kernel, grid, dim3(256), 0, s, part, P, pstride, inv, w, H, k,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 cudaError_t launch_swiglu_finish(const float* part, int P, int64_t pstride, int S, int I,
