@@ -295,7 +295,8 @@ const char* moe_status_string(moe_status_t s);
  * 0); per GEMM whether it runs as clusters of two CTAs sharing M = 256
  * MMAs (1) or one CTA per 128 weight rows (0); and per GEMM the threads that
  * issue its MMAs in a CTA (1, or for int4 / int8 tiles of at most 64 tokens
- * on one CTA 2, each its half of the reduction into its own accumulator). */
+ * on one CTA 2, each its half of the reduction into its own accumulator); for
+ * int4 / int8 the converter warp groups (2 or 3) per GEMM. */
 typedef struct {
   int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
   int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
@@ -303,6 +304,7 @@ typedef struct {
   int32_t slot_kb_up, slot_kb_down;
   int32_t pair_up, pair_down;
   int32_t issuers_up, issuers_down;
+  int32_t conv_groups_up, conv_groups_down;  /* int4 / int8: converter warp groups (else 0) */
 } moe_plan_t;
 
 /* Planner overrides, for tests and benchmarks that want a kernel variant the

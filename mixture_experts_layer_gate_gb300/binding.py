@@ -59,7 +59,8 @@ class Plan(ctypes.Structure):
                 ("smem_down", ctypes.c_int32), ("num_sms", ctypes.c_int32),
                 ("slot_kb_up", ctypes.c_int32), ("slot_kb_down", ctypes.c_int32),
                 ("pair_up", ctypes.c_int32), ("pair_down", ctypes.c_int32),
-                ("issuers_up", ctypes.c_int32), ("issuers_down", ctypes.c_int32)]
+                ("issuers_up", ctypes.c_int32), ("issuers_down", ctypes.c_int32),
+                ("conv_groups_up", ctypes.c_int32), ("conv_groups_down", ctypes.c_int32)]
 
 
 class Tuning(ctypes.Structure):

@@ -275,10 +275,15 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     const int free_cols = 512 - (g.dual ? 2 : 1) * g.acc_bufs * g.acc_cols;
     const int cg_env = knob(tu.conv_groups, 0);
     const int sk_env = knob(tu.slot_kb, 0);
-    // Two converter groups: with whole-stage slots a third measured no faster
-    // (single-thread issue, of TMA copies and of MMAs, set the pace there); three
-    // remain available with CTA pairs and one MMA issuer for tuning.
+    // Converter groups: three for int4 tiles of <= 32 tokens on one CTA with two
+    // MMA issuers, where TMEM holds the third whole-stage slot beside two pairs of
+    // 32-column partial accumulators (DeepSeek-V3 shape, T = 8 to 64: 4-9% faster
+    // than two; 608 threads leave 96 registers, a few spilled outside the dequant
+    // loop).  Two elsewhere: with one issuer a third measured no faster (single-
+    // thread issue, of TMA copies and of MMAs, set the pace); three remain
+    // available with CTA pairs and one MMA issuer for tuning.
     g.conv_groups = 2;
+    if (wk == kW_INT4 && !g.pair && g.dual && g.acc_cols <= 32 && cg_env != 2) g.conv_groups = 3;
     if (cg_env == 3 && g.pair && wk == kW_INT4 && !g.dual) g.conv_groups = 3;
     auto slots_needed = [&](int sk) { return (g.conv_groups - 1) * (kSuper / sk) + 1; };
     auto slots_fit = [&](int sk) { return std::min(kMaxSlotsInt4, free_cols / (32 * sk)); };
@@ -826,6 +831,8 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->pair_down = d.pair;
   plan->issuers_up = u.dual ? 2 : 1;
   plan->issuers_down = d.dual ? 2 : 1;
+  plan->conv_groups_up = u.conv_groups;
+  plan->conv_groups_down = d.conv_groups;
   return MOE_OK;
 }
 

@@ -668,14 +668,18 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           const uint32_t full_cl = map_to_rank(FULL(st), 0);
-          if (leader) mbar_expect_tx(FULL(st), 2u * (kABytes + static_cast<uint32_t>(half) * 128u));
+          // full_box: every tile's token rows as one box of the full tile height
+          // (rows past the tile are loaded and not used): one copy per k-block
+          const bool fullb = half == half_max || p.full_box;
+          const uint32_t brows = static_cast<uint32_t>(fullb ? half_max : half);
+          if (leader) mbar_expect_tx(FULL(st), 2u * (kABytes + brows * 128u));
           const uint32_t adst = sA + st * kABytes;
           if (p.is_up)
             tma_load_5d_pair(adst, &maps.a, full_cl, kb * kelem, 0, 0, fb * 4, t.e, pol_w);
           else
             tma_load_3d_pair(adst, &maps.a, full_cl, kb * kelem, fb * 128, t.e, pol_w);
           const uint32_t bdst = sR + st * L.r_stride;
-          if (half == half_max)
+          if (fullb)
             tma_load_2d_pair(bdst, &maps.b, full_cl, kb * kelem, r0, pol_t);
           else
             load_rows_split<true>(maps, bdst, full_cl, kb * kelem, r0, half, pol_t);
@@ -1284,6 +1288,7 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
           if (p.dual) return launch_wna16<4, 2, true, 4, true>(maps, p, grid, smem, s);
           return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
         }
+        if (!p.pair && p.conv_groups == 3 && p.dual) return launch_wna16<4, 3, false, 4, true>(maps, p, grid, smem, s);
         if (!p.pair && p.conv_groups == 2) {
           if (p.dual) return launch_wna16<4, 2, false, 4, true>(maps, p, grid, smem, s);
           return launch_wna16<4, 2, false, 4>(maps, p, grid, smem, s);

@@ -45,7 +45,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
-    assert ctypes.sizeof(binding.Plan) == 68
+    assert ctypes.sizeof(binding.Plan) == 76     # 19 four-byte fields
+    assert ctypes.sizeof(binding.Tuning) == 44   # 11 four-byte fields
 
 
 def test_status_strings(lib):
@@ -183,8 +184,13 @@ def _check_plan(shape, pl):
                 assert st >= ast and (st % 2 == 0 or st == 3)
             else:
                 assert st % 2 == 0 or st % 3 == 0
-            if issuers == 2:  # whole-stage slots, two converter groups' ring
+            cg = getattr(pl, f"conv_groups_{side}")
+            assert cg in (2, 3) and ast >= (cg - 1) * (4 // sk) + 1
+            if issuers == 2:  # whole-stage slots
                 assert sk == 4
+            if cg == 3 and issuers == 2:  # int4 tiles of <= 32 tokens on one CTA
+                assert shape.wdtype == "int4" and acc <= 32 and getattr(pl, f"pair_{side}") == 0
+                assert st % 3 == 0
         else:
             assert ast == 0 and getattr(pl, f"slot_kb_{side}") == 0 and issuers == 1
     return pl

@@ -389,8 +389,6 @@ def _accepted_plans():
                 for ks in (False, True):
                     for dual in (False, True):
                         for nbuf in (1, 2):
-                            if dual and cg != 2:
-                                continue        # the planner keeps two issuers to two groups
                             for ns in range(2, 9):
                                 for na in range(2, 8):
                                     pl = Plan(ns, na, cg, sk, ks, dual, nbuf, ctas)
@@ -416,7 +414,8 @@ def test_protocol_holds_for_every_accepted_plan(chunk):
 
 
 @pytest.mark.parametrize("pl", [
-    Plan(ns=6, na=3, dual=True, nbuf=2),              # int4 decode tile (bn 32), one CTA
+    Plan(ns=6, na=3, dual=True, nbuf=2),              # int4 decode tile (bn 32), one CTA, two groups
+    Plan(ns=6, na=3, cg=3, dual=True, nbuf=2),        # int4 decode tile (bn 32), one CTA, three groups
     Plan(ns=4, na=2, dual=True, nbuf=1, ctas=2),      # int4 CTA pair, 128-token tile
     Plan(ns=3, na=2, ks=True, ctas=2),                # int8 CTA pair, k-split ring
     Plan(ns=2, na=2, nbuf=1, ctas=2),                 # int4 CTA pair, 256-token tile, one issuer
