@@ -202,6 +202,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     moe.load()
+    if args.tuning:
+        moe.set_tuning(**json.loads(args.tuning))
     shape = SHAPES[args.config]
     if args.E:
         # profiling aid: same layer shape with fewer experts (smaller device footprint)
@@ -427,6 +429,8 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if args.tuning:
+        line["config"]["planner_overrides"] = json.loads(args.tuning)
     if sweep:
         line["sweep"] = sweep
     if sweeps:
@@ -766,6 +770,8 @@ def main():
     ap.add_argument("--T", type=int, default=4096)
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling small cases)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--tuning", default=None,
+                    help="planner overrides as JSON (moe_set_tuning), e.g. '{\"full_box\": 1}'; for experiments")
     ap.add_argument("--sweep-configs", default=None,
                     help="comma-separated further workloads to sweep in the same run (default with the "
                          "Mixtral headline: qwen2,dsv3,scout,tiny; else none)")
