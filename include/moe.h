@@ -322,8 +322,9 @@ typedef struct {
  *   slot_kb     int4 / int8: k-blocks per converted weight slot, 2 or 4
  *   ksplit      int4 / int8: 1 = both converter groups convert every stage
  *   dual        int4 / int8: 1 = two MMA-issuing threads, 0 = one
- *   full_box    1 = whole token tiles in one TMA box per stage, 0 = 64- and
- *               16-row boxes for an expert's ragged last tile
+ *   full_box    1 = every token tile loaded as one box of the full tile
+ *               height (rows past the tile are loaded and not used), 0 = 64-
+ *               and 16-row boxes for an expert's ragged last tile
  *   w_stream    1 = weights loaded with the L2 evict-first policy, 0 = normal
  *   unit_order  0 = GEMM work units expert by expert, 1 = weight block by
  *               weight block across experts
