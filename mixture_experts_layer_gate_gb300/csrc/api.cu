@@ -26,7 +26,7 @@ namespace {
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
-constexpr int kMaxStages = 8;  // bf16 / fp8 operand ring
+constexpr int kMaxStages = 12;  // bf16 / fp8 operand ring
 constexpr int kMaxStagesInt4 = 8;
 constexpr int kMaxSlotsInt4 = 7;  // int4 / int8: converted weight tiles in TMEM
 constexpr int kSuper = kInt4StageKb;  // int4 / int8: k-blocks per ring stage
