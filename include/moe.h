@@ -327,7 +327,8 @@ typedef struct {
  *               and 16-row boxes for an expert's ragged last tile
  *   w_stream    1 = weights loaded with the L2 evict-first policy, 0 = normal
  *   unit_order  0 = GEMM work units expert by expert, 1 = weight block by
- *               weight block across experts
+ *               weight block across experts, 2 = experts with more than one
+ *               token tile interleaved with the others in proportion
  * The overrides apply to every later plan of the process (all threads) until
  * the next call; NULL restores the planner's choices.  Values outside those
  * ranges return MOE_ERR_INVALID_ARG and change nothing.  The library never

@@ -26,7 +26,7 @@ namespace {
 constexpr int kMaxE = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxSplits = 16;
-constexpr int kMaxStages = 12;  // bf16 / fp8 operand ring
+constexpr int kMaxStages = 8;  // bf16 / fp8 operand ring (12 measured no better)
 constexpr int kMaxStagesInt4 = 8;
 constexpr int kMaxSlotsInt4 = 7;  // int4 / int8: converted weight tiles in TMEM
 constexpr int kSuper = kInt4StageKb;  // int4 / int8: k-blocks per ring stage
@@ -548,7 +548,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const int ws_env = knob(current_tuning().w_stream, -1);
     if (ws_env == 0 || ws_env == 1) gp.w_stream = ws_env;
   }
-  gp.fb_major = knob(current_tuning().unit_order, 0);
+  gp.unit_order = knob(current_tuning().unit_order, 0);
   gp.KB = g.KB;
   gp.P = g.P;
   gp.bn_max = g.bn_max;
@@ -848,7 +848,7 @@ moe_status_t moe_set_tuning(const moe_tuning_t* t) {
     if (!ok(v.bn_max, 16, 256) || (v.bn_max > 0 && v.bn_max % 16 != 0) || !ok(v.stages, 2, kMaxStages) ||
         !ok(v.splits, 1, kMaxSplits) || !ok(v.pair, 0, 1) || !ok(v.conv_groups, 2, 3) ||
         !(v.slot_kb == -1 || v.slot_kb == 2 || v.slot_kb == 4) || !ok(v.ksplit, 0, 1) || !ok(v.dual, 0, 1) ||
-        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 1))
+        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 2))
       return MOE_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_tuning_mu);

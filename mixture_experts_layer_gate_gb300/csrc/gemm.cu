@@ -77,7 +77,7 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
   L.misc = o;
   o += 16;
   L.tiles = o;
-  o += 2 * (E + 1) * 4;
+  o += 4 * (E + 1) * 4;  // tile_base, off, heavy and light prefixes
   L.total = o + 1024;  // slack to align the dynamic base to 1024 B
   return L;
 }
@@ -95,23 +95,40 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   // its token tiles).  Weight-block-major order: for each fb, every expert's
   // token tiles; concurrent units then mix experts, e.g. one expert's
   // tensor-bound tiles with the weight streams of experts that have few rows.
+  // Heavy / light interleave: experts with more than one token tile (their
+  // weight tiles serve many rows: tensor-bound) and the rest (weight-bound)
+  // are listed separately, and unit positions take from the two lists in
+  // proportion to their sizes, so every stretch of concurrent units mixes
+  // the two kinds instead of running them one after the other.
   int key = tile, fbm = 0;
-  if (p.fb_major) {
+  const int* base = tile_base;
+  if (p.unit_order == 1) {
     const int nt = tile_base[p.E] / p.FB;  // token tiles over all experts
     fbm = tile / nt;
     key = (tile - fbm * nt) * p.FB;
+  } else if (p.unit_order == 2) {
+    const int* hb = off + (p.E + 1);
+    const long long H = hb[p.E], U = tile_base[p.E];
+    const long long nh = (static_cast<long long>(tile) * H) / U;
+    if (((static_cast<long long>(tile) + 1) * H) / U > nh) {
+      base = hb;
+      key = static_cast<int>(nh);
+    } else {
+      base = hb + (p.E + 1);
+      key = tile - static_cast<int>(nh);
+    }
   }
-  int lo = 0, hi = p.E;  // largest e with tile_base[e] <= key
+  int lo = 0, hi = p.E;  // largest e with base[e] <= key
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (tile_base[mid] <= key) lo = mid; else hi = mid;
+    if (base[mid] <= key) lo = mid; else hi = mid;
   }
   t.e = lo;
   const int cnt = off[lo + 1] - off[lo];
   const int nb = (cnt + p.bn_max - 1) / p.bn_max;
-  const int local = key - tile_base[lo];
+  const int local = key - base[lo];
   int tb;
-  if (p.fb_major) {
+  if (p.unit_order == 1) {
     t.fb = fbm;
     tb = local / p.FB;
   } else {
@@ -161,6 +178,43 @@ __device__ void build_tile_table(const GemmParams& p, int lane, int* tile_base, 
   if (lane == 31) {
     tile_base[p.E] = incl;
     off[p.E] = p.offsets[p.E];
+  }
+  if (p.unit_order == 2) {
+    // the same prefix split by kind: heavy (> 1 token tile) and light experts
+    int* hb = off + (p.E + 1);
+    int* lb = hb + (p.E + 1);
+    int lh = 0, ll = 0;
+    for (int j = 0; j < per; ++j) {
+      const int e = e0 + j;
+      if (e < p.E) {
+        const int nb = (p.offsets[e + 1] - p.offsets[e] + p.bn_max - 1) / p.bn_max;
+        if (nb >= 2) lh += nb * p.FB; else ll += nb * p.FB;
+      }
+    }
+    int ih = lh, il = ll;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int vh = __shfl_up_sync(0xffffffffu, ih, o);
+      const int vl = __shfl_up_sync(0xffffffffu, il, o);
+      if (lane >= o) {
+        ih += vh;
+        il += vl;
+      }
+    }
+    int rh = ih - lh, rl = il - ll;
+    for (int j = 0; j < per; ++j) {
+      const int e = e0 + j;
+      if (e < p.E) {
+        const int nb = (p.offsets[e + 1] - p.offsets[e] + p.bn_max - 1) / p.bn_max;
+        hb[e] = rh;
+        lb[e] = rl;
+        if (nb >= 2) rh += nb * p.FB; else rl += nb * p.FB;
+      }
+    }
+    if (lane == 31) {
+      hb[p.E] = ih;
+      lb[p.E] = il;
+    }
   }
 }
 

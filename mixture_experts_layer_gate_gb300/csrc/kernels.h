@@ -138,7 +138,7 @@ struct GemmParams {
                            // of every stage's k-blocks into its own partial accumulator
   int acc_bufs;            // accumulator buffers in TMEM (2; 1 with two issuers and > 64 columns)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
-  int fb_major;            // unit order: 0 expert-major, 1 weight-block-major
+  int unit_order;          // 0 expert-major, 1 weight-block-major, 2 heavy / light interleave
   int epi;                 // EpiKind
   int is_up;
   int R;                   // weight rows per expert (2I or H)
