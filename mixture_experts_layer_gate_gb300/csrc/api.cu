@@ -548,7 +548,9 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
     const int ws_env = knob(current_tuning().w_stream, -1);
     if (ws_env == 0 || ws_env == 1) gp.w_stream = ws_env;
   }
-  gp.unit_order = knob(current_tuning().unit_order, 0);
+  // work-unit order: experts with more than one token tile interleaved with the
+  // others whenever both kinds occur (decided on the device from the counts)
+  gp.unit_order = knob(current_tuning().unit_order, 2);
   gp.KB = g.KB;
   gp.P = g.P;
   gp.bn_max = g.bn_max;

@@ -77,7 +77,7 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
   L.misc = o;
   o += 16;
   L.tiles = o;
-  o += 4 * (E + 1) * 4;  // tile_base, off, heavy and light prefixes
+  o += (4 * (E + 1) + 1) * 4;  // tile_base, off, heavy and light prefixes, order in effect
   L.total = o + 1024;  // slack to align the dynamic base to 1024 B
   return L;
 }
@@ -102,11 +102,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   // the two kinds instead of running them one after the other.
   int key = tile, fbm = 0;
   const int* base = tile_base;
-  if (p.unit_order == 1) {
+  // order in effect (build_tile_table): the interleave only where both kinds exist
+  const int order = off[3 * (p.E + 1)];
+  if (order == 1) {
     const int nt = tile_base[p.E] / p.FB;  // token tiles over all experts
     fbm = tile / nt;
     key = (tile - fbm * nt) * p.FB;
-  } else if (p.unit_order == 2) {
+  } else if (order == 2) {
     const int* hb = off + (p.E + 1);
     const long long H = hb[p.E], U = tile_base[p.E];
     const long long nh = (static_cast<long long>(tile) * H) / U;
@@ -128,7 +130,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
   const int nb = (cnt + p.bn_max - 1) / p.bn_max;
   const int local = key - base[lo];
   int tb;
-  if (p.unit_order == 1) {
+  if (order == 1) {
     t.fb = fbm;
     tb = local / p.FB;
   } else {
@@ -146,75 +148,63 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* tile_base, const i
 }
 
 // Work-unit prefix over experts (run by one full warp): expert e owns
-// ceil(count_e / bn_max) * FB tiles; tile_base[E] is the total.
+// ceil(count_e / bn_max) * FB tiles; tile_base[E] is the total.  With the
+// heavy / light order requested it also writes the prefixes of experts with
+// more than one token tile (heavy) and of the others (light), and records the
+// order in effect: the interleave only when both kinds are present.
 __device__ void build_tile_table(const GemmParams& p, int lane, int* tile_base, int* off) {
   const int per = (p.E + 31) / 32;
   const int e0 = lane * per;
-  int local = 0;
+  int local = 0, lh = 0;
   for (int j = 0; j < per; ++j) {
     const int e = e0 + j;
     if (e < p.E) {
       const int c = p.offsets[e + 1] - p.offsets[e];
-      local += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+      const int nb = (c + p.bn_max - 1) / p.bn_max;
+      local += nb * p.FB;
+      if (nb >= 2) lh += nb * p.FB;
     }
   }
-  int incl = local;
+  int incl = local, ih = lh;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int vh = __shfl_up_sync(0xffffffffu, ih, o);
+    if (lane >= o) {
+      incl += v;
+      ih += vh;
+    }
   }
-  int run = incl - local;
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  const int heavy = __shfl_sync(0xffffffffu, ih, 31);
+  const bool mixed = p.unit_order == 2 && heavy > 0 && heavy < total;
+  int run = incl - local, rh = ih - lh, rl = run - rh;
+  int* hb = off + (p.E + 1);
+  int* lb = hb + (p.E + 1);
   for (int j = 0; j < per; ++j) {
     const int e = e0 + j;
     if (e < p.E) {
       const int o0 = p.offsets[e];
       const int c = p.offsets[e + 1] - o0;
+      const int nt = ((c + p.bn_max - 1) / p.bn_max) * p.FB;
       tile_base[e] = run;
       off[e] = o0;
-      run += ((c + p.bn_max - 1) / p.bn_max) * p.FB;
+      run += nt;
+      if (mixed) {
+        hb[e] = rh;
+        lb[e] = rl;
+        if (nt >= 2 * p.FB) rh += nt; else rl += nt;
+      }
     }
   }
   if (lane == 31) {
     tile_base[p.E] = incl;
     off[p.E] = p.offsets[p.E];
-  }
-  if (p.unit_order == 2) {
-    // the same prefix split by kind: heavy (> 1 token tile) and light experts
-    int* hb = off + (p.E + 1);
-    int* lb = hb + (p.E + 1);
-    int lh = 0, ll = 0;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
-      if (e < p.E) {
-        const int nb = (p.offsets[e + 1] - p.offsets[e] + p.bn_max - 1) / p.bn_max;
-        if (nb >= 2) lh += nb * p.FB; else ll += nb * p.FB;
-      }
+    if (mixed) {
+      hb[p.E] = heavy;
+      lb[p.E] = total - heavy;
     }
-    int ih = lh, il = ll;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int vh = __shfl_up_sync(0xffffffffu, ih, o);
-      const int vl = __shfl_up_sync(0xffffffffu, il, o);
-      if (lane >= o) {
-        ih += vh;
-        il += vl;
-      }
-    }
-    int rh = ih - lh, rl = il - ll;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
-      if (e < p.E) {
-        const int nb = (p.offsets[e + 1] - p.offsets[e] + p.bn_max - 1) / p.bn_max;
-        hb[e] = rh;
-        lb[e] = rl;
-        if (nb >= 2) rh += nb * p.FB; else rl += nb * p.FB;
-      }
-    }
-    if (lane == 31) {
-      hb[p.E] = ih;
-      lb[p.E] = il;
-    }
+    off[3 * (p.E + 1)] = mixed ? 2 : (p.unit_order == 1 ? 1 : 0);
   }
 }
 

@@ -273,10 +273,10 @@ def test_full_size_sampled(dev, name, T):
     ("dsv3", {"unit_order": 1}),
     ("scout", {"unit_order": 1}),
     ("dsv3_awq", {"unit_order": 1, "bn_max": 256, "pair": 1}),
-    ("scout", {"unit_order": 2}),
+    ("scout", {"unit_order": 0}),
     ("mixtral", {"unit_order": 2, "pair": 0}),
-    ("dsv3", {"unit_order": 2}),
-    ("qwen2_dyn", {"unit_order": 2}),
+    ("dsv3", {"unit_order": 0}),
+    ("qwen2_dyn", {"unit_order": 0}),
 ])
 def test_forced_kernel_variants(dev, name, knobs):
     shape = small(name)
