@@ -187,9 +187,15 @@ long long plan_tiles(const moe_problem_t& p, bool up, int bn_max) {
   return touched * ((m_avg + bn_max - 1) / bn_max) * FB;
 }
 
+// Split-K factor: the smallest P whose units fill their waves of the SM count
+// to min_eff.  int4 / int8 units carry more fixed cost (converter pipeline,
+// group scales), so they accept emptier waves before splitting: the DeepSeek-V3
+// int4 gate_up at T = 1 took 51.8 us unsplit (84% of one wave's SMs busy) and
+// 58.1 us in four slices.
 int plan_splits(const moe_problem_t& p, bool up, int bn_max, int KB, int sms) {
   const long long tiles = plan_tiles(p, up, bn_max);
   if (tiles >= 4ll * sms) return 1;
+  const double min_eff = (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) ? 0.8 : 0.9;
   const int pmax = std::max(1, std::min(kMaxSplits, KB / 4));
   int best = 1;
   double best_eff = 0.0;
@@ -197,7 +203,7 @@ int plan_splits(const moe_problem_t& p, bool up, int bn_max, int KB, int sms) {
     const long long units = tiles * P;
     const long long waves = (units + sms - 1) / sms;
     const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
-    if (eff >= 0.9) return P;
+    if (eff >= min_eff) return P;
     if (eff > best_eff + 1e-9) {
       best_eff = eff;
       best = P;
