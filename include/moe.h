@@ -296,7 +296,8 @@ const char* moe_status_string(moe_status_t s);
  * MMAs (1) or one CTA per 128 weight rows (0); and per GEMM the threads that
  * issue its MMAs in a CTA (1, or for int4 / int8 tiles of at most 64 tokens
  * on one CTA 2, each its half of the reduction into its own accumulator); for
- * int4 / int8 the converter warp groups (2 or 3) per GEMM. */
+ * int4 / int8 the converter warp groups (2 or 3) per GEMM; per GEMM the warps
+ * that drain its accumulators (4, or 8 taking alternate 32-token columns). */
 typedef struct {
   int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
   int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
@@ -305,6 +306,7 @@ typedef struct {
   int32_t pair_up, pair_down;
   int32_t issuers_up, issuers_down;
   int32_t conv_groups_up, conv_groups_down;  /* int4 / int8: converter warp groups (else 0) */
+  int32_t epi_warps_up, epi_warps_down;      /* epilogue warps per CTA (4 or 8) */
 } moe_plan_t;
 
 /* Planner overrides, for tests and benchmarks that want a kernel variant the
@@ -329,12 +331,16 @@ typedef struct {
  *   unit_order  0 = GEMM work units expert by expert, 1 = weight block by
  *               weight block across experts, 2 = experts with more than one
  *               token tile interleaved with the others in proportion
+ *   epi_warps   4 or 8 warps draining the accumulators (8: bf16 / fp8, and
+ *               int4 / int8 on CTA pairs with two converter groups and
+ *               four-k-block slots; elsewhere 4 is kept)
  * The overrides apply to every later plan of the process (all threads) until
  * the next call; NULL restores the planner's choices.  Values outside those
  * ranges return MOE_ERR_INVALID_ARG and change nothing.  The library never
  * reads tuning from the environment. */
 typedef struct {
   int32_t bn_max, stages, splits, pair, conv_groups, slot_kb, ksplit, dual, full_box, w_stream, unit_order;
+  int32_t epi_warps;
 } moe_tuning_t;
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t);

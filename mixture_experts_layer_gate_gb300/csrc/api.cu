@@ -130,6 +130,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* pt
 
 struct GemmPlan {
   int bn_max, P, stages, astages, slot_kb, conv_groups, ksplit, acc_cols, acc_bufs, pair, dual, full_box, FB, KB;
+  int epi_warps;
   size_t smem;
 };
 
@@ -137,7 +138,7 @@ struct GemmPlan {
 // field of -1 leaves the planner's choice).  Nothing is read from the
 // environment: a process gets these only by calling moe_set_tuning.
 std::mutex g_tuning_mu;
-moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 moe_tuning_t current_tuning() {
   std::lock_guard<std::mutex> lock(g_tuning_mu);
@@ -310,13 +311,21 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     per_stage = 16384 + static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStages;
   }
+  // Epilogue warps: eight (two per TMEM lane quarter, alternate 32-token
+  // columns) on bf16 / fp8 CTA pairs, where a short-K down GEMM otherwise waits
+  // on its epilogue (Qwen2 tensor-parallel slice, I = 640, T = 4096: down GEMM
+  // 0.130 -> 0.105 ms; no workload measured slower); four elsewhere.
+  g.epi_warps = (!converts(wk) && g.pair) ? 8 : 4;
+  const int ew_env = knob(tu.epi_warps, 0);
+  if (ew_env == 4 || (ew_env == 8 && gemm_epi8_supported(wk, g.conv_groups, g.pair, g.slot_kb)))
+    g.epi_warps = ew_env;
   // rows of token tile each CTA stages per K step
   const int brows = g.pair ? g.bn_max / 2 : g.bn_max;
-  const size_t fixed = gemm_smem_bytes(wk, brows, 0, g.astages, p.E);
+  const size_t fixed = gemm_smem_bytes(wk, brows, 0, g.astages, p.E, g.epi_warps);
   g.stages = static_cast<int>(std::min<size_t>(cap, (kMaxDynSmem - fixed) / per_stage));
   const int st_env = knob(tu.stages, 0);
   if (st_env >= 2 && st_env < g.stages) g.stages = st_env;
-  while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E) > kMaxDynSmem)
+  while (g.stages > 2 && gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E, g.epi_warps) > kMaxDynSmem)
     --g.stages;
   if (converts(wk)) {
     // Converter groups alternating stages need a ring depth that is a multiple of
@@ -334,7 +343,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   // whole-stage slots: converters wait on the stage ring for slot reuse, which
   // needs at least as many ring stages as slots (parity-wait rule)
   if (converts(wk) && g.slot_kb == kSuper && g.astages > g.stages) g.astages = g.stages;
-  g.smem = gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E);
+  g.smem = gemm_smem_bytes(wk, brows, g.stages, g.astages, p.E, g.epi_warps);
   return g;
 }
 
@@ -566,6 +575,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.conv_groups = g.conv_groups;
   gp.dual = g.dual;
   gp.acc_bufs = g.acc_bufs;
+  gp.epi_warps = g.epi_warps;
   gp.ksplit = g.ksplit;
   gp.acc_cols = g.acc_cols;
   gp.full_box = g.full_box;
@@ -845,18 +855,21 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->issuers_down = d.dual ? 2 : 1;
   plan->conv_groups_up = u.conv_groups;
   plan->conv_groups_down = d.conv_groups;
+  plan->epi_warps_up = u.epi_warps;
+  plan->epi_warps_down = d.epi_warps;
   return MOE_OK;
 }
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t) {
-  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
   if (t != nullptr) {
     v = *t;
     auto ok = [](int32_t x, int32_t lo, int32_t hi) { return x == -1 || (x >= lo && x <= hi); };
     if (!ok(v.bn_max, 16, 256) || (v.bn_max > 0 && v.bn_max % 16 != 0) || !ok(v.stages, 2, kMaxStages) ||
         !ok(v.splits, 1, kMaxSplits) || !ok(v.pair, 0, 1) || !ok(v.conv_groups, 2, 3) ||
         !(v.slot_kb == -1 || v.slot_kb == 2 || v.slot_kb == 4) || !ok(v.ksplit, 0, 1) || !ok(v.dual, 0, 1) ||
-        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 2))
+        !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 2) ||
+        !(v.epi_warps == -1 || v.epi_warps == 4 || v.epi_warps == 8))
       return MOE_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_tuning_mu);

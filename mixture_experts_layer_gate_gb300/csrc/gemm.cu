@@ -17,9 +17,10 @@
 //     offsets, so no host synchronisation is needed and empty experts cost
 //     nothing.
 //   * Warp roles: warp 0 issues TMA loads into a ring of shared-memory stages,
-//     warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5 drain
-//     the double-buffered accumulator (tcgen05.ld) and run the epilogue while
-//     the next unit accumulates.
+//     warp 1 owns TMEM and issues tcgen05.mma from one thread, warps 2..5
+//     (or 2..9, two per TMEM lane quarter) drain the double-buffered
+//     accumulator (tcgen05.ld) and run the epilogue while the next unit
+//     accumulates.
 //   * int4 / int8 weights (grouped_gemm_wna16_kernel, W4A16 / W8A16): each
 //     ring stage holds 4 k-blocks of codes (128 / 256 bytes per weight row)
 //     plus the 4 matching token tiles; converter warp groups turn the codes,
@@ -41,8 +42,7 @@ namespace {
 constexpr int kABytes = 16384;    // 128 rows x 128 B (bf16 / e4m3 weight tile)
 constexpr int kSuper = kInt4StageKb;  // int4 / int8: k-blocks per ring stage
 constexpr int kCodeBox = 16384;       // int4 / int8: one TMA box of codes, 128 rows x 128 B
-constexpr int kStgBytesPerWarp = 2048;
-constexpr int kStgBytes = 4 * kStgBytesPerWarp;
+constexpr int kStgBytesPerWarp = 2048;  // epilogue staging, per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 
 // Shared-memory plan (offsets from a 1024-aligned base).
@@ -53,7 +53,7 @@ struct SmemLayout {
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages, int astages,
-                                                  int E) {
+                                                  int E, int epi_warps) {
   SmemLayout L;
   uint32_t o = 0;
   const uint32_t bbytes = static_cast<uint32_t>(bn_max) * 128u;  // multiple of 2 KB
@@ -70,7 +70,7 @@ __host__ __device__ inline SmemLayout smem_layout(int wk, int bn_max, int stages
     o += stages * bbytes;
   }
   L.stg = o;
-  o += kStgBytes;
+  o += static_cast<uint32_t>(epi_warps) * kStgBytesPerWarp;
   L.bars = o;
   o += (2 * stages + 2 * astages + 6) * 8;
   o = (o + 15u) & ~15u;
@@ -311,8 +311,12 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
     tma_load_3d_hint(dst, &maps.a, bar, kc, t.fb * 128, t.e, pol);
 }
 
-// Epilogue role (warps 2..5): drains each unit's accumulator from TMEM and
-// writes act (SwiGLU), y_perm, or fp32 split-K partials.
+// Epilogue role (warps 2 .. 2 + 4 * nsub - 1): drains each unit's accumulator
+// from TMEM and writes act (SwiGLU), y_perm, or fp32 split-K partials.  A warp
+// may read only the TMEM lane quarter warp % 4; with nsub = 2 (eight warps) the
+// two warps of a quarter take alternate 32-token column blocks, which halves an
+// epilogue that would otherwise outlast short-K units (a down GEMM of a
+// tensor-parallel slice stores 128 x 256 outputs per 5-20 MMAs).
 // Units are taken from `first` in steps of `stride`; `pair_rank` >= 0 marks a
 // CTA-pair kernel (this CTA's rows are weight block 2*fb + rank); the arrival
 // that frees an accumulator goes, one per warp, to the shared::cluster address
@@ -324,9 +328,11 @@ template <int WK, bool DUAL = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
                                              int units, int first, int stride, int pair_rank,
                                              uint32_t tmem_base, uint32_t tfull0, uint32_t tempty_cl0,
-                                             volatile int* abort_flag, uint8_t* stg_all, int warp, int lane) {
-  const int q = warp & 3;  // TMEM lane quarter this warp may read
-  uint8_t* stg = stg_all + q * kStgBytesPerWarp;
+                                             volatile int* abort_flag, uint8_t* stg_all, int warp, int lane,
+                                             int nsub) {
+  const int q = warp & 3;            // TMEM lane quarter this warp may read
+  const int sub = (warp - 2) >> 2;   // which of the quarter's nsub warps
+  uint8_t* stg = stg_all + (warp - 2) * kStgBytesPerWarp;
   const uint32_t nbuf = static_cast<uint32_t>(p.acc_bufs);
   uint32_t acc = 0, accph = 0;
   for (int u = first; u < units; u += stride) {
@@ -345,7 +351,7 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
                            (DUAL ? 2u * acc : acc) * static_cast<uint32_t>(p.acc_cols);
     const bool part1 = DUAL && t.kb1 - t.kb0 > 2;  // warp-uniform
     uint32_t mx = 0;  // dynamic scales: largest stored |act| (bf16 magnitude bits), valid tokens only
-    for (int cb = 0; cb < t.nvalid; cb += 32) {
+    for (int cb = 32 * sub; cb < t.nvalid; cb += 32 * nsub) {
       // two 16-column loads in flight, one wait
       uint32_t vv[2][16];
       const bool two = cb + 16 < t.nvalid;  // warp-uniform
@@ -470,14 +476,14 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
 // ------------------------------------------------------------------ bf16 / fp8
 
 template <int WK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * kMaxEpiWarps, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const int ns = p.stages;
-  const SmemLayout L = smem_layout(WK, p.bn_max, ns, 0, p.E);
+  const SmemLayout L = smem_layout(WK, p.bn_max, ns, 0, p.E, p.epi_warps);
   const uint32_t sA = base_u32 + L.a;
   const uint32_t sR = base_u32 + L.r;
   const uint32_t bars = base_u32 + L.bars;
@@ -492,6 +498,10 @@ __global__ void __launch_bounds__(192, 1)
   int* off = tile_base + (p.E + 1);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if ((p.epi_warps != 4 && p.epi_warps != 8) || blockDim.x != 64u + 32u * p.epi_warps) {
+    if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x501u);  // host plans never do this
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -500,8 +510,8 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
-    mbar_init(tempty0, 4u);  // one arrival per epilogue warp
-    mbar_init(tempty0 + 8u, 4u);
+    mbar_init(tempty0, static_cast<uint32_t>(p.epi_warps));  // one arrival per epilogue warp
+    mbar_init(tempty0 + 8u, static_cast<uint32_t>(p.epi_warps));
     mbar_init(drain_bar, 1u);
     *abort_flag = 0;
     fence_mbar_init();
@@ -607,7 +617,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     run_epilogue<WK>(p, tile_base, off, units, blockIdx.x, gridDim.x, -1, tmem_base, tfull0,
-                     map_to_rank(tempty0, cluster_ctarank()), abort_flag, base + L.stg, warp, lane);
+                     map_to_rank(tempty0, cluster_ctarank()), abort_flag, base + L.stg, warp, lane,
+                     p.epi_warps / 4);
   }
 #undef FULL
 #undef EMPTY
@@ -632,7 +643,7 @@ __global__ void __launch_bounds__(192, 1)
 //   EMPTY (both): the leader's commit arrives on both CTAs' barrier.
 //   tfull (both) / tempty (leader, one arrival per epilogue warp of each CTA).
 template <int WK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * kMaxEpiWarps, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -640,7 +651,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
   const int ns = p.stages;
   const int half_max = p.bn_max / 2;  // token rows per CTA of a full tile
-  const SmemLayout L = smem_layout(WK, half_max, ns, 0, p.E);
+  const SmemLayout L = smem_layout(WK, half_max, ns, 0, p.E, p.epi_warps);
   const uint32_t sA = base_u32 + L.a;
   const uint32_t sR = base_u32 + L.r;
   const uint32_t bars = base_u32 + L.bars;
@@ -657,6 +668,10 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
+  if ((p.epi_warps != 4 && p.epi_warps != 8) || blockDim.x != 64u + 32u * p.epi_warps) {
+    if (threadIdx.x == 0) record_error(p.err, kErrTimeout, 0x501u);  // host plans never do this
+    return;  // (both CTAs of the pair see the same parameters and return)
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -665,8 +680,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(tfull0, 1u);
     mbar_init(tfull0 + 8u, 1u);
-    mbar_init(tempty0, 8u);  // 4 epilogue warps in each CTA of the pair
-    mbar_init(tempty0 + 8u, 8u);
+    // every epilogue warp of both CTAs of the pair
+    mbar_init(tempty0, 2u * static_cast<uint32_t>(p.epi_warps));
+    mbar_init(tempty0 + 8u, 2u * static_cast<uint32_t>(p.epi_warps));
     mbar_init(drain_bar, 1u);
     *abort_flag = 0;
     fence_mbar_init();
@@ -787,7 +803,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     run_epilogue<WK>(p, tile_base, off, units, first, stride, static_cast<int>(rank), tmem_base, tfull0,
-                     map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
+                     map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane, p.epi_warps / 4);
   }
 #undef FULL
 #undef EMPTY
@@ -835,8 +851,8 @@ __global__ void __launch_bounds__(192, 1)
 // range) arrives without a commit.  Accumulator columns: p.acc_bufs buffers (2,
 // or 1 when two pairs of partials do not fit beside two converted slots) of two
 // partials each.
-template <int BITS, int CG, bool PAIR, int SK, bool DUAL>
-__global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
+template <int BITS, int CG, bool PAIR, int SK, bool DUAL, int EW>
+__global__ void __launch_bounds__(64 + 32 * EW + 128 * CG + (DUAL ? 32 : 0), 1)
     grouped_gemm_wna16_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   static_assert(!DUAL || SK == kSuper, "two issuers: whole-stage slots");
   constexpr int WKQ = BITS == 8 ? kW_INT8 : kW_INT4;
@@ -848,7 +864,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
   const int ns = p.stages;
   const int na = p.astages;
   const int brows = PAIR ? p.bn_max / 2 : p.bn_max;  // token rows this CTA stages per k-block
-  const SmemLayout L = smem_layout(WKQ, brows, ns, na, p.E);
+  const SmemLayout L = smem_layout(WKQ, brows, ns, na, p.E, EW);
   const uint32_t sR = base_u32 + L.r;
   const uint32_t btile = static_cast<uint32_t>(brows) * 128u;
   const uint32_t bars = base_u32 + L.bars;
@@ -872,9 +888,12 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
   const bool leader = (rank == 0);
   constexpr uint32_t kCtas = PAIR ? 2u : 1u;
   static_assert(SK == 2 || SK == 4, "converted slots hold 2 or 4 k-blocks");
+  static_assert(EW == 4 || EW == 8, "one or two epilogue warps per TMEM lane quarter");
+  constexpr int kConv0 = 2 + EW;  // first converter warp
   // k-split: both groups convert every stage (group g its k-blocks 2g, 2g + 1)
   const bool ks = p.ksplit != 0;
-  if (p.slot_kb != SK || p.dual != (DUAL ? 1 : 0) || nbuf < 1u || nbuf > 2u || (SK == kSuper && ns < na) ||
+  if (p.slot_kb != SK || p.dual != (DUAL ? 1 : 0) || p.epi_warps != EW || nbuf < 1u || nbuf > 2u ||
+      (SK == kSuper && ns < na) ||
       (ks && (SK != kSuper || CG != 2)) ||
       (!ks && (na < (CG - 1) * (kSuper / SK) + 1 || ns % CG != 0)) ||
       a_col0 + 32u * static_cast<uint32_t>(SK * na) > kTmemCols) {
@@ -894,8 +913,8 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     }
     mbar_init(tfull0, DUAL ? 2u : 1u);
     mbar_init(tfull0 + 8u, DUAL ? 2u : 1u);
-    mbar_init(tempty0, 4u * kCtas);  // one arrival per epilogue warp (of each CTA)
-    mbar_init(tempty0 + 8u, 4u * kCtas);
+    mbar_init(tempty0, static_cast<uint32_t>(EW) * kCtas);  // one arrival per epilogue warp (of each CTA)
+    mbar_init(tempty0 + 8u, static_cast<uint32_t>(EW) * kCtas);
     mbar_init(drain_bar, 1u);
     if (DUAL) mbar_init(drain_bar + 8u, 1u);
     *abort_flag = 0;
@@ -979,7 +998,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
           if ((issued >> s) & 1u) mbar_wait(RFULL(s), (issued_par >> s) & 1u, nullptr, p.err, 0x180u);
       }
     }
-  } else if (warp == 1 || (DUAL && warp == 6 + 4 * CG)) {
+  } else if (warp == 1 || (DUAL && warp == kConv0 + 4 * CG)) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       // issuer j (DUAL): k-blocks [2j, 2j + 2) of every stage, partial accumulator j
@@ -1104,9 +1123,10 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
         mbar_wait(db, 0u, nullptr, p.err, 0x280u);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < kConv0) {
     run_epilogue<WKQ, DUAL>(p, tile_base, off, units, first, stride, PAIR ? static_cast<int>(rank) : -1,
-                          tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane);
+                          tmem_base, tfull0, map_to_rank(tempty0, 0), abort_flag, base + L.stg, warp, lane,
+                          EW / 4);
   } else {
     // ---------------------------------------- int4 / int8 -> bf16 converters
     // The CTA's stages are numbered i = 0, 1, ... in (unit, k) order; a stage of
@@ -1117,7 +1137,7 @@ __global__ void __launch_bounds__(64 + 128 + 128 * CG + (DUAL ? 32 : 0), 1)
     // costs hundreds of cycles each while the other groups saturate the
     // integer pipe.  The thread owns weight row m of the tile, which is TMEM
     // lane m of the converted tile.
-    const int grp = (warp - 6) >> 2;
+    const int grp = (warp - kConv0) >> 2;
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const __half* scales = static_cast<const __half*>(p.w4_scale);
@@ -1285,7 +1305,8 @@ cudaError_t launch_dense(const GemmMaps& maps, const GemmParams& p, int grid, si
   static int configured = -1;  // attribute set once per device (single-device processes)
   cudaError_t err = set_smem_attr(grouped_gemm_kernel<WK>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl(grouped_gemm_kernel<WK>, dim3(grid), dim3(192), smem, s, maps, p);
+  return launch_pdl(grouped_gemm_kernel<WK>, dim3(grid), dim3(gemm_threads(WK, 0, 0, p.epi_warps)), smem, s,
+                    maps, p);
 }
 
 template <int WK>
@@ -1294,32 +1315,53 @@ cudaError_t launch_pair(const GemmMaps& maps, const GemmParams& p, int grid, siz
   static int configured = -1;
   cudaError_t err = set_smem_attr(grouped_gemm_pair_kernel<WK>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(192), smem, s, 2u, maps, p);
+  return launch_pdl_cluster(grouped_gemm_pair_kernel<WK>, dim3(grid & ~1), dim3(gemm_threads(WK, 0, 0, p.epi_warps)),
+                            smem, s, 2u, maps, p);
 }
 
-template <int BITS, int CG, bool PAIR, int SK, bool DUAL = false>
+template <int BITS, int CG, bool PAIR, int SK, bool DUAL = false, int EW = 4>
 cudaError_t launch_wna16(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
                          cudaStream_t s) {
   static int configured = -1;
-  cudaError_t err = set_smem_attr(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL>, &configured);
+  cudaError_t err = set_smem_attr(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL, EW>, &configured);
   if (err != cudaSuccess) return err;
-  return launch_pdl_cluster(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL>,
-                            dim3(PAIR ? (grid & ~1) : grid), dim3(gemm_threads(kW_INT4, CG, DUAL ? 1 : 0)),
+  return launch_pdl_cluster(grouped_gemm_wna16_kernel<BITS, CG, PAIR, SK, DUAL, EW>,
+                            dim3(PAIR ? (grid & ~1) : grid), dim3(gemm_threads(kW_INT4, CG, DUAL ? 1 : 0, EW)),
                             smem, s, PAIR ? 2u : 1u, maps, p);
+}
+
+// int4 / int8 CTA-pair kernels with two converter groups and whole-stage slots
+// come with eight epilogue warps as well as four
+template <int BITS>
+cudaError_t launch_wna16_pair_cg2(const GemmMaps& maps, const GemmParams& p, int grid, size_t smem,
+                                  cudaStream_t s) {
+  if (p.epi_warps == 8) {
+    if (p.dual) return launch_wna16<BITS, 2, true, 4, true, 8>(maps, p, grid, smem, s);
+    return launch_wna16<BITS, 2, true, 4, false, 8>(maps, p, grid, smem, s);
+  }
+  if (p.dual) return launch_wna16<BITS, 2, true, 4, true>(maps, p, grid, smem, s);
+  return launch_wna16<BITS, 2, true, 4>(maps, p, grid, smem, s);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E) {
-  return smem_layout(wkind, bn_max, stages, astages, E).total;
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E, int epi_warps) {
+  return smem_layout(wkind, bn_max, stages, astages, E, epi_warps).total;
 }
 
-int gemm_threads(int wkind, int conv_groups, int dual) {
-  return converts(wkind) ? 64 + 128 + 128 * conv_groups + (dual ? 32 : 0) : 192;
+int gemm_threads(int wkind, int conv_groups, int dual, int epi_warps) {
+  return 64 + 32 * epi_warps + (converts(wkind) ? 128 * conv_groups + (dual ? 32 : 0) : 0);
+}
+
+bool gemm_epi8_supported(int wkind, int conv_groups, int pair, int slot_kb) {
+  if (!converts(wkind)) return true;
+  return pair && conv_groups == 2 && slot_kb == kSuper;
 }
 
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s) {
+  if (p.epi_warps != 4 && !(p.epi_warps == 8 && gemm_epi8_supported(wkind, p.conv_groups, p.pair, p.slot_kb)))
+    return cudaErrorInvalidValue;
   switch (wkind) {
     case kW_BF16:
       return p.pair ? launch_pair<kW_BF16>(maps, p, grid, smem, s) : launch_dense<kW_BF16>(maps, p, grid, smem, s);
@@ -1328,10 +1370,7 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_INT4:
       if (p.slot_kb == 4) {
         if (p.pair && p.conv_groups == 3) return launch_wna16<4, 3, true, 4>(maps, p, grid, smem, s);
-        if (p.pair && p.conv_groups == 2) {
-          if (p.dual) return launch_wna16<4, 2, true, 4, true>(maps, p, grid, smem, s);
-          return launch_wna16<4, 2, true, 4>(maps, p, grid, smem, s);
-        }
+        if (p.pair && p.conv_groups == 2) return launch_wna16_pair_cg2<4>(maps, p, grid, smem, s);
         if (!p.pair && p.conv_groups == 3 && p.dual) return launch_wna16<4, 3, false, 4, true>(maps, p, grid, smem, s);
         if (!p.pair && p.conv_groups == 2) {
           if (p.dual) return launch_wna16<4, 2, false, 4, true>(maps, p, grid, smem, s);
@@ -1346,10 +1385,7 @@ cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParam
     case kW_INT8:  // two converter groups only
       if (p.conv_groups != 2) return cudaErrorInvalidValue;
       if (p.slot_kb == 4) {
-        if (p.pair) {
-          if (p.dual) return launch_wna16<8, 2, true, 4, true>(maps, p, grid, smem, s);
-          return launch_wna16<8, 2, true, 4>(maps, p, grid, smem, s);
-        }
+        if (p.pair) return launch_wna16_pair_cg2<8>(maps, p, grid, smem, s);
         if (p.dual) return launch_wna16<8, 2, false, 4, true>(maps, p, grid, smem, s);
         return launch_wna16<8, 2, false, 4>(maps, p, grid, smem, s);
       } else if (p.slot_kb == 2) {

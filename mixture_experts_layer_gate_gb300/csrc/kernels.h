@@ -137,6 +137,7 @@ struct GemmParams {
   int dual;                // int4 / int8, whole-stage slots: two MMA-issuing threads, each its half
                            // of every stage's k-blocks into its own partial accumulator
   int acc_bufs;            // accumulator buffers in TMEM (2; 1 with two issuers and > 64 columns)
+  int epi_warps;           // epilogue warps: 4 (one per TMEM lane quarter) or 8 (two per quarter)
   int w_stream;            // 1: each weight tile is read once (evict it from L2 first)
   int unit_order;          // 0 expert-major, 1 weight-block-major, 2 heavy / light interleave
   int epi;                 // EpiKind
@@ -155,8 +156,11 @@ struct GemmMaps {
   CUtensorMap b16;  // the same rows, 16-row box (ragged last tile of an expert)
 };
 
-size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E);
-int gemm_threads(int wkind, int conv_groups, int dual);
+constexpr int kMaxEpiWarps = 8;
+size_t gemm_smem_bytes(int wkind, int bn_max, int stages, int astages, int E, int epi_warps);
+int gemm_threads(int wkind, int conv_groups, int dual, int epi_warps);
+// whether a kernel with eight epilogue warps exists for this configuration
+bool gemm_epi8_supported(int wkind, int conv_groups, int pair, int slot_kb);
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s);
 

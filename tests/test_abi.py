@@ -45,8 +45,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
-    assert ctypes.sizeof(binding.Plan) == 76     # 19 four-byte fields
-    assert ctypes.sizeof(binding.Tuning) == 44   # 11 four-byte fields
+    assert ctypes.sizeof(binding.Plan) == 84     # 21 four-byte fields
+    assert ctypes.sizeof(binding.Tuning) == 48   # 12 four-byte fields
 
 
 def test_status_strings(lib):
@@ -163,6 +163,13 @@ def _check_plan(shape, pl):
         assert getattr(pl, f"smem_{side}") <= 232448
         issuers = getattr(pl, f"issuers_{side}")
         assert issuers in (1, 2)
+        ew = getattr(pl, f"epi_warps_{side}")
+        assert ew in (4, 8)
+        if ew == 8 and shape.wdtype in ("int4", "int8"):
+            # eight epilogue warps exist only for CTA pairs, two converter groups and
+            # whole-stage slots
+            assert getattr(pl, f"pair_{side}") == 1 and getattr(pl, f"conv_groups_{side}") == 2
+            assert getattr(pl, f"slot_kb_{side}") == 4
         if shape.wdtype in ("int4", "int8"):
             # TMEM holds the accumulators (two buffers, or with two issuing threads
             # two partials per buffer and one buffer above 64 columns) and the
@@ -211,6 +218,9 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             two = (shape.wdtype == "int4" and bn <= 128) or (shape.wdtype == "int8" and small)
             assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not small else 0)
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
+            # eight epilogue warps on bf16 / fp8 CTA pairs, four elsewhere
+            conv = shape.wdtype in ("int4", "int8")
+            assert getattr(pl, f"epi_warps_{side}") == (8 if getattr(pl, f"pair_{side}") and not conv else 4)
 
 
 @pytest.mark.parametrize("pair", [0, 1])
@@ -242,9 +252,27 @@ def test_tuning_overrides_are_explicit_and_validated(lib, monkeypatch):
         assert forced.pair_up == 1 - base.pair_up and forced.stages_up == 2
     assert bytes(moe.get_plan(p, num_sms=152)) == bytes(base)  # restored on exit
     for bad in (dict(bn_max=24), dict(bn_max=512), dict(slot_kb=3), dict(pair=2), dict(splits=17),
-                dict(stages=1), dict(conv_groups=4)):
+                dict(stages=1), dict(conv_groups=4), dict(epi_warps=6)):
         with pytest.raises(moe.MoEError):
             moe.set_tuning(**bad)
         assert bytes(moe.get_plan(p, num_sms=152)) == bytes(base)  # a rejected call changes nothing
     with pytest.raises(ValueError):
         moe.set_tuning(no_such_knob=1)
+
+
+def test_epilogue_warp_override(lib):
+    from synth import SHAPES
+    # eight epilogue warps where a kernel has them (int4 / int8 CTA pairs with two
+    # converter groups and whole-stage slots); a one-CTA int4 plan keeps four
+    big = moe.problem(4096, 7168, 256, 256, 8, scoring="sigmoid", n_group=8, topk_group=4, wdtype="int4")
+    with moe.tuning(epi_warps=8):
+        pl = _check_plan(SHAPES["dsv3_tp8"], moe.get_plan(big, num_sms=152))
+        assert pl.pair_down == 1 and pl.epi_warps_down == 8
+        small = moe.problem(4, 7168, 256, 256, 8, scoring="sigmoid", n_group=8, topk_group=4, wdtype="int4")
+        ps = moe.get_plan(small, num_sms=152)
+        assert ps.pair_up == 0 and ps.epi_warps_up == 4
+    bf = moe.problem(4096, 4096, 14336, 8, 2, wdtype="bf16")
+    with moe.tuning(epi_warps=4):
+        assert moe.get_plan(bf, num_sms=152).epi_warps_up == 4
+    pl = moe.get_plan(bf, num_sms=152)
+    assert pl.epi_warps_up == 8 and pl.stages_up >= 6  # the second staging half leaves the ring depth

@@ -230,8 +230,9 @@ def test_full_size_sampled(dev, name, T):
 # library's planner overrides (moe_set_tuning): the single-CTA
 # bf16/fp8 kernel (no CTA pairs), and the int4 / int8 kernel's pair / non-pair,
 # one / two MMA-issuer, two-k-block-slot, three-converter-group, k-split /
-# alternating-stage and per-64/16-row token box (no full box) modes, and the
-# weight-block-major unit order.
+# alternating-stage and per-64/16-row token box (no full box) modes, the
+# weight-block-major unit order, and four epilogue warps where the planner takes
+# eight (bf16 / fp8 pairs) or eight where it takes four.
 @pytest.mark.parametrize("name,knobs", [
     ("mixtral", {"pair": 0}),
     ("qwen2", {"pair": 0}),
@@ -277,6 +278,15 @@ def test_full_size_sampled(dev, name, T):
     ("mixtral", {"unit_order": 2, "pair": 0}),
     ("dsv3", {"unit_order": 0}),
     ("qwen2_dyn", {"unit_order": 0}),
+    ("mixtral", {"epi_warps": 4}),
+    ("qwen2_dyn", {"epi_warps": 4}),
+    ("mixtral", {"pair": 0, "epi_warps": 8}),
+    ("qwen2", {"pair": 0, "epi_warps": 8}),
+    ("dsv3", {"pair": 1, "dual": 1, "epi_warps": 8}),
+    ("dsv3", {"pair": 1, "dual": 0, "epi_warps": 8}),
+    ("dsv3_awq", {"pair": 1, "dual": 1, "ksplit": 1, "epi_warps": 8}),
+    ("mixtral_w8", {"pair": 1, "epi_warps": 8}),
+    ("mixtral_w8_zp", {"pair": 1, "dual": 1, "epi_warps": 8}),
 ])
 def test_forced_kernel_variants(dev, name, knobs):
     shape = small(name)
@@ -284,6 +294,8 @@ def test_forced_kernel_variants(dev, name, knobs):
         plan = moe.get_plan(gc.lib_problem(shape, 300))
         if "slot_kb" in knobs:
             assert plan.slot_kb_up == knobs["slot_kb"]
+        if "epi_warps" in knobs:
+            assert plan.epi_warps_up == knobs["epi_warps"] and plan.epi_warps_down == knobs["epi_warps"]
         if "dual" in knobs:  # tiles of <= 64 tokens
             plan = moe.get_plan(gc.lib_problem(shape, 37))
             want = 2 if knobs["dual"] == 1 else 1
@@ -292,30 +304,34 @@ def test_forced_kernel_variants(dev, name, knobs):
             gc.full_check(shape, T, dev)
 
 
-@pytest.mark.parametrize("name,bn", [("dsv3", 256), ("dsv3_awq", 192), ("mixtral_w8", 256),
-                                     ("mixtral_w8_zp", 160)])
-def test_converted_weights_wide_token_tiles(dev, name, bn):
+@pytest.mark.parametrize("name,bn,ew", [("dsv3", 256, 4), ("dsv3_awq", 192, 4), ("mixtral_w8", 256, 4),
+                                        ("mixtral_w8_zp", 160, 4), ("dsv3", 256, 8), ("dsv3_awq", 160, 8),
+                                        ("mixtral_w8", 192, 8)])
+def test_converted_weights_wide_token_tiles(dev, name, bn, ew):
     # int4 / int8 tiles of more than 128 tokens (CTA pairs, one MMA issuer, one
     # accumulator of up to 256 columns beside two whole-stage slots): about 250
-    # rows per expert, so tiles run full and ragged
+    # rows per expert, so tiles run full and ragged; four or eight epilogue warps
     shape = small(name)
     T = 2000 if shape.top_k == 8 and shape.E == 64 else 1000
-    with moe.tuning(bn_max=bn, pair=1):
+    with moe.tuning(bn_max=bn, pair=1, epi_warps=ew):
         plan = moe.get_plan(gc.lib_problem(shape, T))
         assert plan.bn_max_up == bn and plan.pair_up == 1 and plan.issuers_up == 1
+        assert plan.epi_warps_up == ew
         r = gc.full_check(shape, T, dev)
     assert r["counts"].max() > 128
 
 
-@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("pair,ew", [(0, 4), (1, 4), (1, 8)])
 @pytest.mark.parametrize("splits", [None, 3])
-def test_two_issuers_short_k_ranges(dev, splits, pair):
+def test_two_issuers_short_k_ranges(dev, splits, pair, ew):
     # k ranges that leave the second MMA-issuing thread (k-blocks 2 and 3 of a
     # stage) without work in a stage (split-K tails of one or two k-blocks) or in
     # a whole unit (the down GEMM's K = 128 is two k-blocks), on one CTA and on
     # CTA pairs (whose arrivals then go to both CTAs)
     shape = dataclasses.replace(small("dsv3"), name="dsv3_short_k", I=128)
-    knobs = dict(pair=pair, dual=1) if splits is None else dict(pair=pair, dual=1, splits=splits)
+    knobs = dict(pair=pair, dual=1, epi_warps=ew)
+    if splits is not None:
+        knobs["splits"] = splits
     with moe.tuning(**knobs):
         for T in (1, 37):
             plan = moe.get_plan(gc.lib_problem(shape, T))

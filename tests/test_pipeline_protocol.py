@@ -78,13 +78,15 @@ class Resource:
 
 
 class Plan:
-    def __init__(self, ns, na, cg=2, sk=4, ks=False, dual=False, nbuf=2, ctas=1):
+    def __init__(self, ns, na, cg=2, sk=4, ks=False, dual=False, nbuf=2, ctas=1, ew=4):
         self.ns, self.na, self.cg, self.sk, self.ks = ns, na, cg, sk, ks
         self.dual, self.nbuf, self.ctas = dual, nbuf, ctas
+        self.ew = ew            # epilogue warps per CTA (each arrives on TEMPTY once per unit)
+        self.tempty_count = ew  # arrivals TEMPTY expects per CTA (the kernel: one per epilogue warp)
 
     def __repr__(self):
         return (f"Plan(ns={self.ns}, na={self.na}, cg={self.cg}, sk={self.sk}, ks={self.ks}, "
-                f"dual={self.dual}, nbuf={self.nbuf}, ctas={self.ctas})")
+                f"dual={self.dual}, nbuf={self.nbuf}, ctas={self.ctas}, ew={self.ew})")
 
 
 def kernel_accepts(pl):
@@ -134,7 +136,7 @@ class Sim:
         for a in range(pl.na):
             bar(("AFULL", a), conv_arrivals)            # the leader's
         for b in range(pl.nbuf):
-            bar(("TEMPTY", b), 4 * pl.ctas)             # the leader's
+            bar(("TEMPTY", b), pl.tempty_count * pl.ctas)  # the leader's
         self.res = {}
         self.mma_queue = {}     # issuer -> in-flight MMAs in issue order: (reads, writes)
         self.issued = {}        # issuer -> MMAs issued so far
@@ -251,7 +253,7 @@ class Sim:
             for g in range(pl.cg):
                 for w in range(4):
                     gens[("converter", c, g, w)] = self.converter(c, g, w)
-            for w in range(4):
+            for w in range(pl.ew):
                 gens[("epilogue", c, w)] = self.epilogue(c, w)
         for j in range(2 if pl.dual else 1):
             gens[("issuer", j)] = self.issuer(j)
@@ -419,6 +421,8 @@ def test_protocol_holds_for_every_accepted_plan(chunk):
     Plan(ns=4, na=2, dual=True, nbuf=1, ctas=2),      # int4 CTA pair, 128-token tile
     Plan(ns=3, na=2, ks=True, ctas=2),                # int8 CTA pair, k-split ring
     Plan(ns=2, na=2, nbuf=1, ctas=2),                 # int4 CTA pair, 256-token tile, one issuer
+    Plan(ns=2, na=2, nbuf=1, ctas=2, ew=8),           # the same, eight epilogue warps per CTA
+    Plan(ns=4, na=2, dual=True, nbuf=1, ctas=2, ew=8),  # int4 CTA pair, 128-token tile, eight epilogue warps
     Plan(ns=6, na=5, cg=3, sk=2, ctas=2),             # three groups, two-k-block slots
 ])
 def test_protocol_holds_for_planner_shapes_over_many_schedules(pl):
@@ -676,8 +680,10 @@ def test_kernel_bookkeeping_matches_the_model():
 # both CTAs (EMPTY) and hand the accumulator to both CTAs' epilogues (TFULL).
 
 class DenseSim(Sim):
-    def __init__(self, ns, ctas, units, rng):
-        self.pl = Plan(ns, 2, ctas=ctas)
+    def __init__(self, ns, ctas, units, rng, ew=4, tempty_count=None):
+        self.pl = Plan(ns, 2, ctas=ctas, ew=ew)
+        if tempty_count is not None:
+            self.pl.tempty_count = tempty_count
         self.units, self.rng = units, rng
         self.kblocks = [(u, kb) for u, nkb in enumerate(units) for kb in range(nkb)]
         self.bars = {}
@@ -689,7 +695,7 @@ class DenseSim(Sim):
         for st in range(ns):
             self.bars[("FULL", st)] = Barrier(("FULL", st), 1 + ctas)   # leader's
         for b in range(2):
-            self.bars[("TEMPTY", b)] = Barrier(("TEMPTY", b), 4 * ctas)
+            self.bars[("TEMPTY", b)] = Barrier(("TEMPTY", b), self.pl.tempty_count * ctas)
         self.res, self.mma_queue, self.issued, self.completed, self.commits = {}, {}, {}, {}, {}
         self.async_ops = []
 
@@ -697,7 +703,7 @@ class DenseSim(Sim):
         gens = {}
         for c in range(self.pl.ctas):
             gens[("producer", c)] = self.dense_producer(c)
-            for w in range(4):
+            for w in range(self.pl.ew):
                 gens[("epilogue", c, w)] = self.dense_epilogue(c, w)
         gens[("issuer", 0)] = self.dense_issuer()
         return gens
@@ -737,15 +743,29 @@ def _dense_units(rng):
     return [rng.choice([1, 2, 3, 5, 8, 13, 28, 56]) for _ in range(rng.randint(1, 6))]
 
 
+@pytest.mark.parametrize("ew", [4, 8])
 @pytest.mark.parametrize("ctas", [1, 2])
-def test_dense_protocol_holds(ctas):
+def test_dense_protocol_holds(ctas, ew):
     for ns in range(2, 9):
         for seed in range(6):
             rng = random.Random(100 * ns + seed)
             try:
-                DenseSim(ns, ctas, _dense_units(rng), rng).run()
+                DenseSim(ns, ctas, _dense_units(rng), rng, ew=ew).run()
             except ProtocolError as e:
-                raise ProtocolError(f"ns={ns}, ctas={ctas}, seed {seed}: {e}") from None
+                raise ProtocolError(f"ns={ns}, ctas={ctas}, ew={ew}, seed {seed}: {e}") from None
+
+
+def test_dense_model_catches_an_accumulator_freed_by_half_the_epilogue():
+    # eight epilogue warps but TEMPTY counting four arrivals per CTA: the issuer
+    # may overwrite an accumulator that the slower four warps still read
+    failures = 0
+    for seed in range(40):
+        rng = random.Random(seed)
+        try:
+            DenseSim(4, 2, _dense_units(rng), rng, ew=8, tempty_count=4).run()
+        except ProtocolError:
+            failures += 1
+    assert failures > 0
 
 
 def test_dense_model_catches_a_stage_freed_before_its_mmas_complete(monkeypatch):
