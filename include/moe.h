@@ -297,7 +297,9 @@ const char* moe_status_string(moe_status_t s);
  * issue its MMAs in a CTA (1, or for int4 / int8 tiles of at most 64 tokens
  * on one CTA 2, each its half of the reduction into its own accumulator); for
  * int4 / int8 the converter warp groups (2 or 3) per GEMM; per GEMM the warps
- * that drain its accumulators (4, or 8 taking alternate 32-token columns). */
+ * that drain its accumulators (4, or 8 taking alternate 32-token columns) and
+ * the accumulator buffers in tensor memory (2 let a unit's epilogue overlap the
+ * next unit's MMAs; 1 where the tile leaves no room for a second). */
 typedef struct {
   int32_t bn_max_up, splits_up, stages_up, astages_up, smem_up;
   int32_t bn_max_down, splits_down, stages_down, astages_down, smem_down;
@@ -307,6 +309,7 @@ typedef struct {
   int32_t issuers_up, issuers_down;
   int32_t conv_groups_up, conv_groups_down;  /* int4 / int8: converter warp groups (else 0) */
   int32_t epi_warps_up, epi_warps_down;      /* epilogue warps per CTA (4 or 8) */
+  int32_t acc_bufs_up, acc_bufs_down;        /* accumulator buffers (1 or 2) */
 } moe_plan_t;
 
 /* Planner overrides, for tests and benchmarks that want a kernel variant the
@@ -334,13 +337,16 @@ typedef struct {
  *   epi_warps   4 or 8 warps draining the accumulators (8: bf16 / fp8, and
  *               int4 / int8 on CTA pairs with two converter groups and
  *               four-k-block slots; elsewhere 4 is kept)
+ *   acc_bufs    int4 / int8 tiles of 129-192 tokens: 2 = two accumulator
+ *               buffers beside one converted-weight slot that both converter
+ *               groups fill, 1 = one buffer beside two slots (the default)
  * The overrides apply to every later plan of the process (all threads) until
  * the next call; NULL restores the planner's choices.  Values outside those
  * ranges return MOE_ERR_INVALID_ARG and change nothing.  The library never
  * reads tuning from the environment. */
 typedef struct {
   int32_t bn_max, stages, splits, pair, conv_groups, slot_kb, ksplit, dual, full_box, w_stream, unit_order;
-  int32_t epi_warps;
+  int32_t epi_warps, acc_bufs;
 } moe_tuning_t;
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t);

@@ -61,13 +61,14 @@ class Plan(ctypes.Structure):
                 ("pair_up", ctypes.c_int32), ("pair_down", ctypes.c_int32),
                 ("issuers_up", ctypes.c_int32), ("issuers_down", ctypes.c_int32),
                 ("conv_groups_up", ctypes.c_int32), ("conv_groups_down", ctypes.c_int32),
-                ("epi_warps_up", ctypes.c_int32), ("epi_warps_down", ctypes.c_int32)]
+                ("epi_warps_up", ctypes.c_int32), ("epi_warps_down", ctypes.c_int32),
+                ("acc_bufs_up", ctypes.c_int32), ("acc_bufs_down", ctypes.c_int32)]
 
 
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("bn_max", "stages", "splits", "pair", "conv_groups", "slot_kb",
                                              "ksplit", "dual", "full_box", "w_stream", "unit_order",
-                                             "epi_warps")]
+                                             "epi_warps", "acc_bufs")]
 
 
 TUNING_KNOBS = tuple(n for n, _ in Tuning._fields_)

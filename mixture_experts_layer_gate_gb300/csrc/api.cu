@@ -138,7 +138,7 @@ struct GemmPlan {
 // field of -1 leaves the planner's choice).  Nothing is read from the
 // environment: a process gets these only by calling moe_set_tuning.
 std::mutex g_tuning_mu;
-moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+moe_tuning_t g_tuning = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
 
 moe_tuning_t current_tuning() {
   std::lock_guard<std::mutex> lock(g_tuning_mu);
@@ -259,6 +259,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
   // roofline better for Mixtral, Qwen2 and Scout at 64-4096 tokens, with no
   // batch size slower, against 64- and 16-row boxes for an expert's last tile.
   g.full_box = knob(tu.full_box, 1) != 0 ? 1 : 0;
+  bool one_slot = false;  // int4 / int8: two wide accumulators beside one converted slot
   if (converts(wk)) {
     // TMEM: two accumulators of acc_cols columns, then converted slots of
     // slot_kb k-blocks (32 columns each).  A converter group that fills the
@@ -276,10 +277,26 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     // converted weight tile then serves up to 256 tokens, so an expert with
     // 129..256 rows is converted once instead of twice, and the MMAs of a
     // stage (M = 256, N up to 256) outlast its conversion.
+    // A second issuer that costs the second accumulator buffer (tiles of 65-128
+    // tokens) only where units carry >= 16 k-blocks: with fewer, a unit's MMAs
+    // are shorter than its epilogue, which must then overlap the next unit's
+    // MMAs (DeepSeek-V3 TP8 slice, down GEMM with K = 256, T = 2048: 0.446 ms
+    // with two issuers and one buffer, 0.365 ms with one issuer and two).
+    // Tiles of 129-192 tokens can instead take two accumulator buffers beside a
+    // single whole-stage slot that both converter groups fill (k-split; tuning
+    // only): each stage's conversion then waits for the previous stage's MMAs.
+    // On short-K units (the DeepSeek-V3 TP8 down GEMM, K = 256, T = 4096) it
+    // measured no faster (0.471 vs 0.467 ms), on long ones far slower.
+    const bool dual_pays = g.acc_cols <= 64 || g.KB / g.P >= 16;
     const int dual_env = knob(tu.dual, -1);
+    const int ab_env = knob(tu.acc_bufs, 0);
     if (g.acc_cols > 128) {
       g.acc_bufs = 1;
-    } else if (dual_env == 1 || (dual_env != 0 && dual_fit)) {
+      if (g.acc_cols <= 192 && ab_env == 2) {
+        g.acc_bufs = 2;
+        one_slot = true;
+      }
+    } else if (dual_env == 1 || (dual_env != 0 && dual_fit && dual_pays)) {
       g.dual = 1;
       g.acc_bufs = g.acc_cols <= 64 ? 2 : 1;
     }
@@ -302,6 +319,11 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     if ((sk_env == 2 || sk_env == 4) && !g.dual && slots_fit(sk_env) >= slots_needed(sk_env)) g.slot_kb = sk_env;
     if (slots_fit(g.slot_kb) < slots_needed(g.slot_kb)) g.conv_groups = 2;  // 3 groups do not fit
     g.astages = slots_fit(g.slot_kb);
+    if (one_slot) {
+      g.conv_groups = 2;
+      g.slot_kb = kSuper;
+      g.astages = 1;
+    }
     per_stage = static_cast<size_t>(raw_stage_bytes(wk)) + 4 * static_cast<size_t>(g.pair ? g.bn_max / 2 : g.bn_max) * 128 + 16;
     cap = kMaxStagesInt4;
   } else {
@@ -337,7 +359,7 @@ GemmPlan plan_gemm(const moe_problem_t& p, bool up, int sms) {
     const int alt = g.stages - g.stages % g.conv_groups;
     const int ks_env = knob(tu.ksplit, -1);
     const bool can_ks = g.conv_groups == 2 && g.slot_kb == kSuper;
-    g.ksplit = (can_ks && (ks_env == 1 || (ks_env != 0 && alt < 4 && g.stages > alt))) ? 1 : 0;
+    g.ksplit = (can_ks && (one_slot || ks_env == 1 || (ks_env != 0 && alt < 4 && g.stages > alt))) ? 1 : 0;
     if (!g.ksplit) g.stages = alt;
   }
   // whole-stage slots: converters wait on the stage ring for slot reuse, which
@@ -857,11 +879,13 @@ moe_status_t moe_get_plan_for_sms(const moe_problem_t* p, int32_t num_sms, moe_p
   plan->conv_groups_down = d.conv_groups;
   plan->epi_warps_up = u.epi_warps;
   plan->epi_warps_down = d.epi_warps;
+  plan->acc_bufs_up = u.acc_bufs;
+  plan->acc_bufs_down = d.acc_bufs;
   return MOE_OK;
 }
 
 moe_status_t moe_set_tuning(const moe_tuning_t* t) {
-  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  moe_tuning_t v = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
   if (t != nullptr) {
     v = *t;
     auto ok = [](int32_t x, int32_t lo, int32_t hi) { return x == -1 || (x >= lo && x <= hi); };
@@ -869,7 +893,7 @@ moe_status_t moe_set_tuning(const moe_tuning_t* t) {
         !ok(v.splits, 1, kMaxSplits) || !ok(v.pair, 0, 1) || !ok(v.conv_groups, 2, 3) ||
         !(v.slot_kb == -1 || v.slot_kb == 2 || v.slot_kb == 4) || !ok(v.ksplit, 0, 1) || !ok(v.dual, 0, 1) ||
         !ok(v.full_box, 0, 1) || !ok(v.w_stream, 0, 1) || !ok(v.unit_order, 0, 2) ||
-        !(v.epi_warps == -1 || v.epi_warps == 4 || v.epi_warps == 8))
+        !(v.epi_warps == -1 || v.epi_warps == 4 || v.epi_warps == 8) || !ok(v.acc_bufs, 1, 2))
       return MOE_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_tuning_mu);

@@ -45,8 +45,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layout_matches_header():
     assert ctypes.sizeof(binding.Problem) == 52
     assert ctypes.sizeof(binding.WeightsStruct) == 64
-    assert ctypes.sizeof(binding.Plan) == 84     # 21 four-byte fields
-    assert ctypes.sizeof(binding.Tuning) == 48   # 12 four-byte fields
+    assert ctypes.sizeof(binding.Plan) == 92     # 23 four-byte fields
+    assert ctypes.sizeof(binding.Tuning) == 52   # 13 four-byte fields
 
 
 def test_status_strings(lib):
@@ -177,22 +177,27 @@ def _check_plan(shape, pl):
             sk = getattr(pl, f"slot_kb_{side}")
             assert sk in (2, 4) and (bn <= 128 or getattr(pl, f"pair_{side}") == 1)
             acc = (bn + 31) // 32 * 32
-            # one buffer above 128 columns (one issuer) or with two issuers above 64
-            bufs = 1 if acc > 128 else (2 if issuers == 1 or acc <= 64 else 1)
+            bufs = getattr(pl, f"acc_bufs_{side}")
             if acc > 128:
+                # one issuer; one buffer beside two slots, or (short-K units, <= 192
+                # columns) two buffers beside one slot that both groups fill
                 assert issuers == 1
-            assert 2 <= ast <= 7 and issuers * bufs * acc + 32 * sk * ast <= 512
-            # a ring of g converter groups needs (g - 1) * 4 / sk + 1 slots and a
-            # stage count that is a multiple of g; g = 2 always satisfies both here
-            assert ast >= 4 // sk + 1
+                assert bufs == 1 or (bufs == 2 and ast == 1 and acc <= 192 and sk == 4)
+            else:
+                # two buffers, or one with two issuers above 64 columns
+                assert bufs == (2 if issuers == 1 or acc <= 64 else 1)
+            assert 1 <= ast <= 7 and issuers * bufs * acc + 32 * sk * ast <= 512
+            # a ring of g converter groups alternating stages needs (g - 1) * 4 / sk + 1
+            # slots and a stage count that is a multiple of g (one slot: k-split)
+            assert ast >= 4 // sk + 1 or ast == 1
             if sk == 4:
                 # whole-stage slots reuse the stage ring's barriers; an odd depth only
                 # with both groups converting every stage (k-split, for a shallow ring)
-                assert st >= ast and (st % 2 == 0 or st == 3)
+                assert st >= ast and (st % 2 == 0 or st == 3 or ast == 1)
             else:
                 assert st % 2 == 0 or st % 3 == 0
             cg = getattr(pl, f"conv_groups_{side}")
-            assert cg in (2, 3) and ast >= (cg - 1) * (4 // sk) + 1
+            assert cg in (2, 3) and (ast >= (cg - 1) * (4 // sk) + 1 or (ast == 1 and cg == 2))
             if issuers == 2:  # whole-stage slots
                 assert sk == 4
             if cg == 3 and issuers == 2:  # int4 tiles of <= 32 tokens on one CTA
@@ -214,8 +219,11 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             bn = getattr(pl, f"bn_max_{side}")
             fb = shape.I // 64 if side == "up" else shape.H // 128
             small = shape.wdtype in ("int4", "int8") and bn <= 32
-            # two issuers share TMEM with two buffers of partials: tiles of <= 128 tokens
-            two = (shape.wdtype == "int4" and bn <= 128) or (shape.wdtype == "int8" and small)
+            # two issuers share TMEM with two buffers of partials: tiles of <= 128 tokens;
+            # above 64 tokens (one buffer of partials) only for units of >= 16 k-blocks
+            kb = (shape.H if side == "up" else shape.I) // 64 // getattr(pl, f"splits_{side}")
+            two = (shape.wdtype == "int4" and bn <= 128 and (bn <= 64 or kb >= 16)) or \
+                  (shape.wdtype == "int8" and small)
             assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not small else 0)
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
             # eight epilogue warps on bf16 / fp8 CTA pairs, four elsewhere

@@ -304,19 +304,29 @@ def test_forced_kernel_variants(dev, name, knobs):
             gc.full_check(shape, T, dev)
 
 
-@pytest.mark.parametrize("name,bn,ew", [("dsv3", 256, 4), ("dsv3_awq", 192, 4), ("mixtral_w8", 256, 4),
-                                        ("mixtral_w8_zp", 160, 4), ("dsv3", 256, 8), ("dsv3_awq", 160, 8),
-                                        ("mixtral_w8", 192, 8)])
-def test_converted_weights_wide_token_tiles(dev, name, bn, ew):
-    # int4 / int8 tiles of more than 128 tokens (CTA pairs, one MMA issuer, one
-    # accumulator of up to 256 columns beside two whole-stage slots): about 250
-    # rows per expert, so tiles run full and ragged; four or eight epilogue warps
+@pytest.mark.parametrize("name,bn,ew,ab", [("dsv3", 256, 4, None), ("dsv3_awq", 192, 4, None),
+                                           ("mixtral_w8", 256, 4, None), ("mixtral_w8_zp", 160, 4, None),
+                                           ("dsv3", 256, 8, None), ("dsv3_awq", 160, 8, None),
+                                           ("mixtral_w8", 192, 8, None), ("dsv3_awq", 192, 4, 2),
+                                           ("dsv3", 192, 4, 2), ("mixtral_w8_zp", 160, 8, 2)])
+def test_converted_weights_wide_token_tiles(dev, name, bn, ew, ab):
+    # int4 / int8 tiles of more than 128 tokens (CTA pairs, one MMA issuer): one
+    # accumulator of up to 256 columns beside two whole-stage slots, or (forced)
+    # two of up to 192 columns beside one slot that both converter groups fill;
+    # about 250 rows per expert, so tiles run full and ragged; four or eight
+    # epilogue warps
     shape = small(name)
     T = 2000 if shape.top_k == 8 and shape.E == 64 else 1000
-    with moe.tuning(bn_max=bn, pair=1, epi_warps=ew):
+    knobs = dict(bn_max=bn, pair=1, epi_warps=ew)
+    if ab is not None:
+        knobs["acc_bufs"] = ab
+    with moe.tuning(**knobs):
         plan = moe.get_plan(gc.lib_problem(shape, T))
         assert plan.bn_max_up == bn and plan.pair_up == 1 and plan.issuers_up == 1
         assert plan.epi_warps_up == ew
+        assert plan.acc_bufs_up == (ab or 1) and plan.acc_bufs_down == (ab or 1)
+        if ab == 2:
+            assert plan.astages_up == 1 and plan.astages_down == 1
         r = gc.full_check(shape, T, dev)
     assert r["counts"].max() > 128
 

@@ -392,7 +392,7 @@ def _accepted_plans():
                     for dual in (False, True):
                         for nbuf in (1, 2):
                             for ns in range(2, 9):
-                                for na in range(2, 8):
+                                for na in range(1, 8):
                                     pl = Plan(ns, na, cg, sk, ks, dual, nbuf, ctas)
                                     if kernel_accepts(pl):
                                         plans.append(pl)
@@ -422,6 +422,7 @@ def test_protocol_holds_for_every_accepted_plan(chunk):
     Plan(ns=3, na=2, ks=True, ctas=2),                # int8 CTA pair, k-split ring
     Plan(ns=2, na=2, nbuf=1, ctas=2),                 # int4 CTA pair, 256-token tile, one issuer
     Plan(ns=2, na=2, nbuf=1, ctas=2, ew=8),           # the same, eight epilogue warps per CTA
+    Plan(ns=3, na=1, ks=True, nbuf=2, ctas=2),        # short-K units, 192-token tiles: two buffers, one slot
     Plan(ns=4, na=2, dual=True, nbuf=1, ctas=2, ew=8),  # int4 CTA pair, 128-token tile, eight epilogue warps
     Plan(ns=6, na=5, cg=3, sk=2, ctas=2),             # three groups, two-k-block slots
 ])
