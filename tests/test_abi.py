@@ -219,12 +219,14 @@ def test_plans_respect_hardware_and_pipeline_invariants(lib, sms):
             bn = getattr(pl, f"bn_max_{side}")
             fb = shape.I // 64 if side == "up" else shape.H // 128
             small = shape.wdtype in ("int4", "int8") and bn <= 32
+            kb = (shape.H if side == "up" else shape.I) // 64 // getattr(pl, f"splits_{side}")
+            # ... except units of <= 8 k-blocks once the batch has >= 64 rows
+            short_units = kb <= 8 and p.T * shape.top_k >= 64
             # two issuers share TMEM with two buffers of partials: tiles of <= 128 tokens;
             # above 64 tokens (one buffer of partials) only for units of >= 16 k-blocks
-            kb = (shape.H if side == "up" else shape.I) // 64 // getattr(pl, f"splits_{side}")
             two = (shape.wdtype == "int4" and bn <= 128 and (bn <= 64 or kb >= 16)) or \
                   (shape.wdtype == "int8" and small)
-            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and not small else 0)
+            assert getattr(pl, f"pair_{side}") == (1 if fb % 2 == 0 and (not small or short_units) else 0)
             assert getattr(pl, f"issuers_{side}") == (2 if two else 1)
             # eight epilogue warps on bf16 / fp8 CTA pairs, four elsewhere
             conv = shape.wdtype in ("int4", "int8")
