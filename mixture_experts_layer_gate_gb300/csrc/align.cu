@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(AlignArgs a
   pdl_trigger();
   if (threadIdx.x < a.k) rows[threadIdx.x] = a.inv[static_cast<size_t>(t) * a.k + threadIdx.x];
   __syncthreads();
-  gather_token<FP8>(a, t, rows, threadIdx.x, kGatherThreads);
+  gather_token<FP8>(a, t, rows, 0, a.H / 8, threadIdx.x, kGatherThreads);
 }
 
 __global__ void __launch_bounds__(256)

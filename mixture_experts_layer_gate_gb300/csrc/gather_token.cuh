@@ -9,15 +9,17 @@
 
 namespace moe {
 
-// rows[j] = permuted row of slot t*k + j; run by `nthreads` threads, thread `tid`.
+// rows[j] = permuted row of slot t*k + j; run by `nthreads` threads, thread
+// `tid`, over the 8-element column groups [c0, c1) of the row (0 .. H / 8 for
+// the whole row).
 template <bool FP8>
-__device__ __forceinline__ void gather_token(const AlignArgs& a, int t, const int* rows, int tid, int nthreads) {
+__device__ __forceinline__ void gather_token(const AlignArgs& a, int t, const int* rows, int c0, int c1, int tid,
+                                             int nthreads) {
   const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.x) +
                                                     static_cast<size_t>(t) * a.H);
-  const int nvec = a.H / 8;
   if (!FP8) {
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.x_perm);
-    for (int c = tid; c < nvec; c += nthreads) {
+    for (int c = c0 + tid; c < c1; c += nthreads) {
       const uint4 v = __ldg(src + c);
       for (int j = 0; j < a.k; ++j)
         reinterpret_cast<uint4*>(dst + static_cast<size_t>(rows[j]) * a.H)[c] = v;
@@ -25,7 +27,7 @@ __device__ __forceinline__ void gather_token(const AlignArgs& a, int t, const in
   } else {
     const float s = a.a1[0];
     uint8_t* dst = static_cast<uint8_t*>(a.x_perm);
-    for (int c = tid; c < nvec; c += nthreads) {
+    for (int c = c0 + tid; c < c1; c += nthreads) {
       const uint4 v = __ldg(src + c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t q[2];

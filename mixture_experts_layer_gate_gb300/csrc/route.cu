@@ -4,8 +4,10 @@
 // A decode step would otherwise pay four dependent launches for a few
 // microseconds of work.  Every CTA computes the whole routing in its own shared
 // memory (at most kRouteMaxSlots slots: cheaper than waiting for another CTA),
-// CTA 0 alone writes ids, weights, counts, offsets, perm and inv, and CTA b
-// gathers tokens b, b + G, ...  The gate is the same per-token routine as
+// CTA 0 alone writes ids, weights, counts, offsets, perm and inv, and the
+// gather is split into T x `chunks` pieces (a token's row in `chunks` column
+// ranges, so a batch of a few tokens still spreads its k row copies over many
+// SMs), CTA b taking pieces b, b + G, ...  The gate is the same per-token routine as
 // gate_topk_kernel, the ranking gives the same unique stable order as
 // align_count + align_scatter and the gather is the same per-token copy, so the
 // results are bit-identical to that path.
@@ -22,7 +24,7 @@ static_assert(kRouteThreads >= kRouteMaxSlots, "one slot per thread");
 
 template <int EPL, bool FP8>
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_small_kernel(GateArgs g, AlignArgs a, int scratch_bytes) {
+    route_small_kernel(GateArgs g, AlignArgs a, int scratch_bytes, int chunks) {
   extern __shared__ __align__(16) unsigned char route_smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E;
@@ -124,9 +126,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncthreads();
 
-  // gather: this CTA's tokens, each to the rows its k slots landed on
-  for (int t = blockIdx.x; t < g.T; t += gridDim.x)
-    gather_token<FP8>(a, t, s_pos + static_cast<size_t>(t) * a.k, tid, kRouteThreads);
+  // gather: this CTA's pieces (token, column range), each to the rows its k
+  // slots landed on
+  const int nvec = a.H / 8;
+  for (int w = blockIdx.x; w < g.T * chunks; w += gridDim.x) {
+    const int t = w / chunks, c = w - t * chunks;
+    gather_token<FP8>(a, t, s_pos + static_cast<size_t>(t) * a.k, c * nvec / chunks, (c + 1) * nvec / chunks, tid,
+                      kRouteThreads);
+  }
 }
 
 template <int EPL>
@@ -148,17 +155,26 @@ cudaError_t launch_route(const GateArgs& g, const AlignArgs& a, cudaStream_t s) 
     if (err != cudaSuccess) return err;
     configured = dev;
   }
-  // one CTA per token up to the SM count: every CTA repeats the routing, so
-  // more CTAs only shorten the gather
+  // up to one CTA per SM: every CTA repeats the routing, so more CTAs only
+  // shorten the gather.  Batches of <= 4 tokens split a token's row into
+  // column ranges of at least 64 x 8 elements until the pieces fill the SMs
+  // (DeepSeek-V3 shapes, T = 1-4: 1-3% faster layer); larger ones keep one
+  // piece per token, since routing CTAs beyond the tokens' count hold SMs the
+  // next GEMM's prologue could use (TP8 slice, T = 64: 1.3% slower split).
   int sms = 0;
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
-  const int grid = g.T < sms ? g.T : sms;
+  int chunks = g.T <= 4 ? sms / g.T : 1;
+  const int max_chunks = a.H / (8 * 64);
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1) chunks = 1;
+  const int pieces = g.T * chunks;
+  const int grid = pieces < sms ? pieces : sms;
   if (a.fp8)
     return launch_pdl(route_small_kernel<EPL, true>, dim3(grid), dim3(kRouteThreads), smem, s, g, a,
-                      static_cast<int>(scratch));
+                      static_cast<int>(scratch), chunks);
   return launch_pdl(route_small_kernel<EPL, false>, dim3(grid), dim3(kRouteThreads), smem, s, g, a,
-                    static_cast<int>(scratch));
+                    static_cast<int>(scratch), chunks);
 }
 
 }  // namespace
