@@ -435,6 +435,18 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Four 8 x 8 b16 matrices from shared memory, transposed: this thread's
+// address is row (lane % 8) of matrix lane / 8; register j receives elements
+// (2 (lane % 4), lane / 4) and (2 (lane % 4) + 1, lane / 4) of matrix j.
+__device__ __forceinline__ uint4 ldmatrix_x4_trans(uint32_t saddr) {
+  uint4 r;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(saddr)
+               : "memory");
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

@@ -324,6 +324,17 @@ __device__ __forceinline__ void load_weight_tile(const GemmMaps& maps, const Gem
 // (columns 2b and 2b + 1 times acc_cols) from two MMA-issuing threads, the
 // second written only for units of more than two k-blocks; the epilogue adds them;
 // the ring then has p.acc_bufs (1 or 2) buffers, else always 2.
+// Byte offset of 16-token half `c` of row h (output column) of the staged
+// 32 x 16 bf16 store tile: rows of 32 bytes, four to a 128-byte line, the
+// line's eight 16-byte units permuted by a line-dependent XOR so that the
+// rows' 16-byte stores (a quarter warp: 8 consecutive rows) and the transposing
+// reads (rows 2j, 2j + 1, 8 + 2j, ... 25 + 2j) fall on distinct bank groups.
+__device__ __forceinline__ uint32_t stg_swizzle(int h, int c) {
+  const int L = h >> 2;
+  const int g = (L & 1) ^ (4 * ((L >> 1) & 1)) ^ ((L >> 2) & 1);
+  return static_cast<uint32_t>(L * 128 + (((2 * (h & 3) + c) ^ g) << 4));
+}
+
 template <int WK, bool DUAL = false>
 __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* tile_base, const int* off,
                                              int units, int first, int stride, int pair_rank,
@@ -421,19 +432,28 @@ __device__ __forceinline__ void run_epilogue(const GemmParams& p, const int* til
                 *reinterpret_cast<const uint4*>(stg + tok * 32 + half * 16);
         }
       } else if (p.epi == kEpiStore) {
+        // Lane h packs its column's token pairs to bf16x2 and stages them as
+        // row h of a 32 x 16 bf16 tile (two 16-byte stores); a transposing
+        // ldmatrix then hands lane l the 8 consecutive outputs 8 (l % 4) .. +7
+        // of token l / 4 (and l / 4 + 8), one 16-byte store each.  The tile is
+        // swizzled so that neither the stores nor the reads conflict on banks.
+        uint32_t w[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          reinterpret_cast<__nv_bfloat16*>(stg)[c * 32 + lane] =
-              __float2bfloat16_rn(__uint_as_float(v[c]) * sc);
+        for (int i = 0; i < 8; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * sc, __uint_as_float(v[2 * i + 1]) * sc);
+        *reinterpret_cast<uint4*>(stg + stg_swizzle(lane, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(stg + stg_swizzle(lane, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         __syncwarp();
-        const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32;
+        // lane l addresses row l % 8 of matrix l / 8: output column hr
+        const int mj = lane >> 3, mi = lane & 7;
+        const int hr = (mi >> 1) * 8 + 2 * mj + (mi & 1);
+        const size_t col = static_cast<size_t>(t.fb) * 128 + q * 32 + 8 * (lane & 3);
 #pragma unroll
-        for (int i = lane; i < 64; i += 32) {
-          const int tok = i >> 2, part = i & 3;
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint4 r = ldmatrix_x4_trans(smem_u32(stg + stg_swizzle(hr, hf)));
+          const int tok = hf * 8 + (lane >> 2);
           if (tok < ntok)
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld +
-                                      col + part * 8) =
-                *reinterpret_cast<const uint4*>(stg + tok * 64 + part * 16);
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (row + tok) * p.out_ld + col) = r;
         }
       } else {  // fp32 split-K partials
 #pragma unroll
