@@ -202,7 +202,8 @@ FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), 
               # tensor-parallel slices (I split over 2..8 ranks): short K in the down GEMM,
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
-              ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("scout_tp8", 32), ("scout_tp8", 4096)]
+              ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("dsv3_tp8", 2048), ("scout_tp8", 32),
+              ("scout_tp8", 4096)]
 
 
 def test_dynamic_scales_full_size_multi_tile_exact(dev):
@@ -310,6 +311,23 @@ def test_forced_kernel_variants(dev, name, knobs):
                                            ("mixtral_w8", 192, 8, None), ("dsv3_awq", 192, 4, 2),
                                            ("dsv3", 192, 4, 2), ("mixtral_w8_zp", 160, 8, 2)])
 def test_converted_weights_wide_token_tiles(dev, name, bn, ew, ab):
+    _wide_tiles(dev, name, bn, ew, ab)
+
+
+def test_short_k_units_one_issuer_two_buffers(dev):
+    # int4 tiles of 65-128 tokens: two MMA issuers for the gate_up (K = 1024,
+    # 16 k-blocks per unit), one issuer with two accumulator buffers for the
+    # down GEMM (K = 256, 4 k-blocks per unit)
+    shape = small("dsv3")
+    with moe.tuning(bn_max=128, pair=1):
+        for T in (300, 1000):
+            plan = moe.get_plan(gc.lib_problem(shape, T))
+            assert plan.bn_max_down == 128 and plan.issuers_up == 2 and plan.acc_bufs_up == 1
+            assert plan.issuers_down == 1 and plan.acc_bufs_down == 2
+            gc.full_check(shape, T, dev)
+
+
+def _wide_tiles(dev, name, bn, ew, ab):
     # int4 / int8 tiles of more than 128 tokens (CTA pairs, one MMA issuer): one
     # accumulator of up to 256 columns beside two whole-stage slots, or (forced)
     # two of up to 192 columns beside one slot that both converter groups fill;
