@@ -33,7 +33,25 @@ WORKLOADS = {"mixtral_tp2": "mixtral_8x7b_moe_layer_tp2_slice", "qwen2_tp4": "qw
              "mixtral": "mixtral_8x7b_moe_layer", "qwen2": "qwen2_57b_a14b_moe_layer_fp8",
              "dsv3": "deepseek_v3_moe_layer_int4", "dsv3_awq": "deepseek_v3_moe_layer_int4_zero_points",
              "qwen2_dyn": "qwen2_57b_a14b_moe_layer_fp8_dynamic_scales",
-             "mixtral_w8": "mixtral_8x7b_moe_layer_int8", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer"}
+             "mixtral_w8": "mixtral_8x7b_moe_layer_int8", "scout": "llama4_scout_moe_layer", "tiny": "tiny_moe_layer",
+             "dsv3_paired": "deepseek_v3_moe_layer_int4_paired_codes",
+             "dsv3_awq_paired": "deepseek_v3_moe_layer_int4_zero_points_paired_codes",
+             "dsv3_paired_tp8": "deepseek_v3_moe_layer_int4_paired_codes_tp8_slice"}
+
+
+def lib_wdtype(shape):
+    """The weight format the library is told: int4 shapes whose codes are
+    prepared once by moe_repack_int4 run as MOE_W_INT4_G128_PAIRED."""
+    return "int4_paired" if shape.int4_order == "paired" else shape.wdtype
+
+
+def lib_codes(moe, shape, w):
+    """w13 / w2 as the library reads them: the generated codes, or for the paired
+    format a copy prepared by moe_repack_int4 (one-time weight preparation, not
+    part of a step).  The oracle keeps reading the generated codes."""
+    if shape.int4_order == "paired":
+        return moe.repack_int4(w.w13), moe.repack_int4(w.w2)
+    return w.w13, w.w2
 
 
 def _peaks():
@@ -216,9 +234,10 @@ def run_ours(args):
     tok = make_tokens(shape, T, dev, seed=rank)
     p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                     renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
-                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=lib_wdtype(shape),
                     act_scale=shape.act_scale)
-    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+    codes = lib_codes(moe, shape, w)
+    wts = moe.Weights(codes[0], codes[1], w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
                        w.w13_zero, w.w2_zero)
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
@@ -389,7 +408,7 @@ def run_ours(args):
     if args.sweep and rank == 0:
         with ClockSampler(local) as sclk:
             sclk.mark(True)
-            sweep = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+            sweep = run_sweep(moe, torch, shape, w, codes, dev, stream, hbm, bf16_peak)
             sclk.mark(False)
         sweeps[args.config] = {"workload": WORKLOADS.get(args.config, args.config), "rows": sweep,
                                "clocks": sclk.summary(), "dominant_kernel_T4096": roof if T == 4096 else None}
@@ -408,7 +427,9 @@ def run_ours(args):
                    (f", {shape.n_group} groups keep {shape.topk_group}" if shape.n_group else ""),
                    "weights": {"bf16": "bf16", "fp8": "e4m3 per-expert scale" +
                                (", dynamic per-tensor activation scales" if shape.act_scale == "dynamic" else ""),
-                               "int4": "int4 group-128" + (" + zero points" if shape.zero_point else ""),
+                               "int4": "int4 group-128" + (" + zero points" if shape.zero_point else "") +
+                                       (", codes paired once by moe_repack_int4" if shape.int4_order == "paired"
+                                        else ""),
                                "int8": "int8 group-128" + (" + zero points" if shape.zero_point else "")}[shape.wdtype],
                    "global_batch": world * T, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": l2_note,
@@ -523,18 +544,20 @@ def sweep_config(moe, torch, cfg, dev, stream, local, hbm, bf16_peak, peak_src):
     from synth import SHAPES, make_tokens, make_weights
     shape = SHAPES[cfg]
     w = make_weights(shape, dev, seed=0)
+    codes = lib_codes(moe, shape, w)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark(True)
-        rows = run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak)
+        rows = run_sweep(moe, torch, shape, w, codes, dev, stream, hbm, bf16_peak)
         clk.mark(False)
     T = 4096
     tok = make_tokens(shape, T, dev, seed=0)
     p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                     renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
-                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                    routed_scaling_factor=shape.routed_scaling_factor, wdtype=lib_wdtype(shape),
                     act_scale=shape.act_scale)
-    wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale, w.w13_zero, w.w2_zero)
+    wts = moe.Weights(codes[0], codes[1], w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale, w.w13_zero,
+                      w.w2_zero)
     ws = moe.alloc_workspace(p, dev)
     ids = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
     tw = torch.empty((T, shape.top_k), dtype=torch.float32, device=dev)
@@ -553,12 +576,12 @@ def sweep_config(moe, torch, cfg, dev, stream, local, hbm, bf16_peak, peak_src):
         raise RuntimeError(f"device error in the {cfg} sweep")
     out = {"workload": WORKLOADS.get(cfg, cfg), "rows": rows, "clocks": clk.summary(),
            "dominant_kernel_T4096": roof}
-    del w, wts, ws, bufs, tok
+    del w, codes, wts, ws, bufs, tok
     torch.cuda.empty_cache()
     return out
 
 
-def run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak):
+def run_sweep(moe, torch, shape, w, codes, dev, stream, hbm, bf16_peak):
     """Per-T tokens/s and roofline fraction of the whole layer (CUDA graph, 20 reps;
     L2 flushed before each rep, outside its events, when the rep's bytes could stay in L2)."""
     from synth import T_SWEEP, make_tokens
@@ -569,9 +592,9 @@ def run_sweep(moe, torch, shape, w, dev, stream, hbm, bf16_peak):
         tok = make_tokens(shape, T, dev, seed=0)
         p = moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                         renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
-                        routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                        routed_scaling_factor=shape.routed_scaling_factor, wdtype=lib_wdtype(shape),
                     act_scale=shape.act_scale)
-        wts = moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+        wts = moe.Weights(codes[0], codes[1], w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
                        w.w13_zero, w.w2_zero)
         ws = moe.alloc_workspace(p, dev)
         out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)

@@ -66,7 +66,13 @@ typedef enum {
   MOE_ERR_TIMEOUT = 6           /* a kernel pipeline wait ran out (about 1 s) */
 } moe_status_t;
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_FP8_E4M3 = 1, MOE_W_INT4_G128 = 2, MOE_W_INT8_G128 = 3 } moe_wdtype_t;
+typedef enum {
+  MOE_W_BF16 = 0,
+  MOE_W_FP8_E4M3 = 1,
+  MOE_W_INT4_G128 = 2,
+  MOE_W_INT8_G128 = 3,
+  MOE_W_INT4_G128_PAIRED = 4 /* int4 codes prepared by moe_repack_int4 */
+} moe_wdtype_t;
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
 /* fp8 activation scales ("[kernel] introduce fused_moe_triton_splitk to
  * sglang" and the FBGEMM grouped-GEMM blog run fp8 W8A8 with per-tensor
@@ -106,6 +112,13 @@ typedef struct {
  *          the shape of the scales) the codes are unsigned 0..15 and
  *          value = (code - zero) * scale (asymmetric, AWQ-style).  Setting
  *          only one of the two is MOE_ERR_INVALID_ARG.
+ *   int4 paired (MOE_W_INT4_G128_PAIRED): the int4 tensors, scales and zero
+ *          points above, with the codes of every 4-byte word (8 consecutive K
+ *          indices k0..k7 of one row) reordered by moe_repack_int4: k0, k2,
+ *          k4, k6 in the nibbles of the low 16 bits and k1, k3, k5, k7 in
+ *          those of the high 16 bits, lowest first.  Results are those of the
+ *          same weights in the packed order; the converters need fewer
+ *          integer instructions per code.
  *   int8 : w13 uint8 [E, 2I, H], w2 uint8 [E, H, I], one code per byte;
  *          scales and zero points exactly as for int4 (zero points 0..255).
  *          Without zero points a byte is a signed two's-complement code
@@ -271,6 +284,19 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
  * launches recorded into a CUDA graph once (at capture); for measurement, e.g.
  * the launches of one moe_forward = the count's change across one call. */
 uint64_t moe_launch_count(void);
+
+/* Weight preparation for int4 ("[Kernel] add triton fused moe kernel for
+ * gptq/awq" streams group-quantised int4 codes packed two per byte; Marlin
+ * reorders such codes once at load time for its own kernel).  Rewrites
+ * n_bytes of int4 codes in the packed order (two codes per byte, the low
+ * nibble holding the even K index: w13 or w2 of MOE_W_INT4_G128) into the
+ * order of MOE_W_INT4_G128_PAIRED, a permutation inside every 4-byte word.
+ * codes and out are device pointers, 4-byte aligned, and may be equal (in
+ * place); n_bytes is a multiple of 4 (any int4 w13 / w2 tensor is).  Scales
+ * and zero points are not touched.  Asynchronous on `stream`.  Returns
+ * MOE_ERR_INVALID_ARG for a null or misaligned pointer or a size that is not
+ * a multiple of 4, MOE_OK for n_bytes == 0. */
+moe_status_t moe_repack_int4(const void* codes, void* out, size_t n_bytes, moe_stream_t stream);
 
 /* Dynamic fp8 scales (MOE_ACT_SCALE_DYNAMIC): device pointer to float [2]
  * inside the workspace ws, {a1, a2}.  moe_align_permute / moe_forward write

@@ -8,4 +8,4 @@ from .binding import (MoEError, Problem, Plan, Weights, MoELayer, load, problem,
                       align_permute_noalloc,
                       align_block_size, grouped_gemm_swiglu, grouped_gemm_down, unpermute_reduce,
                       forward, get_device_error, get_plan, dynamic_scales, launch_count, status_string, EXPORTED,
-                      LIB_PATH, set_tuning, tuning, TUNING_KNOBS)
+                      LIB_PATH, set_tuning, tuning, TUNING_KNOBS, repack_int4)

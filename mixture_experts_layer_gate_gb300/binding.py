@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BAD_INDEX", 6: "MOE_ERR_TIMEOUT"}
-WDTYPES = {"bf16": 0, "fp8": 1, "int4": 2, "int8": 3}
+WDTYPES = {"bf16": 0, "fp8": 1, "int4": 2, "int8": 3, "int4_paired": 4}
 ACT_SCALES = {"static": 0, "dynamic": 1}
 SCORING = {"softmax": 0, "sigmoid": 1}
 
@@ -24,7 +24,7 @@ EXPORTED = ("moe_scratch_size", "moe_workspace_size", "moe_padded_capacity", "mo
             "moe_align_permute", "moe_align_block_size", "moe_grouped_gemm_swiglu",
             "moe_grouped_gemm_down", "moe_unpermute_reduce", "moe_forward", "moe_get_device_error",
             "moe_status_string", "moe_get_plan", "moe_get_plan_for_sms", "moe_align_permute_noalloc",
-            "moe_dynamic_scales", "moe_launch_count", "moe_set_tuning")
+            "moe_dynamic_scales", "moe_launch_count", "moe_set_tuning", "moe_repack_int4")
 
 
 class MoEError(RuntimeError):
@@ -105,6 +105,7 @@ def load(path: str = LIB_PATH):
         "moe_dynamic_scales": (vp, [vp]),
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_set_tuning": (st, [ctypes.POINTER(Tuning)]),
+        "moe_repack_int4": (st, [vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -231,6 +232,21 @@ def get_device_error(ws, stream=None) -> int:
 def launch_count() -> int:
     """Kernel launches the library has issued in this process (graph captures once)."""
     return int(load().moe_launch_count())
+
+
+def repack_int4(codes, out=None, stream=None):
+    """int4 codes (uint8 tensor, packed order) -> a tensor of the same shape in the
+    paired order of MOE_W_INT4_G128_PAIRED (moe_repack_int4); `out` may be
+    `codes` itself (in place).  Returns the output tensor."""
+    import torch
+    if out is None:
+        out = torch.empty_like(codes)
+    if out.numel() != codes.numel() or codes.dtype != torch.uint8 or out.dtype != torch.uint8:
+        raise ValueError("repack_int4: uint8 tensors of equal size")
+    if not (codes.is_contiguous() and out.is_contiguous()):
+        raise ValueError("repack_int4: contiguous tensors")
+    _check(load().moe_repack_int4(_ptr(codes), _ptr(out), codes.numel(), _stream(stream)), "moe_repack_int4")
+    return out
 
 
 def dynamic_scales(ws):

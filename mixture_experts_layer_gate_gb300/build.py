@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["gemm.cu", "api.cu", "gate.cu", "align.cu", "route.cu", "reduce.cu", "noalloc.cu", "scale.cu"]
+SOURCES = ["gemm.cu", "api.cu", "gate.cu", "align.cu", "route.cu", "reduce.cu", "noalloc.cu", "scale.cu",
+           "repack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

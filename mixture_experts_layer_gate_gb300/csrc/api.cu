@@ -61,9 +61,10 @@ moe_status_t moe::validate_problem(const moe_problem_t* p) {
     return MOE_ERR_INVALID_ARG;
   }
   if (p->wdtype != MOE_W_BF16 && p->wdtype != MOE_W_FP8_E4M3 && p->wdtype != MOE_W_INT4_G128 &&
-      p->wdtype != MOE_W_INT8_G128)
+      p->wdtype != MOE_W_INT8_G128 && p->wdtype != MOE_W_INT4_G128_PAIRED)
     return MOE_ERR_INVALID_ARG;
-  if ((p->wdtype == MOE_W_INT4_G128 || p->wdtype == MOE_W_INT8_G128) && p->group_size != 128)
+  if ((p->wdtype == MOE_W_INT4_G128 || p->wdtype == MOE_W_INT4_G128_PAIRED || p->wdtype == MOE_W_INT8_G128) &&
+      p->group_size != 128)
     return MOE_ERR_UNSUPPORTED;
   if (p->act_scale != MOE_ACT_SCALE_STATIC && p->act_scale != MOE_ACT_SCALE_DYNAMIC) return MOE_ERR_INVALID_ARG;
   if (p->act_scale == MOE_ACT_SCALE_DYNAMIC && p->wdtype != MOE_W_FP8_E4M3) return MOE_ERR_INVALID_ARG;
@@ -152,6 +153,7 @@ int wkind_of(const moe_problem_t& p) {
   switch (p.wdtype) {
     case MOE_W_FP8_E4M3: return kW_FP8;
     case MOE_W_INT4_G128: return kW_INT4;
+    case MOE_W_INT4_G128_PAIRED: return kW_INT4;
     case MOE_W_INT8_G128: return kW_INT8;
     default: return kW_BF16;
   }
@@ -174,7 +176,7 @@ int plan_bn_max(const moe_problem_t& p) {
   const long long m_avg = (S + touched - 1) / touched;
   long long bn = std::max(3 * m_avg, m_avg + 24);
   long long cap = 256;
-  if (p.wdtype == MOE_W_INT4_G128) cap = m_avg >= 128 ? 192 : 128;
+  if (wkind_of(p) == kW_INT4) cap = m_avg >= 128 ? 192 : 128;
   if (p.wdtype == MOE_W_INT8_G128) cap = m_avg >= 192 ? 256 : 128;
   bn = std::min<long long>(cap, std::max<long long>(16, bn));
   return roundup16(static_cast<int>(bn));
@@ -196,7 +198,7 @@ long long plan_tiles(const moe_problem_t& p, bool up, int bn_max) {
 int plan_splits(const moe_problem_t& p, bool up, int bn_max, int KB, int sms) {
   const long long tiles = plan_tiles(p, up, bn_max);
   if (tiles >= 4ll * sms) return 1;
-  const double min_eff = (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) ? 0.8 : 0.9;
+  const double min_eff = converts(wkind_of(p)) ? 0.8 : 0.9;
   const int pmax = std::max(1, std::min(kMaxSplits, KB / 4));
   int best = 1;
   double best_eff = 0.0;
@@ -577,6 +579,7 @@ moe_status_t run_gemm(const moe_problem_t& p, const moe_weights_t& wt, bool up, 
   gp.amax = (dyn && up) ? &ds->amax[1] : nullptr;
   gp.w4_scale = up ? wt.w13_scale : wt.w2_scale;
   gp.w4_zero = static_cast<const uint8_t*>(up ? wt.w13_zero : wt.w2_zero);
+  gp.w4_paired = p.wdtype == MOE_W_INT4_G128_PAIRED ? 1 : 0;
   gp.E = p.E;
   gp.S = S;
   gp.I = p.I;
@@ -656,7 +659,7 @@ moe_status_t check_weights(const moe_problem_t& p, const moe_weights_t* w) {
     const bool given = w->a1_scale && w->a2_scale, none = !w->a1_scale && !w->a2_scale;
     if (dynamic_scales(p) ? !none : !given) return MOE_ERR_INVALID_ARG;
   }
-  if (p.wdtype == MOE_W_INT4_G128 || p.wdtype == MOE_W_INT8_G128) {
+  if (converts(wkind_of(p))) {
     if (!w->w13_scale || !w->w2_scale || !aligned(w->w13_scale, 2) || !aligned(w->w2_scale, 2))
       return MOE_ERR_INVALID_ARG;
     if ((w->w13_zero == nullptr) != (w->w2_zero == nullptr)) return MOE_ERR_INVALID_ARG;
@@ -828,6 +831,16 @@ moe_status_t moe_forward(const moe_problem_t* p, const moe_weights_t* w, const v
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_repack_int4(const void* codes, void* out, size_t n_bytes, moe_stream_t stream) {
+  if (n_bytes == 0) return MOE_OK;
+  if (codes == nullptr || out == nullptr || n_bytes % 4 != 0 || reinterpret_cast<uintptr_t>(codes) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(out) % 4 != 0)
+    return MOE_ERR_INVALID_ARG;
+  const cudaError_t e = launch_repack_int4(static_cast<const uint32_t*>(codes), static_cast<uint32_t*>(out),
+                                           n_bytes / 4, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 float* moe_dynamic_scales(void* ws) {
   if (ws == nullptr || !aligned(ws, 256)) return nullptr;

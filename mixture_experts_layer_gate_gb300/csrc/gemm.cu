@@ -235,6 +235,27 @@ __device__ __forceinline__ uint4 dequant8(uint32_t x, uint32_t flip, __nv_bfloat
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same for 8 codes in the paired order of moe_repack_int4 (nibbles of the
+// low 16 bits: k0, k2, k4, k6; of the high 16 bits: k1, k3, k5, k7): a shift of
+// the word by 4 i puts k 2i and 2i + 1 at the bottom of the two halves, so one
+// masked XOR per pair forms 128 + q with no byte permute: 7 integer operations
+// per 8 codes instead of 9, the bf16x2 subtract and scale unchanged.
+__device__ __forceinline__ uint4 dequant8_paired(uint32_t x, uint32_t flip, __nv_bfloat162 off,
+                                                 __nv_bfloat162 s2) {
+  uint32_t o[4];
+  o[0] = (x & 0x000F000Fu) ^ flip;          // k0, k1
+  o[1] = ((x >> 4) & 0x000F000Fu) ^ flip;   // k2, k3
+  o[2] = ((x >> 8) & 0x000F000Fu) ^ flip;   // k4, k5
+  o[3] = ((x >> 12) & 0x000F000Fu) ^ flip;  // k6, k7
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&o[i]);
+    v = __hmul2(__hsub2(v, off), s2);
+    o[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // 4 unsigned 8-bit codes (byte i = k i) -> 4 bf16 (code - zero) * scale in k
 // order.  A byte permute writes code q into the low byte of the float
 // 2^23 (bit pattern 0x4B000000), giving exactly 2^23 + q; subtracting
@@ -1165,6 +1186,7 @@ __global__ void __launch_bounds__(64 + 32 * EW + 128 * CG + (DUAL ? 32 : 0), 1)
     // with zero point 8 (int4) or 128 (int8)
     const uint8_t* zeros = p.w4_zero;
     const uint32_t flip = zeros ? 0x43004300u : 0x43084308u;  // int4 (see dequant8)
+    const bool paired = BITS == 4 && p.w4_paired != 0;       // int4 codes in the paired order
     const uint32_t flip8 = zeros ? 0u : 0x80808080u;           // int8
     const float zdef = BITS == 8 ? 128.0f : 8.0f;
     const uint32_t tlane = static_cast<uint32_t>(q * 32) << 16;
@@ -1239,13 +1261,24 @@ __global__ void __launch_bounds__(64 + 32 * EW + 128 * CG + (DUAL ? 32 : 0), 1)
             const uint4 r0 = *reinterpret_cast<const uint4*>(rrow + (((2 * j) ^ (m & 7)) << 4));
             const uint4 r1 = *reinterpret_cast<const uint4*>(rrow + (((2 * j + 1) ^ (m & 7)) << 4));
             const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            if (paired) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint4 o = dequant8(w[i], flip, off, s2);
-              outv[4 * i + 0] = o.x;
-              outv[4 * i + 1] = o.y;
-              outv[4 * i + 2] = o.z;
-              outv[4 * i + 3] = o.w;
+              for (int i = 0; i < 8; ++i) {
+                const uint4 o = dequant8_paired(w[i], flip, off, s2);
+                outv[4 * i + 0] = o.x;
+                outv[4 * i + 1] = o.y;
+                outv[4 * i + 2] = o.z;
+                outv[4 * i + 3] = o.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint4 o = dequant8(w[i], flip, off, s2);
+                outv[4 * i + 0] = o.x;
+                outv[4 * i + 1] = o.y;
+                outv[4 * i + 2] = o.z;
+                outv[4 * i + 3] = o.w;
+              }
             }
           } else {
             // 64 bytes of codes = chunks 4 (j & 1) .. + 3 of box j / 2

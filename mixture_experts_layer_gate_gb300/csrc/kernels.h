@@ -118,6 +118,7 @@ struct GemmParams {
   uint32_t* amax;          // dynamic fp8 gate_up: running max of the stored |bf16 act| bits, or null
   const void* w4_scale;    // int4 / int8: half [E, R, G]
   const uint8_t* w4_zero;  // int4 / int8: uint8 [E, R, G] zero points (unsigned codes), or null (signed)
+  int w4_paired;           // int4: codes in the paired order of moe_repack_int4 (else the packed order)
   int64_t out_ld;          // elements per output row
   int64_t part_stride;     // elements between split-K slices
   int E, S, I;
@@ -163,5 +164,9 @@ int gemm_threads(int wkind, int conv_groups, int dual, int epi_warps);
 bool gemm_epi8_supported(int wkind, int conv_groups, int pair, int slot_kb);
 cudaError_t launch_grouped_gemm(int wkind, const GemmMaps& maps, const GemmParams& p, int grid,
                                 size_t smem, cudaStream_t s);
+
+// int4 codes from the packed order (low nibble = even K index) to the paired
+// order (per 4-byte word: even K indices in the low 16 bits, odd in the high).
+cudaError_t launch_repack_int4(const uint32_t* in, uint32_t* out, size_t n_words, cudaStream_t s);
 
 }  // namespace moe

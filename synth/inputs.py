@@ -51,6 +51,8 @@ class MoEShape:
     weight_sd: float = 0.02
     zero_point: bool = False  # int4 / int8: unsigned codes with per-group zero points
     act_scale: str = "static"  # fp8: "static" scales from the generator, or "dynamic" (computed per batch)
+    int4_order: str = "packed"  # int4: weights are generated packed; "paired": the library gets a copy
+                                # prepared by moe_repack_int4 (format MOE_W_INT4_G128_PAIRED)
 
 
 SHAPES = {
@@ -72,6 +74,10 @@ SHAPES = {
 # DeepSeek-V3 with asymmetric AWQ-style int4 (unsigned codes, per-group zero
 # points), the format of the DeepSeek-V3-AWQ checkpoints the pages benchmark.
 SHAPES["dsv3_awq"] = dataclasses.replace(SHAPES["dsv3"], name="dsv3_awq", zero_point=True)
+# The same int4 weights prepared once by moe_repack_int4 (codes paired for the
+# converters), symmetric and with zero points.
+SHAPES["dsv3_paired"] = dataclasses.replace(SHAPES["dsv3"], name="dsv3_paired", int4_order="paired")
+SHAPES["dsv3_awq_paired"] = dataclasses.replace(SHAPES["dsv3_awq"], name="dsv3_awq_paired", int4_order="paired")
 # Mixtral-8x7B with 8-bit group-128 GPTQ-style weights (W8A16, symmetric).
 SHAPES["mixtral_w8"] = dataclasses.replace(SHAPES["mixtral"], name="mixtral_w8", wdtype="int8")
 # Qwen2-57B-A14B fp8 W8A8 with dynamic per-tensor activation scales.
@@ -80,7 +86,7 @@ SHAPES["qwen2_dyn"] = dataclasses.replace(SHAPES["qwen2"], name="qwen2_dyn", act
 # Tensor-parallel slices of the same layers as the pages run them (the expert
 # intermediate size split over the TP ranks; one rank's share on one GPU):
 # Mixtral-8x7B TP2, Qwen2-57B-A14B TP4, DeepSeek-V3 TP8, Llama-4-Scout TP8.
-for _base, _tp in (("mixtral", 2), ("qwen2", 4), ("dsv3", 8), ("scout", 8)):
+for _base, _tp in (("mixtral", 2), ("qwen2", 4), ("dsv3", 8), ("scout", 8), ("dsv3_paired", 8)):
     _s = SHAPES[_base]
     SHAPES[f"{_base}_tp{_tp}"] = dataclasses.replace(_s, name=f"{_base}_tp{_tp}", I=_s.I // _tp)
 del _base, _tp, _s

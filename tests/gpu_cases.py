@@ -15,15 +15,25 @@ from oracle.torch_io import np_of, oracle_inputs
 TOL = {"bf16": 1e-2, "fp8": 3e-2, "int4": 4e-2, "int8": 2e-2}
 
 
+def lib_wdtype(shape):
+    # int4 weights the library receives prepared by moe_repack_int4
+    return "int4_paired" if shape.int4_order == "paired" else shape.wdtype
+
+
 def lib_problem(shape, T):
     return moe.problem(T, shape.H, shape.I, shape.E, shape.top_k, scoring=shape.scoring,
                        renormalize=shape.renormalize, n_group=shape.n_group, topk_group=shape.topk_group,
-                       routed_scaling_factor=shape.routed_scaling_factor, wdtype=shape.wdtype,
+                       routed_scaling_factor=shape.routed_scaling_factor, wdtype=lib_wdtype(shape),
                        group_size=shape.group_size, act_scale=shape.act_scale)
 
 
-def lib_weights(w, tok):
-    return moe.Weights(w.w13, w.w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
+def lib_weights(w, tok, shape=None):
+    # the oracle reads the generated (packed) codes; the library a repacked copy
+    # where the shape asks for the paired format
+    w13, w2 = w.w13, w.w2
+    if shape is not None and shape.int4_order == "paired":
+        w13, w2 = moe.repack_int4(w.w13), moe.repack_int4(w.w2)
+    return moe.Weights(w13, w2, w.w13_scale, w.w2_scale, tok.a1_scale, tok.a2_scale,
                        w.w13_zero, w.w2_zero)
 
 
@@ -45,7 +55,7 @@ class StageOut:
 
 def run_stages(shape, T, weights, tok, device) -> StageOut:
     p = lib_problem(shape, T)
-    wts = lib_weights(weights, tok)
+    wts = lib_weights(weights, tok, shape)
     k, S, H, I, E = shape.top_k, T * shape.top_k, shape.H, shape.I, shape.E
     adt = torch.uint8 if shape.wdtype == "fp8" else torch.bfloat16
     ids = torch.full((T, k), -1, dtype=torch.int32, device=device)

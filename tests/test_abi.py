@@ -286,3 +286,23 @@ def test_epilogue_warp_override(lib):
         assert moe.get_plan(bf, num_sms=152).epi_warps_up == 4
     pl = moe.get_plan(bf, num_sms=152)
     assert pl.epi_warps_up == 8 and pl.stages_up >= 6  # the second staging half leaves the ring depth
+
+
+def test_repack_int4_rejects_bad_arguments(lib):
+    # refused before any device work: sizes that are not whole 4-byte words,
+    # misaligned or null pointers; an empty tensor is a no-op
+    vp = ctypes.c_void_p
+    assert lib.moe_repack_int4(vp(256), vp(512), 6, None) == 1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(vp(258), vp(512), 8, None) == 1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(vp(256), vp(514), 8, None) == 1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(None, vp(512), 8, None) == 1  # MOE_ERR_INVALID_ARG
+    assert lib.moe_repack_int4(vp(256), vp(512), 0, None) == binding.MOE_OK
+
+
+def test_paired_int4_plans_match_packed_int4(lib):
+    # the paired code order changes only the converters' instructions
+    for T in (1, 37, 512, 4096):
+        a = moe.problem(T, 7168, 2048, 256, 8, scoring="sigmoid", n_group=8, topk_group=4, wdtype="int4")
+        b = moe.problem(T, 7168, 2048, 256, 8, scoring="sigmoid", n_group=8, topk_group=4, wdtype="int4_paired")
+        assert bytes(moe.get_plan(a, num_sms=152)) == bytes(moe.get_plan(b, num_sms=152))
+    assert moe.scratch_size(b) == moe.scratch_size(a) > 0

@@ -37,7 +37,7 @@ def small(name):
         return shrink(base, H=512, I=1024)
     if name in ("qwen2", "qwen2_dyn"):
         return shrink(base, H=384, I=256, E=16)
-    if name in ("dsv3", "dsv3_awq"):
+    if name in ("dsv3", "dsv3_awq", "dsv3_paired", "dsv3_awq_paired"):
         return dataclasses.replace(shrink(base, H=1024, I=256, E=64), n_group=8, topk_group=4)
     if name == "scout":
         return shrink(base, H=512, I=512)
@@ -99,7 +99,7 @@ def test_cuda_graph_capture_matches_eager(dev, name):
     w = make_weights(shape, dev, 0)
     tok = make_tokens(shape, T, dev, 0)
     p = gc.lib_problem(shape, T)
-    wts = gc.lib_weights(w, tok)
+    wts = gc.lib_weights(w, tok, shape)
     ws = moe.alloc_workspace(p, dev)
     out_e = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
     moe.forward(p, wts, tok.x, tok.logits, tok.bias, out_e, ws)
@@ -203,7 +203,9 @@ FULL_CASES = [("mixtral", 1), ("mixtral", 33), ("mixtral", 4096), ("qwen2", 1), 
               # few weight blocks per expert
               ("mixtral_tp2", 7), ("mixtral_tp2", 512), ("qwen2_tp4", 1), ("qwen2_tp4", 512),
               ("dsv3_tp8", 1), ("dsv3_tp8", 32), ("dsv3_tp8", 512), ("dsv3_tp8", 2048), ("scout_tp8", 32),
-              ("scout_tp8", 4096)]
+              ("scout_tp8", 4096),
+              # int4 codes prepared by moe_repack_int4
+              ("dsv3_paired", 2), ("dsv3_paired", 700), ("dsv3_awq_paired", 33), ("dsv3_paired_tp8", 256)]
 
 
 def test_dynamic_scales_full_size_multi_tile_exact(dev):
@@ -380,7 +382,7 @@ def test_launch_count_of_forward(dev, name, T):
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty((T, shape.H), dtype=torch.bfloat16, device=dev)
     n0 = moe.launch_count()
-    moe.forward(p, gc.lib_weights(w, tok), tok.x, tok.logits, tok.bias, out, ws)
+    moe.forward(p, gc.lib_weights(w, tok, shape), tok.x, tok.logits, tok.bias, out, ws)
     torch.cuda.synchronize()
     small_path = T * shape.top_k <= 1024
     expect = (1 if small_path else 4)             # route with its gather | gate + count + scatter + gather
@@ -402,3 +404,46 @@ def test_limit_token_count(dev):
     # the largest T (65535): 131070 slots through the multi-CTA counting sort
     shape = dataclasses.replace(SHAPES["tiny"], name="max_tokens", H=128, I=128)
     gc.full_check(shape, 65535, dev)
+
+
+def _paired_reference(codes: np.ndarray) -> np.ndarray:
+    """The paired code order written out from its definition (include/moe.h):
+    per 4-byte word, K indices k0..k7 (k at nibble k of the packed word) go to
+    nibbles 0..3 (even k) and 4..7 (odd k) in increasing k."""
+    words = codes.view(np.uint32)
+    out = np.zeros_like(words)
+    for k in range(8):
+        nib = (words >> np.uint32(4 * k)) & np.uint32(0xF)
+        pos = k // 2 if k % 2 == 0 else 4 + k // 2
+        out |= nib << np.uint32(4 * pos)
+    return out.view(np.uint8)
+
+
+@pytest.mark.parametrize("n_bytes,offset", [(4, 0), (1 << 20, 0), (4 * 1001, 0), (4 * 4097, 4), (64 * 3 + 8, 12)])
+def test_repack_int4_is_the_paired_permutation(dev, n_bytes, offset):
+    # bit for bit against the definition, on the vector path (16-byte aligned)
+    # and the word path (4-byte aligned sizes and offsets), out of place and in place
+    gen = torch.Generator(device="cpu").manual_seed(n_bytes)
+    host = torch.randint(0, 256, (n_bytes + 16,), dtype=torch.uint8, generator=gen)
+    src = host.to(dev)[offset: offset + n_bytes]
+    want = _paired_reference(host[offset: offset + n_bytes].numpy().copy())
+    out = moe.repack_int4(src)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), want)
+    inplace = src.clone()
+    moe.repack_int4(inplace, inplace)
+    torch.cuda.synchronize()
+    assert np.array_equal(inplace.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name", ["dsv3_paired", "dsv3_awq_paired"])
+@pytest.mark.parametrize("knobs", [{}, {"pair": 1, "dual": 0}, {"bn_max": 192, "pair": 1}, {"pair": 0, "dual": 1,
+                                                                                          "bn_max": 64}])
+def test_paired_int4_codes(dev, name, knobs):
+    # weights prepared by moe_repack_int4 against the oracle on the packed codes:
+    # decode tiles (three converter groups), CTA pairs with one and two issuers,
+    # wide tiles, symmetric and with zero points
+    shape = small(name)
+    with moe.tuning(**knobs):
+        for T in (5, 37, 300):
+            gc.full_check(shape, T, dev)
