@@ -797,7 +797,7 @@ def main():
                     help="planner overrides as JSON (moe_set_tuning), e.g. '{\"full_box\": 1}'; for experiments")
     ap.add_argument("--sweep-configs", default=None,
                     help="comma-separated further workloads to sweep in the same run (default with the "
-                         "Mixtral headline: qwen2,dsv3,scout,qwen2_tp4,dsv3_tp8,tiny; else none)")
+                         "Mixtral headline: qwen2,dsv3,dsv3_paired,scout,qwen2_tp4,dsv3_tp8,tiny; else none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=4096)
     ap.add_argument("--ref-sample", type=int, default=16)
@@ -807,7 +807,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.sweep_configs is None:
-        args.sweep_configs = "qwen2,dsv3,scout,qwen2_tp4,dsv3_tp8,tiny" if args.config == CONFIG_NAME else ""
+        args.sweep_configs = "qwen2,dsv3,dsv3_paired,scout,qwen2_tp4,dsv3_tp8,tiny" if args.config == CONFIG_NAME else ""
     args.sweep_configs = [c for c in args.sweep_configs.split(",") if c]
     if args.measure_tensor_peaks:
         measure_tensor_peaks()
