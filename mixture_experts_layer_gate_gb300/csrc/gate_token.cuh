@@ -24,7 +24,7 @@ constexpr int kMaxTopK = 32;
 struct Cand {
   float key;
   int idx;
-  float val;  // softmax: logit; sigmoid: sigmoid score (the weight before scaling)
+  float val;  // softmax: exp(logit - max); sigmoid: sigmoid score (the weight before scaling)
 };
 
 __device__ __forceinline__ bool better(float k1, int i1, float k2, int i2) {
@@ -72,12 +72,15 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
   }
   float zsum = 0.f;
   if (!a.sigmoid) {
+    // rank on the logits; carry exp(logit - max), the softmax numerator, as the value
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       key[i] = val[i];
-      if (!((taken >> i) & 1u)) zsum += expf(val[i] - lmax);
+      const float ev = ((taken >> i) & 1u) ? 0.f : expf(val[i] - lmax);
+      zsum += ev;
+      val[i] = ev;
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) zsum += __shfl_xor_sync(0xffffffffu, zsum, off);
@@ -136,9 +139,11 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
     }
   }
 
-  // k rounds of warp arg-max; the winner's owner lane retires it.
-  int sel_idx[kMaxTopK];
-  float sel_val[kMaxTopK];
+  // k rounds of warp arg-max; the winner's owner lane retires it and lane j
+  // keeps the j-th selection.
+  const float inv_z = a.sigmoid ? 1.0f : 1.0f / zsum;
+  int my_idx = 0;
+  float my_val = 0.f;
   float total = 0.f;
 #pragma unroll 1
   for (int j = 0; j < a.k; ++j) {
@@ -156,24 +161,20 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
     }
     c = warp_best(c);
     if ((c.idx & 31) == lane) taken |= 1u << (c.idx >> 5);
-    const float wv = a.sigmoid ? c.val : expf(c.val - lmax) / zsum;
-    if (lane == 0) {
-      sel_idx[j] = c.idx;
-      sel_val[j] = wv;
+    const float wv = c.val * inv_z;  // softmax: exp / sum; sigmoid: the score
+    if (lane == j) {
+      my_idx = c.idx;
+      my_val = wv;
     }
     total += wv;
   }
-  if (lane == 0) {
-    int32_t* ids = a.ids + static_cast<size_t>(t) * a.k;
-    float* w = a.w + static_cast<size_t>(t) * a.k;
+  if (lane < a.k) {
     // selected scores that are all zero (every selected logit NaN) give zero
     // weights instead of 0 / 0
     const float inv = a.renormalize ? (total > 0.f ? 1.0f / total : 0.f) : 1.0f;
-#pragma unroll 1
-    for (int j = 0; j < a.k; ++j) {
-      ids[j] = sel_idx[j];
-      w[j] = a.renormalize ? (sel_val[j] * inv) * a.scale : sel_val[j] * a.scale;
-    }
+    const size_t o = static_cast<size_t>(t) * a.k + lane;
+    a.ids[o] = my_idx;
+    a.w[o] = a.renormalize ? (my_val * inv) * a.scale : my_val * a.scale;
   }
 }
 
