@@ -291,8 +291,9 @@ uint64_t moe_launch_count(void);
  * n_bytes of int4 codes in the packed order (two codes per byte, the low
  * nibble holding the even K index: w13 or w2 of MOE_W_INT4_G128) into the
  * order of MOE_W_INT4_G128_PAIRED, a permutation inside every 4-byte word.
- * codes and out are device pointers, 4-byte aligned, and may be equal (in
- * place); n_bytes is a multiple of 4 (any int4 w13 / w2 tensor is).  Scales
+ * codes and out are device pointers, 4-byte aligned, either equal (in place)
+ * or not overlapping at all (a partial overlap races); n_bytes is a multiple
+ * of 4 (any int4 w13 / w2 tensor is).  Scales
  * and zero points are not touched.  Asynchronous on `stream`.  Returns
  * MOE_ERR_INVALID_ARG for a null or misaligned pointer or a size that is not
  * a multiple of 4, MOE_OK for n_bytes == 0. */

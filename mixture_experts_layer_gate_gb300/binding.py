@@ -237,7 +237,8 @@ def launch_count() -> int:
 def repack_int4(codes, out=None, stream=None):
     """int4 codes (uint8 tensor, packed order) -> a tensor of the same shape in the
     paired order of MOE_W_INT4_G128_PAIRED (moe_repack_int4); `out` may be
-    `codes` itself (in place).  Returns the output tensor."""
+    `codes` itself (in place) but must not partly overlap it.  Returns the output
+    tensor."""
     import torch
     if out is None:
         out = torch.empty_like(codes)
