@@ -99,20 +99,28 @@ __device__ __forceinline__ void gate_token(const GateArgs& a, int t, int lane, f
   }
 
   if (a.n_group > 0) {
-    // Group scores: sum of the two largest keys of each contiguous group.
+    // Group scores: sum of the two largest keys of each contiguous group.  The
+    // keys are stored transposed (member j of group g at j * n_group + g), so
+    // the lanes that score the groups read consecutive words, free of bank
+    // conflicts, in the same member order.
     const int gs = a.E / a.n_group;
+    const bool pow2 = (gs & (gs - 1)) == 0;
+    const int gshift = __ffs(gs) - 1;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = lane + 32 * i;
-      if (e < a.E) skeys[e] = key[i];
+      if (e < a.E) {
+        const int g = pow2 ? (e >> gshift) : e / gs;
+        skeys[(e - g * gs) * a.n_group + g] = key[i];
+      }
     }
     __syncwarp();
     float gscore = -INFINITY;
     if (lane < a.n_group) {
       float m1 = -INFINITY, m2 = -INFINITY;
-      const float* g = &skeys[lane * gs];
+      const float* g = &skeys[lane];
       for (int j = 0; j < gs; ++j) {
-        const float v = g[j];
+        const float v = g[j * a.n_group];
         if (v > m1) {
           m2 = m1;
           m1 = v;
